@@ -1,0 +1,256 @@
+"""Pins for the oracle's attention functions (no GPU): closed forms, invariants
+and special cases that reduce to textbook results."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import to_bf16_bits, bf16_bits_to_f32
+
+
+def bf(x):
+    return to_bf16_bits(np.asarray(x, np.float32))
+
+
+def rnd(shape, seed, scale=1.0, integer=False):
+    rng = np.random.default_rng(seed)
+    if integer:
+        return bf(rng.integers(-3, 4, shape).astype(np.float32))
+    return bf(rng.standard_normal(shape).astype(np.float32) * scale)
+
+
+def allrows(B, H, S):
+    return np.arange(B * H * S, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------- exact attention
+def test_exact_zero_query_gives_visible_mean():
+    B, H, S, D = 1, 2, 40, 64
+    q = bf(np.zeros((B, H, S, D)))
+    k = rnd((B, H, S, D), 1)
+    v = rnd((B, H, S, D), 2)
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    for causal in (False, True):
+        out = oracle.attn_exact(q, k, v, causal, 0.125, allrows(B, H, S))
+        for h in range(H):
+            for i in range(S):
+                n = i + 1 if causal else S
+                ref = vf[0, h, :n].mean(axis=0)
+                assert np.allclose(out[h * S + i], ref, rtol=0, atol=1e-12)
+
+
+def test_exact_two_keys_logistic():
+    rng = np.random.default_rng(7)
+    q = rnd((1, 1, 1, 64), 3)
+    k = rnd((1, 1, 2, 64), 4)
+    v = rnd((1, 1, 2, 64), 5)
+    qf, kf, vf = (bf16_bits_to_f32(a).astype(np.float64) for a in (q, k, v))
+    s = 0.125 * (kf[0, 0] @ qf[0, 0, 0])
+    w0 = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+    out = oracle.attn_exact(q, k, v, False, 0.125, [0])[0]
+    assert np.allclose(out, w0 * vf[0, 0, 0] + (1 - w0) * vf[0, 0, 1], atol=1e-13)
+
+
+def test_exact_causal_row0_and_constant_v_and_shift_invariance():
+    B, H, S, D = 1, 1, 33, 64
+    q, k, v = rnd((B, H, S, D), 1, integer=True), rnd((B, H, S, D), 2, integer=True), rnd((B, H, S, D), 3)
+    out = oracle.attn_exact(q, k, v, True, 0.125, allrows(B, H, S))
+    assert np.array_equal(out[0], bf16_bits_to_f32(v)[0, 0, 0].astype(np.float64))
+    ones = bf(np.ones((B, H, S, D)))
+    assert np.allclose(oracle.attn_exact(q, k, ones, False, 0.125, allrows(B, H, S)), 1.0, atol=1e-14)
+    # adding the same vector u to every key shifts a row's scores by q.u: softmax unchanged
+    u = np.random.default_rng(9).integers(-2, 3, D).astype(np.float32)
+    k2 = bf(bf16_bits_to_f32(k) + u)
+    out2 = oracle.attn_exact(q, k2, v, True, 0.125, allrows(B, H, S))
+    assert np.allclose(out, out2, atol=1e-12)
+
+
+def test_exact_gqa_mapping():
+    B, H, Hkv, S, D = 2, 4, 2, 20, 64
+    q, k, v = rnd((B, H, S, D), 1), rnd((B, Hkv, S, D), 2), rnd((B, Hkv, S, D), 3)
+    rows = allrows(B, H, S)
+    out = oracle.attn_exact(q, k, v, False, 0.125, rows)
+    k4, v4 = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    assert np.array_equal(out, oracle.attn_exact(q, k4, v4, False, 0.125, rows))
+
+
+def test_exact_causal_rectangular_offset():
+    # Sq < Sk: query i sees keys j <= i + Sk - Sq (bottom-right aligned)
+    q, k, v = rnd((1, 1, 4, 64), 1), rnd((1, 1, 10, 64), 2), rnd((1, 1, 10, 64), 3)
+    full = oracle.attn_exact(q, k[:, :, :7], v[:, :, :7], False, 0.125, [0])
+    causal = oracle.attn_exact(q, k, v, True, 0.125, [0])
+    assert np.allclose(full, causal, atol=1e-14)
+
+
+# --------------------------------------------------------------------------- error floor
+def test_floor_unquantised_p_equals_exact_on_representable_inputs():
+    # integer inputs in [-3, 3] are exact in every MX format used here
+    B, H, S, D = 1, 1, 70, 64
+    q, k, v = (rnd((B, H, S, D), s, integer=True) for s in (1, 2, 3))
+    for fq, fv in [(0, 0), (1, 1), (2, 2)]:
+        mx = oracle.MxInputs.from_bf16(q, k, v, fq, fv)
+        rows = allrows(B, H, S)
+        fl = oracle.attn_floor(mx, S, True, 0.125, fv, rows, quantize_p=False)
+        ex = oracle.attn_exact(q, k, v, True, 0.125, rows)
+        assert np.allclose(fl, ex, atol=1e-12)
+
+
+def test_floor_uniform_rows_and_error_order():
+    B, H, S, D = 1, 1, 100, 64
+    q0 = bf(np.zeros((B, H, S, D)))
+    k, v = rnd((B, H, S, D), 2), rnd((B, H, S, D), 3)
+    mx = oracle.MxInputs.from_bf16(q0, k, v, 0, 0)
+    vh = oracle.decode_array(0, mx.vc) * 2.0 ** (np.repeat(mx.vs.astype(np.int64), 32, -1) - 127)
+    out = oracle.attn_floor(mx, S, False, 0.125, 0, [0])
+    assert np.allclose(out[0], vh[0, 0, :, :S].mean(axis=1), atol=1e-12)
+    # quantising P adds error of the order of the P format's precision
+    q = rnd((B, H, S, D), 1, 2.0)
+    mx = oracle.MxInputs.from_bf16(q, k, v, 0, 0)
+    rows = allrows(B, H, S)
+    a = oracle.attn_floor(mx, S, False, 0.125, 0, rows, quantize_p=False)
+    errs = []
+    for fp, bound in [(0, 0.04), (1, 0.09), (2, 0.3)]:
+        b = oracle.attn_floor(mx, S, False, 0.125, fp, rows, quantize_p=True)
+        rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+        assert 0 < rel < bound, (fp, rel)
+        errs.append(rel)
+    assert errs[0] < errs[1] < errs[2]        # 3, 3 and 1 mantissa bits, narrower range for E2M3
+
+
+# --------------------------------------------------------------------------- exp2 approximation
+def test_exp2_poly_exact_at_integers_and_error_bound():
+    for n in range(-60, 10):
+        assert oracle.exp2_poly(float(n)) == 2.0 ** n
+    assert oracle.exp2_poly(-1000.0) == 2.0 ** -64           # clamp
+    assert oracle.exp2_poly(float("-inf")) == 2.0 ** -64
+    r = np.linspace(-20, 9.999, 20001, dtype=np.float32)
+    p = np.array([oracle.exp2_poly(float(x)) for x in r])
+    rel = np.abs(p / np.exp2(r.astype(np.float64)) - 1)
+    assert rel.max() < 1.6e-4
+    # interpolation nodes 1/3, 2/3 are met to fp32 rounding
+    for f in (1 / 3, 2 / 3):
+        assert abs(oracle.exp2_poly(float(np.float32(f))) / 2 ** float(np.float32(f)) - 1) < 1e-6
+
+
+# --------------------------------------------------------------------------- emulation
+FMTS = [(0, 0, 0), (1, 1, 1), (2, 2, 2), (2, 2, 3)]      # (fmt_qk, fmt_v, fmt_p)
+
+
+@pytest.mark.parametrize("fq,fv,fp", FMTS)
+@pytest.mark.parametrize("mufu", [0, 0x55555555])
+def test_emulate_zero_query_and_causal_row0(fq, fv, fp, mufu):
+    B, H, S, D = 1, 1, 300, 128
+    q0 = bf(np.zeros((B, H, S, D)))
+    k, v = rnd((B, H, S, D), 2), rnd((B, H, S, D), 3)
+    mx = oracle.MxInputs.from_bf16(q0, k, v, fq, fv)
+    vh = oracle.decode_array(fv, mx.vc) * 2.0 ** (np.repeat(mx.vs.astype(np.int64), 32, -1) - 127)
+    res = oracle.fsa_emulate(mx, S, True, 1 / math.sqrt(D), fp, allrows(B, H, S), mufu_mask=mufu)
+    for i in (0, 1, 127, 128, 299):
+        assert np.allclose(res["out"][i], vh[0, 0, :, :i + 1].mean(axis=1), atol=1e-12)
+    assert not res["fallbacks"].any()
+    assert np.array_equal(res["tiles"], np.arange(S) // 128 + 1)
+
+
+@pytest.mark.parametrize("fq,fv,fp", FMTS)
+def test_emulate_constant_v_is_one(fq, fv, fp):
+    B, H, S, D = 1, 2, 257, 64
+    q, k = rnd((B, H, S, D), 1), rnd((B, H, S, D), 2)
+    ones = bf(np.ones((B, H, S, D)))
+    mx = oracle.MxInputs.from_bf16(q, k, ones, fq, fv)
+    res = oracle.fsa_emulate(mx, S, False, 0.125, fp, allrows(B, H, S))
+    assert np.allclose(res["out"], 1.0, atol=1e-13)
+
+
+def test_emulate_planted_score_fires_one_fallback():
+    B, H, S, D = 1, 1, 384, 64
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((B, H, S, D)).astype(np.float32) * 0.1
+    k = rng.standard_normal((B, H, S, D)).astype(np.float32) * 0.1
+    k[0, 0, 7] = 2.0          # a key in the first tile that dominates every row's max
+    q[0, 0, :, :] = np.abs(q[0, 0, :, :]) * np.sign(k[0, 0, 7])
+    v = rnd((B, H, S, D), 3)
+    rows = allrows(B, H, S)
+    base = oracle.fsa_emulate(oracle.MxInputs.from_bf16(bf(q), bf(k), v, 0, 0), S, False, 0.125, 0, rows)
+    assert not base["fallbacks"].any()
+    k[0, 0, 300] = 8.0 * q[0, 0, 5] / np.abs(q[0, 0, 5]).max()   # large score for row 5, tile 2
+    mx = oracle.MxInputs.from_bf16(bf(q), bf(k), v, 0, 0)
+    res = oracle.fsa_emulate(mx, S, False, 0.125, 0, rows, dump=True)
+    fired = np.nonzero(res["fallbacks"])[0]
+    assert 5 in fired and res["fallbacks"][5] == 1
+    mf = res["m_frozen"][5]
+    assert mf[0] == mf[1] < mf[2]
+    # a margin larger than the planted excess suppresses it; the output agrees to quantisation noise
+    big = oracle.fsa_emulate(mx, S, False, 0.125, 0, rows, delta=40.0)
+    assert not big["fallbacks"].any()
+    ex = oracle.attn_floor(mx, S, False, 0.125, 0, rows, quantize_p=False)
+    e_res = np.linalg.norm(res["out"] - ex) / np.linalg.norm(ex)
+    e_big = np.linalg.norm(big["out"] - ex) / np.linalg.norm(ex)
+    assert e_res < 0.1 and e_big < 0.1 and 0.5 < e_res / e_big < 2.0, (e_res, e_big)
+    # a margin only moves the block exponents (the per-block scales absorb it): the
+    # output stays within quantisation noise of the margin-free result
+    d43 = oracle.fsa_emulate(mx, S, False, 0.125, 0, rows, delta=43.0)
+    assert np.linalg.norm(d43["out"] - big["out"]) / np.linalg.norm(big["out"]) < 0.02
+
+
+def test_emulate_pgen_block_structure():
+    """Block max element gets the top codes; EFQ codes are a monotone function of
+    the score within a block; integer residuals map to exact powers of two."""
+    B, H, S, D = 1, 1, 256, 64
+    q, k, v = rnd((B, H, S, D), 1, 1.5), rnd((B, H, S, D), 2), rnd((B, H, S, D), 3)
+    mx = oracle.MxInputs.from_bf16(q, k, v, 2, 2)
+    res = oracle.fsa_emulate(mx, S, False, 0.125, 3, allrows(B, H, S), dump=True)
+    s, pc = res["s"], res["p_codes"]
+    for row in range(0, S, 17):
+        for b in range(S // 32):
+            blk_s, blk_c = s[row, 32 * b:32 * b + 32], pc[row, 32 * b:32 * b + 32]
+            assert blk_c[np.argmax(blk_s)] in (6, 7)
+            order = np.argsort(blk_s, kind="stable")
+            assert np.all(np.diff(blk_c[order].astype(int)) >= 0)
+    mx8 = oracle.MxInputs.from_bf16(q, k, v, 0, 0)
+    r8 = oracle.fsa_emulate(mx8, S, False, 0.125, 0, allrows(B, H, S), dump=True)
+    top = {0x78, 0x7E}    # block max lands in [2^8, 448] (E4M3 256 .. 448)
+    for row in range(0, S, 13):
+        for b in range(S // 32):
+            c = r8["p_codes"][row, 32 * b + np.argmax(r8["s"][row, 32 * b:32 * b + 32])]
+            assert 0x78 <= c <= 0x7E
+
+
+@pytest.mark.parametrize("fq,fp,bound", [(0, 0, 1.1), (1, 1, 1.1), (2, 2, 1.1), (2, 3, 2.0)])
+def test_emulate_error_close_to_floor_on_tiny(fq, fp, bound):
+    """The pages' claim (Fused-Softmax brief, abstract): the approximation's extra
+    error stays near the floor set by quantising the GEMM operands.  The exp paths
+    meet 1.1x; the EFQ direct-code reading costs more (measured ~1.5x) because its
+    log-domain rounding zeroes values below ~0.59 2^E that E2M1 rounding keeps."""
+    from workloads import WORKLOADS, generate, sample_rows
+    w = WORKLOADS["tiny"]
+    q, k, v = generate(w)
+    fv = 2 if fp == 3 else fp
+    mx = oracle.MxInputs.from_bf16(q, k, v, fq, fv)
+    rows = sample_rows(w)
+    ex = oracle.attn_exact(q, k, v, w.causal, w.scale, rows)
+    fl = oracle.attn_floor(mx, w.Sk, w.causal, w.scale, fv, rows)
+    em = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows)["out"]
+    e_fl = np.linalg.norm(fl - ex) / np.linalg.norm(ex)
+    e_em = np.linalg.norm(em - ex) / np.linalg.norm(ex)
+    assert e_em <= bound * e_fl, (e_em, e_fl)
+
+
+# --------------------------------------------------------------------------- bf16 baseline emulation
+def test_bf16_emulate_pins():
+    B, H, S, D = 1, 2, 300, 64
+    q, k, v = rnd((B, H, S, D), 1, 2.0), rnd((B, H, S, D), 2), rnd((B, H, S, D), 3)
+    rows = allrows(B, H, S)
+    z = oracle.bf16_emulate(bf(np.zeros((B, H, S, D))), k, v, True, 0.125, rows)["out"]
+    vf = bf16_bits_to_f32(v).astype(np.float64)
+    assert np.allclose(z[S + 200], vf[0, 1, :201].mean(axis=0), atol=1e-12)
+    ones = oracle.bf16_emulate(q, k, bf(np.ones((B, H, S, D))), False, 0.125, rows)["out"]
+    assert np.allclose(ones, 1.0, atol=1e-13)
+    ex = oracle.attn_exact(q, k, v, True, 0.125, rows)
+    em = oracle.bf16_emulate(q, k, v, True, 0.125, rows)["out"]
+    assert np.abs(em - ex).max() / np.sqrt((ex ** 2).mean()) < 1e-2
+    # growing scores across tiles trigger the lazy rescale only past tau
+    kk = bf16_bits_to_f32(k).copy()
+    kk[0, 0, 200] = 8.0 * bf16_bits_to_f32(q)[0, 0, 250]
+    r = oracle.bf16_emulate(q, bf(kk), v, False, 0.125, rows)
+    assert r["rescales"][250] == 1

@@ -1,0 +1,175 @@
+/*
+ * fsa.h -- C ABI of libfsa: MX block-scaled attention forward with a
+ * reformulated softmax, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (by page title and section):
+ *   "Fused-Softmax for efficient quantized attention" (The Singularity Report),
+ *       abstract: QK^T and PV as MXFP8/MXFP6/MXFP4 GEMMs; softmax reformulated
+ *       and approximated so its dominant work folds into the GEMMs; BF16
+ *       attention as the comparison point.
+ *   "Moving softmax to matrix operations speeds up AI inference by over 2x"
+ *       (zot.news), summary, "Read it as" and the "How it works" figure: max
+ *       subtraction and exponentiation folded into the score GEMM; the row
+ *       maximum frozen speculatively with a fallback; a fast exponential;
+ *       "Exp + MX Quant" fused; probabilities summed on the matrix unit.
+ *   "EFQ-Softmax: Exp-Free Quantization for Softmax" (paper-with-me),
+ *       abstract: per 32-element block an exponent-only scale from the local
+ *       maximum and nonnegative E2M1 probability codes from one affine rule;
+ *       the same operand feeds the P~V numerator and the P~1 denominator;
+ *       final normalisation in high precision.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, allocated and owned by the
+ *     caller; the library keeps no reference after the call returns.  The
+ *     library allocates no device memory on any entry point below.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Work is enqueued asynchronously; no entry point
+ *     synchronises.
+ *   - Return value: FSA_OK (0) or a negative FSA_ERR_* code.  Argument errors
+ *     are detected on the host before any launch; nothing is enqueued then.
+ *   - Shapes: B batch, H query heads, Hkv key/value heads (H % Hkv == 0; query
+ *     head h reads kv head h / (H/Hkv)), Sq queries, Sk keys, head dim D in
+ *     {64, 128}.  Causal masking is bottom-right aligned: key j is visible to
+ *     query i iff j <= i + Sk - Sq.  A query with no visible key gets a zero
+ *     output row.
+ */
+#ifndef FSA_H
+#define FSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define FSA_OK                   0
+#define FSA_ERR_INVALID_ARG     -1  /* null pointer, bad shape, misaligned pointer */
+#define FSA_ERR_UNSUPPORTED_FMT -2  /* e.g. E2M1_EFQ as a QK^T operand format */
+#define FSA_ERR_LAUNCH          -3  /* CUDA runtime/driver error at launch */
+#define FSA_ERR_TIMEOUT         -4  /* a bounded on-chip wait gave up (reported via fsa_stats) */
+#define FSA_ERR_NO_DEVICE       -5  /* no sm_100-family device with tcgen05 */
+
+/* ------------------------------------------------------- element formats */
+/* OCP MX element types; E2M1_EFQ is the E2M1 operand produced by the EFQ
+ * direct-code rule and is valid only as the PV format. */
+typedef enum {
+  FSA_FMT_E4M3 = 0,      /* MXFP8 */
+  FSA_FMT_E2M3 = 1,      /* MXFP6 */
+  FSA_FMT_E2M1 = 2,      /* MXFP4, P by exp then round-to-nearest-even */
+  FSA_FMT_E2M1_EFQ = 3   /* MXFP4, P by the EFQ affine rule (fmt_pv only) */
+} fsa_fmt;
+
+/* ------------------------------------------------------------ MX tensors */
+/* An MX tensor holds element codes plus one E8M0 scale byte (2^(byte-127))
+ * per 32 consecutive elements along the contraction dimension.
+ *
+ * FSA_MX_ROWS (Q and K; blocks along D).  Source x[B][H][S][D] bf16.
+ *   codes : [B*H][S][row_bytes], row_bytes = D (E4M3, E2M3) or D/2 (E2M1).
+ *           E4M3: one byte per element.  E2M3: each group of 16 elements is
+ *           12 bytes of 6-bit codes packed least-significant-bit first,
+ *           followed by 4 zero bytes.  E2M1: two elements per byte, the even
+ *           element in the low nibble.
+ *   scales: [B*H][ceil(S/128)][512] bytes: for row r of a 128-row tile and
+ *           block b (b < D/32), byte (r%32)*16 + (r/32)*4 + b.  Slots with no
+ *           data (rows >= S, blocks >= D/32) hold 0x7F.
+ * FSA_MX_COLS_T (V; blocks along S, stored transposed, K-major for PV).
+ *   codes : [B*H][D][Sp] elements, Sp = S rounded up to 128, packed as above
+ *           along the key axis; codes of keys >= S are 0.
+ *   scales: [B*H][Sp/128][512] bytes: for d (row of V^T) and key block b of
+ *           a 128-key tile, byte (d%32)*16 + (d/32)*4 + b.  Rows d >= D hold
+ *           0x7F; blocks of keys wholly >= S hold 0x7F.
+ * The block scale is E = clamp(floor(log2 amax) - emax, -127, 127) (emax 8
+ * for E4M3, 2 for E2M3/E2M1), codes = round-to-nearest-even, saturating, of
+ * x * 2^-E; a block with a non-finite element gets scale 0xFF.           */
+typedef enum { FSA_MX_ROWS = 0, FSA_MX_COLS_T = 1 } fsa_mx_layout;
+
+typedef struct {
+  void*    codes;    /* device, 16-byte aligned */
+  uint8_t* scales;   /* device, 16-byte aligned */
+  int32_t  fmt;      /* fsa_fmt of the codes (E4M3, E2M3 or E2M1) */
+  int32_t  layout;   /* fsa_mx_layout */
+  int32_t  B, H, S, D;
+} fsa_mx_tensor;
+
+/* Bytes of the codes and scales buffers for an MX tensor. */
+int fsa_mx_sizes(int B, int H, int S, int D, int layout, int fmt, size_t* codes_bytes, size_t* scales_bytes);
+
+/* Quantise x_bf16 [B][H][S][D] (device, 16-byte aligned) into out->codes /
+ * out->scales with the given layout and element format.  The shape, layout
+ * and format fields of *out are written by the call.  Cited: MXFP8/6/4 GEMM
+ * operands ("Fused-Softmax for efficient quantized attention", abstract). */
+int fsa_mx_quantize(const void* x_bf16, int B, int H, int S, int D, int layout, int fmt,
+                    fsa_mx_tensor* out, void* stream);
+
+/* ------------------------------------------------------ options and stats */
+typedef enum {
+  FSA_EXP_POLY = 0,   /* cubic interpolant of 2^f on the FMA pipe for every element */
+  FSA_EXP_MUFU = 1,   /* hardware ex2.approx for every element */
+  FSA_EXP_SPLIT = 2   /* even key positions ex2.approx, odd positions the cubic */
+} fsa_exp_mode;
+
+typedef struct {
+  float    delta;        /* frozen-max margin in log2 units (default 0) */
+  int32_t  exp_mode;     /* fsa_exp_mode (default FSA_EXP_SPLIT) */
+  int32_t  efq_beta;     /* integer offset of the EFQ rule code = rne(2 r + beta) (default 2) */
+  uint32_t timeout_ms;   /* limit of each on-chip wait (0: 4000 ms) */
+  int32_t* row_fallbacks;/* optional device int32 [B][H][Sq]: fallback count per row */
+  int32_t  inject_stall; /* test hook: 1 makes the MMA warp wait on a barrier nobody
+                            arrives on, so the bounded wait expires (status TIMEOUT) */
+  int32_t  reserved[3];
+} fsa_opts;
+
+typedef struct {                      /* device memory, zeroed by the caller */
+  unsigned long long fallback_events; /* (row, tile) pairs whose score beat the frozen max */
+  unsigned long long row_tiles;       /* (row, tile) pairs with at least one visible key */
+  int32_t status;                     /* FSA_OK or FSA_ERR_TIMEOUT */
+  int32_t reserved;
+} fsa_stats;
+
+void fsa_default_opts(fsa_opts* opts);
+
+/* ------------------------------------------------------------- attention */
+/* O[B][H][Sq][D] fp32 = softmax(scale * Q K^T) V computed by the fused MX
+ * algorithm: QK^T as a block-scaled MMA into tensor memory; the row maximum
+ * frozen from the first key tile of 128 (plus delta), with a fallback that
+ * rescales the accumulator when a later tile's maximum exceeds it; per
+ * 32-key block an exponent-only scale from the block maximum and codes by
+ * exp-then-round (fmt_pv E4M3/E2M3/E2M1) or the EFQ rule (E2M1_EFQ);
+ * P~ [V^|1] as a block-scaled MMA whose extra ones column accumulates the
+ * denominator; O = O_acc / l in fp32.
+ * q, k: FSA_MX_ROWS tensors in fmt_qk; v: FSA_MX_COLS_T tensor in the
+ * element format of fmt_pv (E2M1 for E2M1_EFQ).  out: device fp32, 16-byte
+ * aligned.  scale: softmax scale (e.g. 1/sqrt(D)). */
+int fsa_attention_fwd(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, float* out,
+                      int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                      int fmt_qk, int fmt_pv, void* stream);
+
+/* As fsa_attention_fwd with options (NULL: defaults) and device statistics
+ * (NULL: none; without stats a wait that times out is not reported). */
+int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, float* out,
+                         int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                         int fmt_qk, int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream);
+
+/* Rearrange V [B][Hkv][S][D] bf16 into V^T [B][Hkv][D][Sp] bf16 (Sp = S
+ * rounded up to 128, zero padded) for the BF16 kernel. */
+int fsa_bf16_transpose_v(const void* v, void* vt, int B, int Hkv, int S, int D, void* stream);
+
+/* In-house baseline: the same kernel skeleton with BF16 operands and exact
+ * online softmax (standard attention of the "How it works" figure, tiled with
+ * the running maximum and historical rescaling that the EFQ page keeps
+ * unchanged; rescale only when the maximum grows by more than 8 in log2
+ * units).  q [B][H][Sq][D], vt from fsa_bf16_transpose_v, k [B][Hkv][Sk][D],
+ * all bf16 device, 16-byte aligned; out fp32. */
+int fsa_attention_fwd_bf16(const void* q, const void* k, const void* vt, float* out,
+                           int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                           fsa_stats* stats, void* stream);
+
+const char* fsa_status_string(int status);
+int fsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FSA_H */

@@ -1,0 +1,222 @@
+"""ctypes binding of libfsa (include/fsa.h).  Argument marshalling only: every
+step of the computation runs in the library's CUDA kernels; torch provides
+device memory and the current stream.  There is no CPU fallback: without the
+compiled library every entry point raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+FSA_OK, FSA_ERR_INVALID_ARG, FSA_ERR_UNSUPPORTED_FMT, FSA_ERR_LAUNCH, FSA_ERR_TIMEOUT, FSA_ERR_NO_DEVICE = \
+    0, -1, -2, -3, -4, -5
+FSA_FMT_E4M3, FSA_FMT_E2M3, FSA_FMT_E2M1, FSA_FMT_E2M1_EFQ = 0, 1, 2, 3
+FSA_MX_ROWS, FSA_MX_COLS_T = 0, 1
+FSA_EXP_POLY, FSA_EXP_MUFU, FSA_EXP_SPLIT = 0, 1, 2
+FMT_BY_NAME = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
+
+
+class FsaError(RuntimeError):
+    def __init__(self, status, what):
+        try:
+            msg = status_string(status)
+        except Exception:  # library not loadable
+            msg = "libfsa unavailable"
+        super().__init__(f"{what}: {msg} ({status})")
+        self.status = status
+
+
+class fsa_mx_tensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("fmt", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("S", ctypes.c_int32),
+                ("D", ctypes.c_int32)]
+
+
+class fsa_opts(ctypes.Structure):
+    _fields_ = [("delta", ctypes.c_float), ("exp_mode", ctypes.c_int32), ("efq_beta", ctypes.c_int32),
+                ("timeout_ms", ctypes.c_uint32), ("row_fallbacks", ctypes.c_void_p), ("inject_stall", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
+
+
+STATS_BYTES = 24      # fsa_stats: u64 fallback_events, u64 row_tiles, i32 status, i32 reserved
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libfsa.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_missing else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libfsa.so not found at {path}")
+            L = ctypes.CDLL(path)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            L.fsa_mx_sizes.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
+            L.fsa_mx_quantize.argtypes = [vp, i, i, i, i, i, i, ctypes.POINTER(fsa_mx_tensor), vp]
+            L.fsa_attention_fwd.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + [vp, i, i, i, i, i, i, i, f, i, i, vp]
+            L.fsa_attention_fwd_ex.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + \
+                [vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, vp]
+            L.fsa_bf16_transpose_v.argtypes = [vp, vp, i, i, i, i, vp]
+            L.fsa_attention_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp]
+            L.fsa_default_opts.argtypes = [ctypes.POINTER(fsa_opts)]
+            L.fsa_default_opts.restype = None
+            L.fsa_status_string.argtypes = [i]
+            L.fsa_status_string.restype = ctypes.c_char_p
+            for n in ("fsa_mx_sizes", "fsa_mx_quantize", "fsa_attention_fwd", "fsa_attention_fwd_ex",
+                      "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version"):
+                getattr(L, n).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return load().fsa_status_string(int(s)).decode()
+
+
+def _check(status, what):
+    if status != FSA_OK:
+        raise FsaError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _fmt(f):
+    return FMT_BY_NAME[f] if isinstance(f, str) else int(f)
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise FsaError(FSA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise FsaError(FSA_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise FsaError(FSA_ERR_INVALID_ARG, f"{name} must be {dtype}")
+
+
+# ----------------------------------------------------------------------------- MX tensors
+class MxTensor:
+    """Device MX tensor: codes and scales owned by torch, described by fsa_mx_tensor."""
+
+    def __init__(self, codes: torch.Tensor, scales: torch.Tensor, fmt: int, layout: int, B, H, S, D):
+        self.codes, self.scales = codes, scales
+        self.fmt, self.layout, self.B, self.H, self.S, self.D = int(fmt), int(layout), B, H, S, D
+
+    def struct(self) -> fsa_mx_tensor:
+        return fsa_mx_tensor(self.codes.data_ptr(), self.scales.data_ptr(), self.fmt, self.layout,
+                             self.B, self.H, self.S, self.D)
+
+
+def fsa_mx_sizes(B, H, S, D, layout, fmt):
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().fsa_mx_sizes(B, H, S, D, int(layout), _fmt(fmt), ctypes.byref(cb), ctypes.byref(sb)), "fsa_mx_sizes")
+    return cb.value, sb.value
+
+
+def empty_mx(B, H, S, D, layout, fmt, device) -> MxTensor:
+    cb, sb = fsa_mx_sizes(B, H, S, D, layout, fmt)
+    return MxTensor(torch.empty(cb, dtype=torch.uint8, device=device), torch.empty(sb, dtype=torch.uint8, device=device),
+                    _fmt(fmt), layout, B, H, S, D)
+
+
+def fsa_mx_quantize(x: torch.Tensor, layout, fmt, out: MxTensor | None = None, stream=None) -> MxTensor:
+    """Quantise x (bf16 [B,H,S,D] on the GPU) into an MX tensor (FSA_MX_ROWS for Q/K, FSA_MX_COLS_T for V)."""
+    _need_cuda(x, "x", torch.bfloat16)
+    B, H, S, D = x.shape
+    fmt = _fmt(fmt)
+    if out is None:
+        out = empty_mx(B, H, S, D, layout, fmt, x.device)
+    st = out.struct()
+    _check(load().fsa_mx_quantize(ctypes.c_void_p(x.data_ptr()), B, H, S, D, int(layout), fmt, ctypes.byref(st),
+                                  _stream(stream)), "fsa_mx_quantize")
+    return out
+
+
+def default_opts() -> fsa_opts:
+    o = fsa_opts()
+    load().fsa_default_opts(ctypes.byref(o))
+    return o
+
+
+def new_stats(device=None) -> torch.Tensor:
+    """Zeroed device buffer for fsa_stats (read it back with read_stats)."""
+    return torch.zeros(STATS_BYTES // 8, dtype=torch.int64, device=device or "cuda")
+
+
+def read_stats(stats: torch.Tensor) -> dict:
+    v = stats.cpu()
+    st = int(v[2].item() & 0xFFFFFFFF)
+    st = st - (1 << 32) if st >= 1 << 31 else st
+    return dict(fallback_events=int(v[0].item()), row_tiles=int(v[1].item()), status=st)
+
+
+def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
+                      causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=0.0, exp_mode=FSA_EXP_SPLIT,
+                      efq_beta=2, timeout_ms=0, row_fallbacks: torch.Tensor | None = None, stats=None,
+                      inject_stall=False, stream=None) -> torch.Tensor:
+    """O [B,H,Sq,D] fp32 by the fused MX forward (fsa_attention_fwd_ex)."""
+    B, H, Sq, D = q.B, q.H, q.S, q.D
+    Hkv = k.H if Hkv is None else Hkv
+    Sk = k.S
+    scale = D ** -0.5 if scale is None else scale
+    fmt_qk = q.fmt if fmt_qk is None else _fmt(fmt_qk)
+    fmt_pv = v.fmt if fmt_pv is None else _fmt(fmt_pv)
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=torch.float32, device=q.codes.device)
+    _need_cuda(out, "out", torch.float32)
+    o = default_opts()
+    o.delta, o.exp_mode, o.efq_beta, o.timeout_ms = float(delta), int(exp_mode), int(efq_beta), int(timeout_ms)
+    o.inject_stall = int(bool(inject_stall))
+    if row_fallbacks is not None:
+        _need_cuda(row_fallbacks, "row_fallbacks", torch.int32)
+        o.row_fallbacks = row_fallbacks.data_ptr()
+    qs, ks, vs = q.struct(), k.struct(), v.struct()
+    _check(load().fsa_attention_fwd_ex(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs),
+                                       ctypes.c_void_p(out.data_ptr()), B, H, Hkv, Sq, Sk, D, int(bool(causal)),
+                                       float(scale), fmt_qk, fmt_pv, ctypes.byref(o),
+                                       ctypes.c_void_p(stats.data_ptr() if stats is not None else 0),
+                                       _stream(stream)), "fsa_attention_fwd_ex")
+    return out
+
+
+def fsa_bf16_transpose_v(v: torch.Tensor, vt: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _need_cuda(v, "v", torch.bfloat16)
+    B, Hkv, S, D = v.shape
+    Sp = (S + 127) // 128 * 128
+    if vt is None:
+        vt = torch.empty((B, Hkv, D, Sp), dtype=torch.bfloat16, device=v.device)
+    _check(load().fsa_bf16_transpose_v(ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(vt.data_ptr()), B, Hkv, S, D,
+                                       _stream(stream)), "fsa_bf16_transpose_v")
+    return vt
+
+
+def fsa_attention_fwd_bf16(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, out: torch.Tensor | None = None, *,
+                           causal=False, scale=None, stats=None, stream=None) -> torch.Tensor:
+    """O [B,H,Sq,D] fp32 by the exact-softmax BF16 kernel; vt from fsa_bf16_transpose_v."""
+    for t, n in ((q, "q"), (k, "k"), (vt, "vt")):
+        _need_cuda(t, n, torch.bfloat16)
+    B, H, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    scale = D ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=torch.float32, device=q.device)
+    _check(load().fsa_attention_fwd_bf16(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                         ctypes.c_void_p(vt.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                         B, H, Hkv, Sq, Sk, D, int(bool(causal)), float(scale),
+                                         ctypes.c_void_p(stats.data_ptr() if stats is not None else 0),
+                                         _stream(stream)), "fsa_attention_fwd_bf16")
+    return out

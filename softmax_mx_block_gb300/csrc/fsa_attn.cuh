@@ -1,0 +1,96 @@
+// fsa_attn.cuh -- compile-time configuration of the fused attention kernel:
+// operand storage formats, shared-memory and tensor-memory layouts.
+#pragma once
+#include <cstdint>
+#include "fsa_ptx.cuh"
+
+namespace fsa {
+
+// Operand formats.  F_EFQ stores E2M1 like F_E2M1; it only changes how the
+// softmax warps produce P.
+enum : int { F_E4M3 = 0, F_E2M3 = 1, F_E2M1 = 2, F_EFQ = 3, F_BF16 = 4 };
+
+template <int F> struct Fmt;
+// kind: 0 = kind::f16, 1 = kind::mxf8f6f4 (scale_vec 1X, K = 32), 2 = kind::mxf4 (2X, K = 64)
+// bits2: storage bits per element * 2 (E2M1 packs two per byte)
+template <> struct Fmt<F_BF16> { static constexpr int kind = 0, bits2 = 32, code = 0, emax = 0; };
+template <> struct Fmt<F_E4M3> { static constexpr int kind = 1, bits2 = 16, code = 0, emax = 8; };
+template <> struct Fmt<F_E2M3> { static constexpr int kind = 1, bits2 = 16, code = 3, emax = 2; };  // 16 codes / 16 bytes
+template <> struct Fmt<F_E2M1> { static constexpr int kind = 2, bits2 = 8, code = 1, emax = 2; };
+template <> struct Fmt<F_EFQ>  { static constexpr int kind = 2, bits2 = 8, code = 1, emax = 2; };
+
+__host__ __device__ constexpr int swz_code(int width) { return width == 128 ? 2 : (width == 64 ? 4 : 6); }
+
+template <int FQK, int FPV, int D_>
+struct Cfg {
+  static constexpr int D = D_;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr bool MX = FQK != F_BF16;
+  static_assert((FQK == F_BF16) == (FPV == F_BF16), "BF16 kernel uses BF16 for both GEMMs");
+  static_assert(FQK != F_EFQ, "EFQ is a P format");
+  // ---- QK^T operands (Q, K rows of D elements)
+  static constexpr int RB_QK = D * Fmt<FQK>::bits2 / 16;            // bytes per row
+  static constexpr int W_QK = RB_QK < 128 ? RB_QK : 128;            // swizzle atom width
+  static constexpr int NKA_QK = RB_QK / W_QK;                       // atoms along K
+  static constexpr int QK_STEPS = RB_QK / 32;                       // 32 bytes of K per MMA
+  static constexpr int TILE_QK = BM * RB_QK;                        // bytes of a 128-row tile
+  // ---- PV operands (V^T rows of 128 keys, plus 16 rows: ones row, zero rows)
+  static constexpr int N_PV = D + 16;
+  static constexpr int RB_V = BN * Fmt<FPV>::bits2 / 16;            // bytes per V^T row per key tile
+  static constexpr int W_V = RB_V < 128 ? RB_V : 128;
+  static constexpr int NKA_V = RB_V / W_V;
+  static constexpr int PV_STEPS = RB_V / 32;
+  static constexpr int STEPS_PER_HALF = PV_STEPS / 2;
+  static constexpr int VATOM = N_PV * W_V;                          // bytes of one K-atom of the V tile
+  static constexpr int TILE_V = NKA_V * VATOM;
+  static constexpr int TILE_V_TMA = NKA_V * D * W_V;                // bytes TMA writes per tile
+  // ---- P in tensor memory: 64 keys per softmax half
+  static constexpr int P_COLS_HALF = 64 * Fmt<FPV>::bits2 / 16 / 4;
+  // ---- pipeline
+  static constexpr int NS = MX ? 3 : 2;                             // K/V stages
+  static constexpr int SF_BYTES = 512;
+  // ---- shared memory offsets (1024-aligned tiles)
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE_QK;
+  static constexpr int OFF_V = OFF_K + NS * TILE_QK;
+  static constexpr int OFF_SF = (OFF_V + NS * TILE_V + 1023) / 1024 * 1024;
+  static constexpr int OFF_SFQ = OFF_SF;
+  static constexpr int OFF_SFK = OFF_SFQ + SF_BYTES;
+  static constexpr int OFF_SFV = OFF_SFK + NS * SF_BYTES;
+  static constexpr int OFF_SFONE = OFF_SFV + NS * SF_BYTES;
+  static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // row-max exchange [parity][half][row] fp32
+  static constexpr int OFF_BAR = OFF_RED + 2 * 2 * 128 * 4;
+  static constexpr int NBAR = 1 + 4 * NS + 3 * 2 + 2;               // q, k/v full/empty, s/p/pv x2, drain, stall
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  // ---- tensor memory columns
+  static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256); P aliases its half of S
+  static constexpr uint32_t T_O = 256;        // [256, 256 + N_PV)
+  static constexpr uint32_t T_SFQ = 400;
+  static constexpr uint32_t T_SFK = 404;      // + 4 * parity
+  static constexpr uint32_t T_SFV = 412;      // + 8 * parity (4 from the V atom, 4 constant)
+  static constexpr uint32_t T_SFP = 428;      // + 8 * parity + 4 * half
+  static_assert(T_O + N_PV <= T_SFQ, "tmem");
+  // ---- threads
+  static constexpr int NTHREADS = 320;        // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+};
+
+struct KParams {
+  int B, H, Hkv, Sq, Sk, n_qtiles, causal;
+  float c;                // fp32(scale * log2 e)
+  float delta;
+  int efq_beta;
+  uint64_t timeout_ns;
+  const uint8_t* sf_q;    // [B*H][ceil(Sq/128)][512]
+  const uint8_t* sf_k;    // [B*Hkv][ceil(Sk/128)][512]
+  const uint8_t* sf_v;    // [B*Hkv][Sp/128][512]
+  float* out;             // [B][H][Sq][D]
+  int32_t* row_fallbacks; // optional [B][H][Sq]
+  unsigned long long* stat_fallbacks;
+  unsigned long long* stat_row_tiles;
+  int* status;
+  int inject_stall;
+};
+
+}  // namespace fsa

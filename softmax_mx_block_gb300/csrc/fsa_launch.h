@@ -1,0 +1,28 @@
+// fsa_launch.h -- host-side launch descriptors shared by the API and the kernel TUs.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "fsa_attn.cuh"
+
+namespace fsa {
+
+struct AttnLaunch {
+  CUtensorMap tq, tk, tv;
+  KParams p;
+  int D;
+  int exp_mode;          // 0 poly, 1 MUFU, 2 split (ignored for EFQ and BF16)
+  cudaStream_t stream;
+};
+
+// One explicit instantiation per (QK format, PV format) lives in its own
+// translation unit (compiled in parallel); D and exp_mode dispatch inside.
+template <int FQK, int FPV>
+cudaError_t launch_attn_impl(const AttnLaunch& a);
+
+cudaError_t launch_mx_quant_rows(const void* x, int64_t R, int S, int D, int fmt, void* codes, void* scales,
+                                 cudaStream_t st);
+cudaError_t launch_mx_quant_cols(const void* x, int BH, int S, int D, int fmt, void* codes, void* scales,
+                                 cudaStream_t st);
+cudaError_t launch_transpose_v(const void* v, void* vt, int BH, int S, int D, cudaStream_t st);
+
+}  // namespace fsa

@@ -1,0 +1,278 @@
+// fsa_ptx.cuh -- inline-PTX building blocks for sm_103a: mbarriers with bounded
+// waits, TMA tile and bulk copies, and the tcgen05 tensor-core / tensor-memory
+// instructions.  Layout facts used here (shared-memory matrix descriptors,
+// instruction descriptors, scale-factor placement in tensor memory) follow the
+// PTX ISA for tcgen05 and were checked on the device with small in-bounds MMAs.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fsa {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               " selp.b32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Shared abort state of one CTA: once any wait gives up, every later wait of
+// the CTA returns false at once so that all roles drain and reach teardown.
+struct AbortCtl {
+  volatile int* flag;      // shared memory
+  int* status;             // global status word (may be null)
+  uint64_t limit_ns;
+};
+
+// Wait for phase `parity` of `bar`; false if the limit passed or the CTA aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const AbortCtl& ac) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*ac.flag) return false;
+      if (globaltimer_ns() - t0 > ac.limit_ns) {
+        *ac.flag = 1;
+        if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
+        return false;
+      }
+    }
+  }
+}
+
+// Wait that ignores the CTA abort flag (teardown: drain work still in flight).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- TMA / bulk
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z) : "memory");
+}
+// Untiled bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(smem_u32(slot_smem)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Copy a 512-byte 128x4 scale atom (32 lines of 16 bytes) from shared memory
+// into 4 tensor-memory columns, replicated in all four lane quadrants:
+// lane 32q+r, column c receives line r bytes 4c..4c+3.
+__device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, BF16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem)^T, BF16.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// Block-scaled, 8/6/4-bit elements (one scale per 32 K per MMA, K = 32).
+__device__ __forceinline__ void mma_mxf8f6f4_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_mxf8f6f4_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
+// Block-scaled packed E2M1 (two scales per MMA, K = 64).
+__device__ __forceinline__ void mma_mxf4_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_mxf4_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, stride between 8-row core
+// groups (sbo), leading offset (lbo, unused for K-major swizzled tiles),
+// descriptor version 1 (bit 46), swizzle code in bits 61-63
+// (0 none, 2 = 128B, 4 = 64B, 6 = 32B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
+}
+
+// Instruction descriptors (M = 128, fp32 accumulator).
+__host__ __device__ constexpr uint32_t idesc_f16_bf16(int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+// Block-scaled: a/b element codes (mxf8f6f4: E4M3 0, E2M3 3, E2M1 5; mxf4: E2M1 1),
+// E8M0 scales (bit 23), scale byte selectors sfa_id (bits 29-30), sfb_id (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_bs(int N, uint32_t ab_fmt, uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(128 >> 4) << 24) | (sfa_id << 29);
+}
+
+// tcgen05.ld / st, 32 lanes x 32 bits, N consecutive columns per thread.
+template <int N> struct TmemLd;
+#define FSA_TMEM_LD(N, REGS, ...)                                                            \
+  template <> struct TmemLd<N> {                                                             \
+    __device__ __forceinline__ static void run(uint32_t taddr, uint32_t* r) {                \
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x" #N ".b32 {" REGS "}, [%" #N "];"       \
+                   : __VA_ARGS__ : "r"(taddr) : "memory");                                   \
+    }                                                                                        \
+  };
+FSA_TMEM_LD(1, "%0", "=r"(r[0]))
+FSA_TMEM_LD(8, "%0,%1,%2,%3,%4,%5,%6,%7", "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+            "=r"(r[5]), "=r"(r[6]), "=r"(r[7]))
+FSA_TMEM_LD(16, "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15", "=r"(r[0]), "=r"(r[1]), "=r"(r[2]),
+            "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]),
+            "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]))
+#undef FSA_TMEM_LD
+
+template <int N> struct TmemSt;
+#define FSA_TMEM_ST(N, REGS, ...)                                                            \
+  template <> struct TmemSt<N> {                                                             \
+    __device__ __forceinline__ static void run(uint32_t taddr, const uint32_t* r) {          \
+      asm volatile("tcgen05.st.sync.aligned.32x32b.x" #N ".b32 [%0], {" REGS "};"            \
+                   ::"r"(taddr), __VA_ARGS__ : "memory");                                    \
+    }                                                                                        \
+  };
+FSA_TMEM_ST(1, "%1", "r"(r[0]))
+FSA_TMEM_ST(8, "%1,%2,%3,%4,%5,%6,%7,%8", "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+            "r"(r[6]), "r"(r[7]))
+FSA_TMEM_ST(16, "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16", "r"(r[0]), "r"(r[1]), "r"(r[2]),
+            "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
+            "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]))
+#undef FSA_TMEM_ST
+
+// NCOLS consecutive columns (8, or a multiple of 16).
+template <int NCOLS>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (NCOLS >= 16) {
+#pragma unroll
+    for (int c = 0; c < NCOLS; c += 16) TmemLd<16>::run(taddr + c, r + c);
+  } else {
+    TmemLd<NCOLS>::run(taddr, r);
+  }
+}
+template <int NCOLS>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+  if constexpr (NCOLS >= 16) {
+#pragma unroll
+    for (int c = 0; c < NCOLS; c += 16) TmemSt<16>::run(taddr + c, r + c);
+  } else {
+    TmemSt<NCOLS>::run(taddr, r);
+  }
+}
+
+// ------------------------------------------------------------- conversions
+// Two fp32 -> packed codes; `lo` lands in the low byte / nibble.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e2m3x2(float lo, float hi) {   // each code in a byte, low 6 bits
+  uint16_t r;
+  asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {   // one byte, lo in the low nibble
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Pack 16 six-bit codes (one per byte in w[0..3], little-endian) into 12 bytes
+// (least significant bit first) in out[0..2]; the 16-byte group's last word is 0.
+__device__ __forceinline__ void pack6x16(const uint32_t* w, uint32_t* out) {
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t u = (w[i] & 0x003F003Fu) | ((w[i] & 0x3F003F00u) >> 2);   // 12-bit pairs at bits 0, 16
+    p[i] = (u & 0xFFFu) | ((u >> 4) & 0xFFF000u);                        // 24 bits
+  }
+  out[0] = p[0] | (p[1] << 24);
+  out[1] = (p[1] >> 8) | (p[2] << 16);
+  out[2] = (p[2] >> 16) | (p[3] << 8);
+}
+
+}  // namespace fsa

@@ -1,0 +1,84 @@
+"""The C ABI library loads and exports every entry point include/fsa.h declares;
+host-only calls (sizes, options, status strings, argument checks) work
+without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = ""
+    for name in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if name.endswith(".h"):
+            src += open(os.path.join(ROOT, "include", name)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fsa_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import softmax_mx_block_gb300 as fsa
+    return fsa.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_sizes_and_status(lib):
+    import softmax_mx_block_gb300 as fsa
+    assert fsa.fsa_mx_sizes(1, 32, 4096, 128, fsa.FSA_MX_ROWS, "E4M3") == (32 * 4096 * 128, 32 * 32 * 512)
+    assert fsa.fsa_mx_sizes(1, 32, 4096, 128, fsa.FSA_MX_ROWS, "E2M1") == (32 * 4096 * 64, 32 * 32 * 512)
+    assert fsa.fsa_mx_sizes(1, 40, 75600, 128, fsa.FSA_MX_COLS_T, "E2M3") == (40 * 128 * 75648, 40 * 591 * 512)
+    assert fsa.fsa_mx_sizes(1, 8, 300, 64, fsa.FSA_MX_COLS_T, "E2M1") == (8 * 64 * 384 // 2, 8 * 3 * 512)
+    with pytest.raises(fsa.FsaError):
+        fsa.fsa_mx_sizes(1, 1, 128, 96, 0, "E4M3")
+    assert fsa.status_string(fsa.FSA_ERR_TIMEOUT) == "on-chip wait timed out"
+    o = fsa.default_opts()
+    assert (o.exp_mode, o.efq_beta, o.timeout_ms, o.delta) == (fsa.FSA_EXP_SPLIT, 2, 4000, 0.0)
+
+
+def test_argument_checks_reject_before_launch(lib):
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import fsa_mx_tensor
+    t = fsa_mx_tensor(16, 16, 0, 0, 1, 1, 128, 128)
+    v = fsa_mx_tensor(16, 16, 0, 1, 1, 1, 128, 128)
+    vp = ctypes.c_void_p
+
+    def args(q, k, vv, H, Hkv, D, fq, fp):
+        return (ctypes.byref(q), ctypes.byref(k), ctypes.byref(vv), vp(16), 1, H, Hkv, 128, 128, D, 0,
+                ctypes.c_float(0.125), fq, fp, vp(0))
+    # H not a multiple of Hkv, D outside {64, 128}, EFQ as a QK format, null pointers
+    assert lib.fsa_attention_fwd(*args(t, t, v, 3, 2, 128, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_attention_fwd(*args(t, t, v, 1, 1, 96, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_attention_fwd(*args(t, t, v, 1, 1, 128, 3, 3)) == fsa.FSA_ERR_UNSUPPORTED_FMT
+    assert lib.fsa_attention_fwd(None, None, None, vp(16), 1, 1, 1, 128, 128, 128, 0, ctypes.c_float(0.1), 0, 0,
+                                 vp(0)) == fsa.FSA_ERR_INVALID_ARG
+    # descriptor mismatch: V passed in the row layout
+    assert lib.fsa_attention_fwd(*args(t, t, t, 1, 1, 128, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
+    # misaligned pointer
+    bad = fsa_mx_tensor(17, 16, 0, 0, 1, 1, 128, 128)
+    assert lib.fsa_attention_fwd(*args(bad, t, v, 1, 1, 128, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_attention_fwd_bf16(vp(16), vp(16), vp(16), vp(16), 1, 2, 3, 128, 128, 128, 0,
+                                      ctypes.c_float(0.1), vp(0), vp(0)) == fsa.FSA_ERR_INVALID_ARG
+    x = fsa_mx_tensor(16, 16, 0, 0, 0, 0, 0, 0)
+    assert lib.fsa_mx_quantize(vp(16), 1, 1, 128, 128, 0, 3, ctypes.byref(x), vp(0)) == fsa.FSA_ERR_UNSUPPORTED_FMT
+    assert lib.fsa_mx_quantize(vp(0), 1, 1, 128, 128, 0, 0, ctypes.byref(x), vp(0)) == fsa.FSA_ERR_INVALID_ARG
+
+
+def test_kernel_poly_constants_match_oracle():
+    """The exp2 cubic in the kernel source is the oracle's interpolant (same fp32 values)."""
+    import oracle
+    src = open(os.path.join(ROOT, "softmax_mx_block_gb300", "csrc", "fsa_attn.cu")).read()
+    body = src[src.index("float exp2_poly(float r)"):]
+    body = body[:body.index("}")]
+    lits = [float.fromhex(x[:-1]) for x in re.findall(r"0x1\.[0-9a-f]+p-?\d+f", body)]
+    c = oracle.exp2_poly_coeffs()
+    assert sorted(lits) == sorted(float(x) for x in c[1:])

@@ -1,0 +1,190 @@
+"""Parity of the fused MX attention kernel (fsa_attention_fwd_ex) and the BF16
+kernel (fsa_attention_fwd_bf16) with the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from workloads import WORKLOADS, Workload, generate, sample_rows, small, to_bf16_bits
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
+SPLIT_MASK = 0x55555555          # even key positions use the hardware exp2
+TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
+
+
+def _fsa():
+    import softmax_mx_block_gb300 as fsa
+    return fsa
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def run_mx(w: Workload, q, k, v, exp_mode=2, delta=0.0, row_fb=False, **kw):
+    fsa = _fsa()
+    fq, fp = FMT[w.fmt_qk], FMT[w.fmt_pv]
+    fv = 2 if fp == 3 else fp
+    mq = fsa.fsa_mx_quantize(_dev(q), fsa.FSA_MX_ROWS, fq)
+    mk = fsa.fsa_mx_quantize(_dev(k), fsa.FSA_MX_ROWS, fq)
+    mv = fsa.fsa_mx_quantize(_dev(v), fsa.FSA_MX_COLS_T, fv)
+    stats = fsa.new_stats()
+    rf = torch.zeros((w.B, w.H, w.Sq), dtype=torch.int32, device="cuda") if row_fb else None
+    out = fsa.fsa_attention_fwd(mq, mk, mv, causal=w.causal, scale=w.scale, fmt_qk=fq, fmt_pv=fp,
+                                exp_mode=exp_mode, delta=delta, row_fallbacks=rf, stats=stats, **kw)
+    torch.cuda.synchronize()
+    res = dict(out=out.cpu().numpy().reshape(-1, w.D), stats=fsa.read_stats(stats))
+    if row_fb:
+        res["row_fallbacks"] = rf.cpu().numpy().reshape(-1)
+    return res
+
+
+def oracle_mx(w, q, k, v, rows, mask, delta=0.0, with_floor=True):
+    fq, fp = FMT[w.fmt_qk], FMT[w.fmt_pv]
+    fv = 2 if fp == 3 else fp
+    mx = oracle.MxInputs.from_bf16(q, k, v, fq, fv)
+    emu = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=delta, mufu_mask=mask)
+    res = dict(emu=emu["out"], fallbacks=emu["fallbacks"], tiles=emu["tiles"])
+    if with_floor:
+        res["floor"] = oracle.attn_floor(mx, w.Sk, w.causal, w.scale, fv, rows)
+        res["exact"] = oracle.attn_exact(q, k, v, w.causal, w.scale, rows)
+    return res
+
+
+def rel_err(a, ref):
+    return np.linalg.norm(a - ref) / np.linalg.norm(ref)
+
+
+def check(w, gpu, orc, rows, floor_ratio=1.1):
+    o = gpu["out"][rows]
+    emu = orc["emu"]
+    rms = np.sqrt(np.mean(emu ** 2))
+    err = np.abs(o - emu).max() / rms
+    assert err <= TOL_EMU, f"{w.name}: max|O-O_emu|/rms = {err:.3e}"
+    if "exact" in orc and floor_ratio is not None:
+        e_gpu, e_floor = rel_err(o, orc["exact"]), rel_err(orc["floor"], orc["exact"])
+        assert e_gpu <= floor_ratio * e_floor, f"{w.name}: error {e_gpu:.4f} vs floor {e_floor:.4f}"
+    assert gpu["stats"]["status"] == 0
+
+
+def test_tiny_config_all_rows():
+    w = WORKLOADS["tiny"]
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v)
+    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK)
+    check(w, gpu, orc, rows)
+    assert gpu["stats"]["fallback_events"] == int(orc["fallbacks"].sum())
+    assert gpu["stats"]["row_tiles"] == int(orc["tiles"].sum())
+
+
+PAIRS = [("E4M3", "E4M3"), ("E2M3", "E2M1"), ("E2M1", "E2M1_EFQ"), ("E2M3", "E2M3"), ("E2M1", "E2M1"),
+         ("E4M3", "E2M1"), ("E2M1", "E4M3")]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("fq,fp", PAIRS)
+def test_small_formats(fq, fp, D, causal):
+    w = Workload(f"small_{fq}_{fp}_{D}_{int(causal)}", 1, 4, 2, 300, 300, D, causal, fq, fp, 5)
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v, row_fb=True)
+    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK)
+    ratio = 2.0 if fp == "E2M1_EFQ" else 1.1
+    check(w, gpu, orc, rows, ratio)
+    assert np.array_equal(gpu["row_fallbacks"][rows], orc["fallbacks"])
+
+
+@pytest.mark.parametrize("exp_mode,mask", [(0, 0), (1, 0xFFFFFFFF), (2, SPLIT_MASK)])
+def test_exp_modes(exp_mode, mask):
+    w = small(WORKLOADS["prefill"], 384, H=4, Hkv=2)
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v, exp_mode=exp_mode)
+    check(w, gpu, oracle_mx(w, q, k, v, rows, mask), rows)
+
+
+def test_rectangular_causal_and_empty_rows():
+    # Sq > Sk with causal bottom-right alignment: the first Sq - Sk queries see no key
+    w = Workload("rect", 1, 2, 1, 300, 200, 128, True, "E4M3", "E4M3", 9)
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v)
+    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK, with_floor=False)
+    empty = [r for r in rows if (r % w.Sq) < w.Sq - w.Sk]
+    assert np.all(gpu["out"][empty] == 0.0)
+    check(w, gpu, orc, rows)
+
+
+def test_fallback_counts_adversarial_small():
+    w = small(WORKLOADS["adversarial"], 1024, H=3, B=1)
+    for layer in (0, 1):
+        wl = w.layer(layer)
+        q, k, v = generate(wl)
+        rows = sample_rows(wl)
+        gpu = run_mx(wl, q, k, v, row_fb=True)
+        orc = oracle_mx(wl, q, k, v, rows, SPLIT_MASK, with_floor=False)
+        check(wl, gpu, orc, rows)
+        fb_gpu = gpu["row_fallbacks"][rows]
+        assert orc["fallbacks"].sum() > 0
+        # the decision compares fp32 scores; allow rare one-ulp ties to differ
+        assert np.mean(fb_gpu != orc["fallbacks"]) < 0.01
+        assert gpu["stats"]["fallback_events"] == int(gpu["row_fallbacks"].sum())
+
+
+def test_margin_delta():
+    w = small(WORKLOADS["adversarial"], 512, H=2, B=1).layer(0)
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v, delta=6.0, row_fb=True)
+    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK, delta=6.0, with_floor=False)
+    check(w, gpu, orc, rows)
+
+
+def test_inject_stall_times_out_and_context_survives():
+    fsa = _fsa()
+    w = WORKLOADS["tiny"]
+    q, k, v = generate(w)
+    gpu = run_mx(w, q, k, v, inject_stall=True, timeout_ms=50)
+    assert gpu["stats"]["status"] == fsa.FSA_ERR_TIMEOUT
+    again = run_mx(w, q, k, v)
+    assert again["stats"]["status"] == 0 and np.isfinite(again["out"]).all()
+
+
+# ----------------------------------------------------------------------------- BF16 kernel
+def run_bf16(w, q, k, v):
+    fsa = _fsa()
+    vt = fsa.fsa_bf16_transpose_v(_dev(v))
+    stats = fsa.new_stats()
+    out = fsa.fsa_attention_fwd_bf16(_dev(q), _dev(k), vt, causal=w.causal, scale=w.scale, stats=stats)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().reshape(-1, w.D), fsa.read_stats(stats)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_kernel(D, causal):
+    w = Workload("bf16", 1, 4, 2, 300, 300, D, causal, "E4M3", "E4M3", 7)
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    out, st = run_bf16(w, q, k, v)
+    emu = oracle.bf16_emulate(q, k, v, causal, w.scale, rows)["out"]
+    ex = oracle.attn_exact(q, k, v, causal, w.scale, rows)
+    o = out[rows]
+    assert np.abs(o - emu).max() / np.sqrt(np.mean(emu ** 2)) < 5e-3
+    assert rel_err(o, ex) < 1e-2
+    assert st["status"] == 0
+
+
+def test_bf16_transpose_v():
+    fsa = _fsa()
+    v = to_bf16_bits(np.random.default_rng(2).standard_normal((2, 3, 200, 64)).astype(np.float32))
+    vt = fsa.fsa_bf16_transpose_v(_dev(v))
+    torch.cuda.synchronize()
+    got = vt.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert got.shape == (2, 3, 64, 256)
+    np.testing.assert_array_equal(got[..., :200], np.swapaxes(v, 2, 3))
+    assert not got[..., 200:].any()

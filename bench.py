@@ -1,0 +1,301 @@
+"""Benchmark of the fused MX attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+MX quantisation of Q, K and V (fsa_mx_quantize) and the fused attention
+forward (fsa_attention_fwd_ex).  The metric is attention forward TFLOP/s
+(4*B*H*Sq*Sk*D per layer, halved for causal).  Inputs are resident in HBM when
+the timed region starts; L2 is flushed (a 512 MB write) between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+(the forward needs no exchange between GPUs): value = all ranks' FLOPs / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, Workload, generate, sample_rows  # noqa: E402
+
+DEFAULT_WORKLOAD = "prefill"
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
+# nominal dense ratio of each block-scaled kind to BF16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s)
+KIND_RATIO = {"E4M3": 2.0, "E2M3": 2.0, "E2M1": 6.0, "E2M1_EFQ": 6.0}
+# DRAM bytes per attention launch from an ncu capture of the current kernel build,
+# by workload (profiles/); absent until captured.
+TRAFFIC = {}
+
+
+def metric_name():
+    return "attention fwd TFLOP/s (MXFP8/MXFP4) and % of block-scaled tensor-core peak"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def peak_for(w: Workload):
+    """Dense block-scaled peak for the workload's formats (harmonic mix of the QK and PV kinds)."""
+    bf16, _, src = peaks()
+    pq, pp = bf16 * KIND_RATIO[w.fmt_qk], bf16 * KIND_RATIO[w.fmt_pv]
+    return 1.0 / (0.5 / pq + 0.5 / pp), src
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        rows = [r for r in self.rows if len(r) >= 9]
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, w: Workload, world):
+    import torch
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import empty_mx
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    fsa.load()
+    layers = [w.layer(l) for l in range(w.layers)] if w.layers > 1 else [w]
+    host, inputs, bufs = [], [], []
+    for wl in layers:
+        q, k, v = generate(wl)
+        hs = tuple(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in (q, k, v))
+        host.append(hs)
+        inputs.append(tuple(t.to(dev) for t in hs))
+        fq, fp = FMT[wl.fmt_qk], FMT[wl.fmt_pv]
+        fv = 2 if fp == 3 else fp
+        bufs.append((empty_mx(wl.B, wl.H, wl.Sq, wl.D, 0, fq, dev), empty_mx(wl.B, wl.Hkv, wl.Sk, wl.D, 0, fq, dev),
+                     empty_mx(wl.B, wl.Hkv, wl.Sk, wl.D, 1, fv, dev),
+                     torch.empty((wl.B, wl.H, wl.Sq, wl.D), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.current_stream()
+    stats = fsa.new_stats(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    attn_ev = []
+
+    def step(record=False):
+        for wl, (qd, kd, vd), (mq, mk, mv, out) in zip(layers, inputs, bufs):
+            fq, fp = FMT[wl.fmt_qk], FMT[wl.fmt_pv]
+            fsa.fsa_mx_quantize(qd, 0, fq, out=mq)
+            fsa.fsa_mx_quantize(kd, 0, fq, out=mk)
+            fsa.fsa_mx_quantize(vd, 1, 2 if fp == 3 else fp, out=mv)
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            fsa.fsa_attention_fwd(mq, mk, mv, out, causal=wl.causal, scale=wl.scale, fmt_qk=fq, fmt_pv=fp,
+                                  stats=stats)
+            if record:
+                e1.record(stream)
+                attn_ev.append((e0, e1))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stats.zero_()
+    clk = ClockSampler(dev.index)
+    clk.start()
+    barrier()
+    total_ms = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1.0)                      # evict L2 between timed steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(record=True)
+        e1.record(stream)
+        e1.synchronize()
+        total_ms += e0.elapsed_time(e1)
+    barrier()
+    clocks = clk.stop()
+    st = fsa.read_stats(stats)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+
+    # end to end through the public API: pinned host inputs -> device, quantise, attend, output -> host
+    out_host = [torch.empty(b[3].shape, dtype=torch.float32).pin_memory() for b in bufs]
+    n_e2e = max(1, min(args.steps, 5))
+    e2e_ms = 0.0
+    for _ in range(n_e2e):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for hs, ds in zip(host, inputs):
+            for h_, d_ in zip(hs, ds):
+                d_.copy_(h_, non_blocking=True)
+        step()
+        for oh, b in zip(out_host, bufs):
+            oh.copy_(b[3], non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= n_e2e
+    h2d = sum(t.numel() * 2 for hs in host for t in hs)
+    d2h = sum(b[3].numel() * 4 for b in bufs)
+
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    return dict(ms=ms, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks, stats=st,
+                launches=args.steps * 4 * len(layers))
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def run_oracle_sample(w: Workload, budget_s=15.0):
+    """The oracle's step-by-step emulation on a bounded sample of query rows, timed on
+    the host cores; returns (TFLOP/s-equivalent, description, threads)."""
+    import oracle
+    wl = w.layer(0) if w.layers > 1 else w
+    q, k, v = generate(wl)
+    fp = FMT[wl.fmt_pv]
+    mx = oracle.MxInputs.from_bf16(q, k, v, FMT[wl.fmt_qk], 2 if fp == 3 else fp)
+    rows_all = np.random.default_rng(0).permutation(sample_rows(wl, per_head=256))
+    threads = oracle.nthreads_default()
+    n, t_used, flops, done = 32, 0.0, 0.0, 0
+    while done < len(rows_all):
+        rows = np.sort(rows_all[done:done + n])
+        t0 = time.perf_counter()
+        oracle.fsa_emulate(mx, wl.Sk, wl.causal, wl.scale, fp, rows, mufu_mask=0x55555555)
+        dt = time.perf_counter() - t0
+        i = rows % wl.Sq
+        vis = np.minimum(wl.Sk, i + 1 + wl.Sk - wl.Sq) if wl.causal else np.full(len(rows), wl.Sk)
+        flops += float(np.sum(4.0 * vis * wl.D))
+        t_used += dt
+        done += len(rows)
+        if t_used > budget_s:
+            break
+        n = min(4096, n * 2)
+    desc = (f"oracle emulation (fsa_emulate, fp64 accumulation) of {done} sampled query rows of {wl.name} "
+            f"({wl.fmt_qk}/{wl.fmt_pv}) in {t_used:.1f} s; FLOPs = 4*D*visible keys per row")
+    return flops / t_used / 1e12, desc, threads
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="fsa", choices=["fsa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    flops_per_step = w.flops
+
+    config = {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+              "causal": w.causal, "fmt_qk": w.fmt_qk, "fmt_pv": w.fmt_pv, "layers": w.layers,
+              "l2": "flushed between timed steps (512 MB write)", "parallelism": f"replicas x{max(world, 1)}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, desc, threads = run_oracle_sample(w, budget_s=20.0)
+        line = {"metric": metric_name(), "value": v, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, workloads.py)", "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    r = run_gpu(args, w, world)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    value = flops_per_step * world / (r["ms"] * 1e-3) / 1e12
+    attn_tflops = flops_per_step / w.layers / (r["attn_ms"] * 1e-3) / 1e12
+    peak, src = peak_for(w)
+    rt = r["stats"]["row_tiles"]
+    line = {
+        "metric": metric_name(), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": f"mx-{w.fmt_qk.lower()}/{w.fmt_pv.lower()}",
+        "data": "synthetic (seeded, workloads.py)", "config": config,
+        "attention_kernel": {"tflops": attn_tflops, "ms_per_launch": r["attn_ms"],
+                             "frac_of_block_scaled_peak": attn_tflops / peak},
+        "fallback_rate": (r["stats"]["fallback_events"] / rt) if rt else None,
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": attn_tflops / peak, "traffic": TRAFFIC.get(w.name),
+                     "peak_source": f"{src} bf16 burst x nominal block-scaled/bf16 ratio"},
+        "e2e": {"value": flops_per_step * world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, desc, threads = run_oracle_sample(w, budget_s=15.0)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

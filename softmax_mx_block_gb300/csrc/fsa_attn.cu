@@ -99,16 +99,11 @@ __device__ __forceinline__ uint32_t pgen_block(const float* sv, float bmax, floa
       for (int w = 0; w < 8; ++w)
         out[w] = cvt_e4m3x2(pv[4 * w], pv[4 * w + 1]) | (cvt_e4m3x2(pv[4 * w + 2], pv[4 * w + 3]) << 16);
     } else if constexpr (FPV == F_E2M3) {
+      // P is read by the MMA from tensor memory, where 6-bit operands sit one per
+      // byte (the unpacked form tcgen05.cp produces from the padded shared layout)
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          w[i] = cvt_e2m3x2(pv[16 * g + 4 * i], pv[16 * g + 4 * i + 1]) |
-                 (cvt_e2m3x2(pv[16 * g + 4 * i + 2], pv[16 * g + 4 * i + 3]) << 16);
-        pack6x16(w, out + 4 * g);
-        out[4 * g + 3] = 0u;
-      }
+      for (int w = 0; w < 8; ++w)
+        out[w] = cvt_e2m3x2(pv[4 * w], pv[4 * w + 1]) | (cvt_e2m3x2(pv[4 * w + 2], pv[4 * w + 3]) << 16);
     } else {
 #pragma unroll
       for (int w = 0; w < 4; ++w)

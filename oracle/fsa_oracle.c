@@ -478,9 +478,11 @@ float orc_exp2_poly(float r) {
 /* visible key for the row are skipped; they contribute nothing):               */
 /*  1. s_j = fp32(exact dot(q_hat, k_hat_j))            (raw score, fp32)        */
 /*  2. mx = max visible s_j;  x = fp32(mx * c), c = fp32(scale * log2 e)         */
-/*  3. first tile: M = x + delta (frozen max, log2 units)                        */
-/*     later tile: if x > M: fallback: M' = x + delta, alpha = 2^(M - M'),       */
+/*  3. first tile: M = x (frozen max, log2 units)                                */
+/*     later tile: if x > fp32(M + delta): fallback: M' = x, alpha = 2^(M - M'), */
 /*                 O_acc *= alpha, l *= alpha, M = M', count++                   */
+/*     (delta >= 0 is a margin on the fallback test only; M itself stays a      */
+/*     rounded score product, so the block holding it has tmax = 0 exactly)     */
 /*  4. per 32-key block: smax = max visible s; tmax = fp32(fp32(smax*c) - M);   */
 /*     E = clamp(floor(tmax) - emax, -127, 127); bE = fp32(M + E);               */
 /*     r_j = fmaf(s_j, c, -bE)  (residual: shifted log2 score minus E)           */
@@ -495,7 +497,7 @@ float orc_exp2_poly(float r) {
 /* fmt_p: 0 E4M3, 1 E2M3, 2 E2M1, 3 E2M1 by the EFQ rule.                        */
 /* ------------------------------------------------------------------------- */
 typedef struct {
-  float delta;        /* frozen-max margin, log2 units (default 0) */
+  float delta;        /* fallback margin, log2 units: fall back when x > M + delta */
   uint32_t mufu_mask; /* per position in a 32-block: 1 = hardware exp2 model */
   int beta;           /* EFQ affine offset (default 2) */
 } orc_fsa_opts;
@@ -569,10 +571,10 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
           }
           float x = mx * c;
           if (!M_set) {
-            M = x + opt->delta;
+            M = x;
             M_set = 1;
-          } else if (x > M) {
-            float Mn = x + opt->delta;
+          } else if (x > M + opt->delta) {
+            float Mn = x;
             double alpha = exp2((double)(M - Mn));
             for (int d = 0; d < D; ++d) o[d] *= alpha;
             l *= alpha;

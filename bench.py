@@ -18,7 +18,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -61,46 +60,59 @@ def peak_for(w: Workload):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled every millisecond through NVML
+    (libnvidia-ml, read-only queries) while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index=0):
-        self.index, self.rows, self.proc = index, [], None
+    def __init__(self, pci_bus_id=None):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._thread = None
+        self.nvml = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            ok = False
+            if pci_bus_id:
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) == 0
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) == 0
+            if ok:
+                self.nvml, self.h, self.ct = nv, h, ctypes
+                mx = ctypes.c_uint()
+                if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                    self.max_mhz = float(mx.value)
+        except OSError:
+            self.nvml = None
+
+    def _poll(self):
+        ct, nv, h = self.ct, self.nvml, self.h
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if get_reasons(h, ct.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(0.001)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            threading.Thread(target=self._read, daemon=True).start()
-        except OSError:
-            self.proc = None
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.rows.append([x.strip() for x in line.split(",")])
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
 
     def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        rows = [r for r in self.rows if len(r) >= 9]
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(sm)}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        reasons = sorted(n for b, n in self.REASONS.items() if self.reasons & b)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -139,7 +151,7 @@ def run_gpu(args, w: Workload, world):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
             fsa.fsa_attention_fwd(mq, mk, mv, out, causal=wl.causal, scale=wl.scale, fmt_qk=fq, fmt_pv=fp,
-                                  stats=stats)
+                                  stats=stats, exp_mode=args.exp_mode)
             if record:
                 e1.record(stream)
                 attn_ev.append((e0, e1))
@@ -153,7 +165,12 @@ def run_gpu(args, w: Workload, world):
         step()
     torch.cuda.synchronize()
     stats.zero_()
-    clk = ClockSampler(dev.index)
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+        bus = f"{torch.cuda.get_device_properties(dev).pci_domain_id:08x}:{bus:02x}:{torch.cuda.get_device_properties(dev).pci_device_id:02x}.0"
+    except Exception:
+        bus = None
+    clk = ClockSampler(bus)
     clk.start()
     barrier()
     total_ms = 0.0
@@ -191,13 +208,28 @@ def run_gpu(args, w: Workload, world):
     h2d = sum(t.numel() * 2 for hs in host for t in hs)
     d2h = sum(b[3].numel() * 4 for b in bufs)
 
+    # the in-house BF16 exact-softmax kernel on the same inputs (speedup reference)
+    vts = [fsa.fsa_bf16_transpose_v(ds[2]) for ds in inputs]
+    out_bf = [torch.empty_like(b[3]) for b in bufs]
+    bf_ms = []
+    for it in range(args.warmup + max(3, min(args.steps, 10))):
+        for wl, (qd, kd, _), vt, ob in zip(layers, inputs, vts, out_bf):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fsa.fsa_attention_fwd_bf16(qd, kd, vt, ob, causal=wl.causal, scale=wl.scale)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                bf_ms.append(e0.elapsed_time(e1))
+
     ms = total_ms / args.steps
     if world > 1:
         t = torch.tensor([ms, e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms, e2e_ms = float(t[0]), float(t[1])
     return dict(ms=ms, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks, stats=st,
-                launches=args.steps * 4 * len(layers))
+                launches=args.steps * 4 * len(layers), bf16_ms=statistics.mean(bf_ms))
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
@@ -215,7 +247,7 @@ def run_oracle_sample(w: Workload, budget_s=15.0):
     while done < len(rows_all):
         rows = np.sort(rows_all[done:done + n])
         t0 = time.perf_counter()
-        oracle.fsa_emulate(mx, wl.Sk, wl.causal, wl.scale, fp, rows, mufu_mask=0x55555555)
+        oracle.fsa_emulate(mx, wl.Sk, wl.causal, wl.scale, fp, rows, delta=8.0, mufu_mask=0x77777777)
         dt = time.perf_counter() - t0
         i = rows % wl.Sq
         vis = np.minimum(wl.Sk, i + 1 + wl.Sk - wl.Sq) if wl.causal else np.full(len(rows), wl.Sk)
@@ -239,6 +271,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="fsa", choices=["fsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--exp-mode", type=int, default=2, choices=[0, 1, 2],
+                    help="0 cubic, 1 ex2.approx, 2 split (default)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
@@ -248,7 +282,7 @@ def main():
 
     config = {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
               "causal": w.causal, "fmt_qk": w.fmt_qk, "fmt_pv": w.fmt_pv, "layers": w.layers,
-              "l2": "flushed between timed steps (512 MB write)", "parallelism": f"replicas x{max(world, 1)}"}
+              "l2": "flushed between timed steps (512 MB write)", "exp_mode": args.exp_mode, "parallelism": f"replicas x{max(world, 1)}"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -282,6 +316,9 @@ def main():
         "data": "synthetic (seeded, workloads.py)", "config": config,
         "attention_kernel": {"tflops": attn_tflops, "ms_per_launch": r["attn_ms"],
                              "frac_of_block_scaled_peak": attn_tflops / peak},
+        "bf16_kernel": {"tflops": flops_per_step / w.layers / (r["bf16_ms"] * 1e-3) / 1e12,
+                        "ms_per_launch": r["bf16_ms"]},
+        "speedup_vs_bf16": r["bf16_ms"] / r["attn_ms"],
         "fallback_rate": (r["stats"]["fallback_events"] / rt) if rt else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak, "traffic": TRAFFIC.get(w.name),

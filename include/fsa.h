@@ -107,11 +107,13 @@ int fsa_mx_quantize(const void* x_bf16, int B, int H, int S, int D, int layout, 
 typedef enum {
   FSA_EXP_POLY = 0,   /* cubic interpolant of 2^f on the FMA pipe for every element */
   FSA_EXP_MUFU = 1,   /* hardware ex2.approx for every element */
-  FSA_EXP_SPLIT = 2   /* even key positions ex2.approx, odd positions the cubic */
+  FSA_EXP_SPLIT = 2   /* key positions 4k+3 (of each 32-key block) the cubic, the others ex2.approx */
 } fsa_exp_mode;
 
 typedef struct {
-  float    delta;        /* frozen-max margin in log2 units (default 0) */
+  float    delta;        /* fallback margin in log2 units (default 8): a later tile falls back
+                            only when its maximum exceeds the frozen one by more than delta;
+                            per-block scales make a stale maximum cost no precision */
   int32_t  exp_mode;     /* fsa_exp_mode (default FSA_EXP_SPLIT) */
   int32_t  efq_beta;     /* integer offset of the EFQ rule code = rne(2 r + beta) (default 2) */
   uint32_t timeout_ms;   /* limit of each on-chip wait (0: 4000 ms) */
@@ -133,8 +135,8 @@ void fsa_default_opts(fsa_opts* opts);
 /* ------------------------------------------------------------- attention */
 /* O[B][H][Sq][D] fp32 = softmax(scale * Q K^T) V computed by the fused MX
  * algorithm: QK^T as a block-scaled MMA into tensor memory; the row maximum
- * frozen from the first key tile of 128 (plus delta), with a fallback that
- * rescales the accumulator when a later tile's maximum exceeds it; per
+ * frozen from the first key tile of 128, with a fallback that rescales the
+ * accumulator when a later tile's maximum exceeds it by more than delta; per
  * 32-key block an exponent-only scale from the block maximum and codes by
  * exp-then-round (fmt_pv E4M3/E2M3/E2M1) or the EFQ rule (E2M1_EFQ);
  * P~ [V^|1] as a block-scaled MMA whose extra ones column accumulates the

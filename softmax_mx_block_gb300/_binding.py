@@ -165,7 +165,7 @@ def read_stats(stats: torch.Tensor) -> dict:
 
 
 def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
-                      causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=0.0, exp_mode=FSA_EXP_SPLIT,
+                      causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=None, exp_mode=FSA_EXP_SPLIT,
                       efq_beta=2, timeout_ms=0, row_fallbacks: torch.Tensor | None = None, stats=None,
                       inject_stall=False, stream=None) -> torch.Tensor:
     """O [B,H,Sq,D] fp32 by the fused MX forward (fsa_attention_fwd_ex)."""
@@ -179,7 +179,11 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
         out = torch.empty((B, H, Sq, D), dtype=torch.float32, device=q.codes.device)
     _need_cuda(out, "out", torch.float32)
     o = default_opts()
-    o.delta, o.exp_mode, o.efq_beta, o.timeout_ms = float(delta), int(exp_mode), int(efq_beta), int(timeout_ms)
+    if delta is not None:
+        o.delta = float(delta)
+    o.exp_mode, o.efq_beta = int(exp_mode), int(efq_beta)
+    if timeout_ms:
+        o.timeout_ms = int(timeout_ms)
     o.inject_stall = int(bool(inject_stall))
     if row_fallbacks is not None:
         _need_cuda(row_fallbacks, "row_fallbacks", torch.int32)

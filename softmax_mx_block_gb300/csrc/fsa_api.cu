@@ -100,7 +100,7 @@ extern "C" {
 void fsa_default_opts(fsa_opts* o) {
   if (!o) return;
   std::memset(o, 0, sizeof(*o));
-  o->delta = 0.0f;
+  o->delta = 8.0f;
   o->exp_mode = FSA_EXP_SPLIT;
   o->efq_beta = 2;
   o->timeout_ms = 4000;

@@ -16,8 +16,8 @@
 //
 // Per query row and key tile of 128 (ascending), with s the raw fp32 score and
 // c = fp32(scale * log2 e):
-//   mx = tile max, x = fp32(mx*c); first tile: M = x + delta; later: x > M ->
-//   fallback: O_aug *= 2^(M - M'), M' = x + delta.
+//   mx = tile max, x = fp32(mx*c); first tile: M = x; later: x > fp32(M + delta)
+//   -> fallback: O_aug *= 2^(M - M'), M' = x (delta: margin of the fallback test).
 //   per 32-key block: E = clamp(floor(fp32(fp32(smax*c) - M)) - emax, -127, 127),
 //   r = fma(s, c, -fp32(M + E)); code = RN(exp2approx(r)) in the P format, or
 //   EFQ: code = clamp(rne(2 r + beta), 0, 7); scale byte E + 127.
@@ -39,29 +39,111 @@ namespace fsa {
 
 constexpr float kNegInf = -__builtin_huge_valf();
 
+// ---- packed fp32 pairs (f32x2 FMA-pipe ops on sm_100-family) ------------------
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2_rm(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// max of 32 consecutive values (16 three-input max operations)
+__device__ __forceinline__ float max32(const float* v) {
+  float m0 = max3f(v[0], v[1], v[2]), m1 = max3f(v[3], v[4], v[5]), m2 = max3f(v[6], v[7], v[8]);
+  float m3 = max3f(v[9], v[10], v[11]), m4 = max3f(v[12], v[13], v[14]), m5 = max3f(v[15], v[16], v[17]);
+  float m6 = max3f(v[18], v[19], v[20]), m7 = max3f(v[21], v[22], v[23]), m8 = max3f(v[24], v[25], v[26]);
+  float m9 = max3f(v[27], v[28], v[29]);
+  m0 = max3f(m0, m1, m2);
+  m3 = max3f(m3, m4, m5);
+  m6 = max3f(m6, m7, m8);
+  m9 = max3f(m9, v[30], v[31]);
+  return fmaxf(max3f(m0, m3, m6), m9);
+}
+
 // Cubic through 2^f at f = 0, 1/3, 2/3, 1 (coefficients solved in fp64 from the
 // four nodes and rounded to fp32), Horner with fused multiply-adds; 2^n by
-// exponent addition after clamping r below at -64.
-__device__ __forceinline__ float exp2_poly(float r) {
-  const float rc = fmaxf(r, -64.0f);
-  const float n = floorf(rc);
-  const float f = __fsub_rn(rc, n);
-  float p = __fmaf_rn(0x1.43aa72p-4f, f, 0x1.ccca58p-3f);
-  p = __fmaf_rn(p, f, 0x1.64581cp-1f);
-  p = __fmaf_rn(p, f, 1.0f);
-  return __int_as_float(__float_as_int(p) + ((int)n << 23));
+// exponent addition after clamping r below at -64.  Two values at a time:
+// floor(r) comes from adding 1.5*2^23 rounded toward -inf (exact for
+// |r| < 2^22), f = r - floor(r) is exact, and 2^n is one integer multiply-add
+// on the exponent field.
+constexpr float kC3 = 0x1.43aa72p-4f, kC2 = 0x1.ccca58p-3f, kC1 = 0x1.64581cp-1f;
+__device__ __forceinline__ void exp2_poly2(float& a, float& b) {
+  const uint64_t r = pk2(fmaxf(a, -64.0f), fmaxf(b, -64.0f));
+  const uint64_t j = fadd2_rm(r, pk2(12582912.0f, 12582912.0f));           // floor(r) + 1.5*2^23
+  const uint64_t n = ffma2(j, pk2(1.0f, 1.0f), pk2(-12582912.0f, -12582912.0f));
+  const uint64_t f = ffma2(n, pk2(-1.0f, -1.0f), r);                         // r - floor(r), exact
+  uint64_t p = ffma2(pk2(kC3, kC3), f, pk2(kC2, kC2));
+  p = ffma2(p, f, pk2(kC1, kC1));
+  p = ffma2(p, f, pk2(1.0f, 1.0f));
+  float p0, p1, j0, j1;
+  upk2(p, p0, p1);
+  upk2(j, j0, j1);
+  // (bits(j) - bits(1.5*2^23)) << 23 == bits(j) << 23 (mod 2^32): the magic's low 9 bits are 0
+  a = __int_as_float(__float_as_int(p0) + (__float_as_int(j0) << 23));
+  b = __int_as_float(__float_as_int(p1) + (__float_as_int(j1) << 23));
 }
 
+// exp2 of 32 residuals in place.  EXPM 0: all by the cubic; 1: all by ex2.approx;
+// 2: key positions 4k+3 by the cubic, the others by ex2.approx.
 template <int EXPM>
-__device__ __forceinline__ float exp2_sel(float r, int pos) {
-  if constexpr (EXPM == 0) return exp2_poly(r);
-  else if constexpr (EXPM == 1) return ex2_approx(r);
-  else return (pos & 1) ? exp2_poly(r) : ex2_approx(r);
+__device__ __forceinline__ void exp2_block(float* v) {
+  if constexpr (EXPM == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) exp2_poly2(v[i], v[i + 1]);
+  } else if constexpr (EXPM == 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = ex2_approx(v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      exp2_poly2(v[i + 3], v[i + 7]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if ((e & 3) != 3) v[i + e] = ex2_approx(v[i + e]);
+    }
+  }
 }
 
-// P codes of one 32-key block (values sv[0..31], raw scores, masked = -inf),
-// written as packed words into out[] (8 words for 8-bit storage, 4 for E2M1).
-// Returns the scale byte.
+__device__ __forceinline__ uint32_t pack_b16x2(uint16_t lo, uint16_t hi) {
+  uint32_t r;
+  asm("mov.b32 %0, {%1, %2};" : "=r"(r) : "h"(lo), "h"(hi));
+  return r;
+}
+__device__ __forceinline__ uint16_t cvt16_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t cvt16_e2m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// P codes of one 32-key block (raw scores sv[0..31], masked = -inf), written as
+// packed words into out[] (8 words for one byte per code, 4 for E2M1).  Returns
+// the scale byte.  r = fma(s, c, -fp32(M + E)) two at a time.
 template <int FPV, int EXPM>
 __device__ __forceinline__ uint32_t pgen_block(const float* sv, float bmax, float c, float M, int beta, uint32_t* out) {
   constexpr int emax = Fmt<FPV>::emax;
@@ -75,40 +157,49 @@ __device__ __forceinline__ uint32_t pgen_block(const float* sv, float bmax, floa
   int E = (int)floorf(tmax) - emax;
   E = E < -127 ? -127 : (E > 127 ? 127 : E);
   const float nbE = -__fadd_rn(M, (float)E);
+  const uint64_t c2 = pk2(c, c), nb2 = pk2(nbE, nbE);
+  float r[32];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) upk2(ffma2(pk2(sv[i], sv[i + 1]), c2, nb2), r[i], r[i + 1]);
   if constexpr (FPV == F_EFQ) {
-    const float magic = 12582912.0f;                    // 1.5 * 2^23: integer grid
-    const float kb = magic + (float)beta;               // exact for small integer beta
+    // k = clamp(rne(2 r + beta), 0, 7): fma onto the integer grid of 1.5*2^23, whose
+    // low bits then hold k; four nibbles pair up by shift-add, bytes merge by permute
+    const float magic = 12582912.0f;
+    const uint64_t two2 = pk2(2.0f, 2.0f), kb2 = pk2(magic + (float)beta, magic + (float)beta);
+    uint32_t y[32];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float y0, y1;
+      upk2(ffma2(two2, pk2(r[i], r[i + 1]), kb2), y0, y1);
+      y[i] = __float_as_uint(fminf(fmaxf(y0, magic), magic + 7.0f));
+      y[i + 1] = __float_as_uint(fminf(fmaxf(y1, magic), magic + 7.0f));
+    }
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      uint32_t word = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float r = __fmaf_rn(sv[8 * w + e], c, nbE);
-        float y = __fmaf_rn(2.0f, r, kb);               // magic + rne(2 r + beta)
-        y = fminf(fmaxf(y, magic), magic + 7.0f);
-        word |= (uint32_t)(__float_as_int(y) - 0x4B400000) << (4 * e);
-      }
-      out[w] = word;
+      const uint32_t* t = y + 8 * w;
+      // low byte of (t1 << 4) + t0 is k0 | k1 << 4 (the magic's bits stay above bit 21)
+      const uint32_t a01 = (t[1] << 4) + t[0], a23 = (t[3] << 4) + t[2];
+      const uint32_t a45 = (t[5] << 4) + t[4], a67 = (t[7] << 4) + t[6];
+      out[w] = prmt(prmt(a01, a23, 0x0040u), prmt(a45, a67, 0x0040u), 0x5410u);
     }
   } else {
-    float pv[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) pv[i] = exp2_sel<EXPM>(__fmaf_rn(sv[i], c, nbE), i);
+    exp2_block<EXPM>(r);
     if constexpr (FPV == F_E4M3) {
 #pragma unroll
       for (int w = 0; w < 8; ++w)
-        out[w] = cvt_e4m3x2(pv[4 * w], pv[4 * w + 1]) | (cvt_e4m3x2(pv[4 * w + 2], pv[4 * w + 3]) << 16);
+        out[w] = pack_b16x2(cvt16_e4m3x2(r[4 * w], r[4 * w + 1]), cvt16_e4m3x2(r[4 * w + 2], r[4 * w + 3]));
     } else if constexpr (FPV == F_E2M3) {
-      // P is read by the MMA from tensor memory, where 6-bit operands sit one per
-      // byte (the unpacked form tcgen05.cp produces from the padded shared layout)
+      // tensor memory holds 6-bit A operands one per byte (low 6 bits)
 #pragma unroll
       for (int w = 0; w < 8; ++w)
-        out[w] = cvt_e2m3x2(pv[4 * w], pv[4 * w + 1]) | (cvt_e2m3x2(pv[4 * w + 2], pv[4 * w + 3]) << 16);
+        out[w] = pack_b16x2(cvt16_e2m3x2(r[4 * w], r[4 * w + 1]), cvt16_e2m3x2(r[4 * w + 2], r[4 * w + 3]));
     } else {
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-        out[w] = cvt_e2m1x2(pv[8 * w], pv[8 * w + 1]) | (cvt_e2m1x2(pv[8 * w + 2], pv[8 * w + 3]) << 8) |
-                 (cvt_e2m1x2(pv[8 * w + 4], pv[8 * w + 5]) << 16) | (cvt_e2m1x2(pv[8 * w + 6], pv[8 * w + 7]) << 24);
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t b01 = cvt_e2m1x2(r[8 * w], r[8 * w + 1]), b23 = cvt_e2m1x2(r[8 * w + 2], r[8 * w + 3]);
+        const uint32_t b45 = cvt_e2m1x2(r[8 * w + 4], r[8 * w + 5]), b67 = cvt_e2m1x2(r[8 * w + 6], r[8 * w + 7]);
+        out[w] = prmt(prmt(b01, b23, 0x0040u), prmt(b45, b67, 0x0040u), 0x5410u);
+      }
     }
   }
   return (uint32_t)(E + 127);
@@ -353,15 +444,15 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_ld_cols<64>(tl + C::T_S + 128 * s + 64 * hh, raw);
         tc_wait_ld();
         const int kbase = 128 * j + 64 * hh;
-        const bool need_mask = kbase + 63 > lim;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float x = __uint_as_float(raw[i]);
-          if (need_mask && kbase + i > lim) x = kNegInf;
-          sv[i] = x;
+        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(raw[i]);
+        if (kbase + 63 > lim) {                     // only diagonal / tail tiles mask keys
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (kbase + i > lim) sv[i] = kNegInf;
         }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) { bm0 = fmaxf(bm0, sv[i]); bm1 = fmaxf(bm1, sv[32 + i]); }
+        bm0 = max32(sv);
+        bm1 = max32(sv + 32);
       }
       // exchange the half maxima of this row with the other warpgroup (NaN = this side failed)
       red[(s * 2 + hh) * 128 + rl] = got ? fmaxf(bm0, bm1) : __int_as_float(0x7FC00000);
@@ -375,10 +466,10 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (mx != kNegInf) {
         ++nvis;
         if (M == kNegInf) {
-          M = MX ? __fadd_rn(x, p.delta) : x;
-        } else if (MX ? (x > M) : (__fsub_rn(x, M) > 8.0f)) {
+          M = x;
+        } else if (MX ? (x > __fadd_rn(M, p.delta)) : (__fsub_rn(x, M) > 8.0f)) {
           rescale = true;
-          Mn = MX ? __fadd_rn(x, p.delta) : x;
+          Mn = x;
         }
       }
       // fallback: O_aug row *= 2^(M - M') once the previous PV has landed.  tcgen05.ld/st
@@ -416,11 +507,13 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         TmemSt<1>::run(tl + C::T_SFP + 8 * s + 4 * hh + qd, &sw);
       } else {
         uint32_t pw[32];
+        const float nM = M == kNegInf ? 0.0f : -M;   // no visible key yet: every s is -inf, p = 0
+        const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float a = M == kNegInf ? 0.f : ex2_approx(__fmaf_rn(sv[2 * i], c, -M));
-          const float bb = M == kNegInf ? 0.f : ex2_approx(__fmaf_rn(sv[2 * i + 1], c, -M));
-          pw[i] = cvt_bf16x2(a, bb);
+          float a, bb;
+          upk2(ffma2(pk2(sv[2 * i], sv[2 * i + 1]), c2, nM2), a, bb);
+          pw[i] = cvt_bf16x2(ex2_approx(a), ex2_approx(bb));
         }
         tmem_st_cols<32>(tl + C::T_S + 128 * s + 64 * hh, pw);
       }

@@ -42,7 +42,7 @@ def test_sizes_and_status(lib):
         fsa.fsa_mx_sizes(1, 1, 128, 96, 0, "E4M3")
     assert fsa.status_string(fsa.FSA_ERR_TIMEOUT) == "on-chip wait timed out"
     o = fsa.default_opts()
-    assert (o.exp_mode, o.efq_beta, o.timeout_ms, o.delta) == (fsa.FSA_EXP_SPLIT, 2, 4000, 0.0)
+    assert (o.exp_mode, o.efq_beta, o.timeout_ms, o.delta) == (fsa.FSA_EXP_SPLIT, 2, 4000, 8.0)
 
 
 def test_argument_checks_reject_before_launch(lib):
@@ -77,8 +77,7 @@ def test_kernel_poly_constants_match_oracle():
     """The exp2 cubic in the kernel source is the oracle's interpolant (same fp32 values)."""
     import oracle
     src = open(os.path.join(ROOT, "softmax_mx_block_gb300", "csrc", "fsa_attn.cu")).read()
-    body = src[src.index("float exp2_poly(float r)"):]
-    body = body[:body.index("}")]
-    lits = [float.fromhex(x[:-1]) for x in re.findall(r"0x1\.[0-9a-f]+p-?\d+f", body)]
+    line = next(l for l in src.splitlines() if l.startswith("constexpr float kC3"))
+    lits = [float.fromhex(x[:-1]) for x in re.findall(r"0x1\.[0-9a-f]+p-?\d+f", line)]
     c = oracle.exp2_poly_coeffs()
     assert sorted(lits) == sorted(float(x) for x in c[1:])

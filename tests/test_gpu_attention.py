@@ -10,7 +10,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
-SPLIT_MASK = 0x55555555          # even key positions use the hardware exp2
+SPLIT_MASK = 0x77777777          # key positions 4k+3 use the cubic, the rest the hardware exp2
 TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
 
 
@@ -142,6 +142,20 @@ def test_margin_delta():
     gpu = run_mx(w, q, k, v, delta=6.0, row_fb=True)
     orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK, delta=6.0, with_floor=False)
     check(w, gpu, orc, rows)
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill", "adversarial"])
+def test_default_margin(name):
+    """The library default (frozen-max margin 8 log2 units) against the oracle at the same margin."""
+    w = WORKLOADS[name]
+    w = w if name == "tiny" else small(w, 640, H=4, Hkv=2 if name == "prefill" else None, B=1)
+    w = w.layer(1) if w.layers > 1 else w
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v, delta=None, row_fb=True)
+    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK, delta=8.0)
+    check(w, gpu, orc, rows)
+    assert np.mean(gpu["row_fallbacks"][rows] != orc["fallbacks"]) < 0.01
 
 
 def test_inject_stall_times_out_and_context_survives():

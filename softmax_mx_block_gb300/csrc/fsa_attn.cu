@@ -141,41 +141,46 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// P codes of one 32-key block (raw scores sv[0..31], masked = -inf), written as
-// packed words into out[] (8 words for one byte per code, 4 for E2M1).  Returns
-// the scale byte.  r = fma(s, c, -fp32(M + E)) two at a time.
-template <int FPV, int EXPM>
-__device__ __forceinline__ uint32_t pgen_block(const float* sv, float bmax, float c, float M, int beta, uint32_t* out) {
-  constexpr int emax = Fmt<FPV>::emax;
-  constexpr int NW = FPV == F_E2M1 || FPV == F_EFQ ? 4 : 8;
-  if (bmax == kNegInf) {
-#pragma unroll
-    for (int i = 0; i < NW; ++i) out[i] = 0u;
-    return 0u;
-  }
+// Exponent-only block scale: E = clamp(floor(fp32(fp32(smax*c) - M)) - emax, -127, 127).
+// Returns E and writes -fp32(M + E).  A block with no visible key (smax = -inf)
+// gets E = -127; its scores are -inf, so every code comes out 0.
+template <int FPV>
+__device__ __forceinline__ int block_exp(float bmax, float c, float M, float& nbE) {
   const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
-  int E = (int)floorf(tmax) - emax;
+  int E = (int)fmaxf(floorf(tmax), -256.0f) - Fmt<FPV>::emax;
   E = E < -127 ? -127 : (E > 127 ? 127 : E);
-  const float nbE = -__fadd_rn(M, (float)E);
-  const uint64_t c2 = pk2(c, c), nb2 = pk2(nbE, nbE);
-  float r[32];
+  nbE = -__fadd_rn(M, (float)E);
+  return E;
+}
+
+// P codes of one 64-key half tile (raw scores sv[0..63] as two 32-key blocks,
+// masked = -inf) as packed words in out[] (16 words for one byte per code, 8 for
+// E2M1).  Returns the two scale bytes (block 0 in the low byte).
+template <int FPV, int EXPM>
+__device__ __forceinline__ uint32_t pgen_half(const float* sv, float bm0, float bm1, float c, float M, int beta,
+                                              uint32_t* out) {
+  float nb0, nb1;
+  const int E0 = block_exp<FPV>(bm0, c, M, nb0);
+  const int E1 = block_exp<FPV>(bm1, c, M, nb1);
+  const uint64_t c2 = pk2(c, c), n0 = pk2(nb0, nb0), n1 = pk2(nb1, nb1);
+  float r[64];
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) upk2(ffma2(pk2(sv[i], sv[i + 1]), c2, nb2), r[i], r[i + 1]);
+  for (int i = 0; i < 64; i += 2) upk2(ffma2(pk2(sv[i], sv[i + 1]), c2, i < 32 ? n0 : n1), r[i], r[i + 1]);
   if constexpr (FPV == F_EFQ) {
     // k = clamp(rne(2 r + beta), 0, 7): fma onto the integer grid of 1.5*2^23, whose
-    // low bits then hold k; four nibbles pair up by shift-add, bytes merge by permute
+    // low bits then hold k; nibble pairs combine by shift-add, bytes merge by permute
     const float magic = 12582912.0f;
     const uint64_t two2 = pk2(2.0f, 2.0f), kb2 = pk2(magic + (float)beta, magic + (float)beta);
-    uint32_t y[32];
+    uint32_t y[64];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
+    for (int i = 0; i < 64; i += 2) {
       float y0, y1;
       upk2(ffma2(two2, pk2(r[i], r[i + 1]), kb2), y0, y1);
       y[i] = __float_as_uint(fminf(fmaxf(y0, magic), magic + 7.0f));
       y[i + 1] = __float_as_uint(fminf(fmaxf(y1, magic), magic + 7.0f));
     }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < 8; ++w) {
       const uint32_t* t = y + 8 * w;
       // low byte of (t1 << 4) + t0 is k0 | k1 << 4 (the magic's bits stay above bit 21)
       const uint32_t a01 = (t[1] << 4) + t[0], a23 = (t[3] << 4) + t[2];
@@ -184,25 +189,34 @@ __device__ __forceinline__ uint32_t pgen_block(const float* sv, float bmax, floa
     }
   } else {
     exp2_block<EXPM>(r);
+    exp2_block<EXPM>(r + 32);
     if constexpr (FPV == F_E4M3) {
 #pragma unroll
-      for (int w = 0; w < 8; ++w)
+      for (int w = 0; w < 16; ++w)
         out[w] = pack_b16x2(cvt16_e4m3x2(r[4 * w], r[4 * w + 1]), cvt16_e4m3x2(r[4 * w + 2], r[4 * w + 3]));
     } else if constexpr (FPV == F_E2M3) {
       // tensor memory holds 6-bit A operands one per byte (low 6 bits)
 #pragma unroll
-      for (int w = 0; w < 8; ++w)
+      for (int w = 0; w < 16; ++w)
         out[w] = pack_b16x2(cvt16_e2m3x2(r[4 * w], r[4 * w + 1]), cvt16_e2m3x2(r[4 * w + 2], r[4 * w + 3]));
     } else {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < 8; ++w) {
         const uint32_t b01 = cvt_e2m1x2(r[8 * w], r[8 * w + 1]), b23 = cvt_e2m1x2(r[8 * w + 2], r[8 * w + 3]);
         const uint32_t b45 = cvt_e2m1x2(r[8 * w + 4], r[8 * w + 5]), b67 = cvt_e2m1x2(r[8 * w + 6], r[8 * w + 7]);
         out[w] = prmt(prmt(b01, b23, 0x0040u), prmt(b45, b67, 0x0040u), 0x5410u);
       }
     }
   }
-  return (uint32_t)(E + 127);
+  return (uint32_t)(E0 + 127) | ((uint32_t)(E1 + 127) << 8);
+}
+
+// bar.red.or over `nthreads` threads of named barrier `id`: true if any predicate is set.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n barrier.red.or.pred q, %2, %3, p;\n"
+               " selp.b32 %0, 1, 0, q;\n}" : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
+  return r != 0;
 }
 
 }  // namespace fsa
@@ -454,22 +468,32 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bm0 = max32(sv);
         bm1 = max32(sv + 32);
       }
-      // exchange the half maxima of this row with the other warpgroup (NaN = this side failed)
-      red[(s * 2 + hh) * 128 + rl] = got ? fmaxf(bm0, bm1) : __int_as_float(0x7FC00000);
-      named_bar_sync(1 + qd, 64);
-      const float other = red[(s * 2 + (1 - hh)) * 128 + rl];
-      if (!got || isnan(other)) { ok = false; break; }
-      const float mx = fmaxf(fmaxf(bm0, bm1), other);
-      const float x = __fmul_rn(mx, c);
+      // The row's two halves agree on the tile maximum only when some row of the warp
+      // pair needs it: its first visible tile, a fallback (x > M + delta), or a failed
+      // wait.  The test per half is exact: rounding is monotone, so
+      // fp32(max(a,b)*c) > T  <=>  fp32(a*c) > T or fp32(b*c) > T.
+      const float hm = fmaxf(bm0, bm1);
+      const bool vis = 128 * j <= lim;               // first key of the tile visible to this row
+      const bool need = !got || (vis && (M == kNegInf ||
+                                         (MX ? (__fmul_rn(hm, c) > __fadd_rn(M, p.delta))
+                                             : (__fsub_rn(__fmul_rn(hm, c), M) > 8.0f))));
       bool rescale = false;
       float Mn = M;
-      if (mx != kNegInf) {
-        ++nvis;
-        if (M == kNegInf) {
-          M = x;
-        } else if (MX ? (x > __fadd_rn(M, p.delta)) : (__fsub_rn(x, M) > 8.0f)) {
-          rescale = true;
-          Mn = x;
+      if (vis) ++nvis;
+      if (named_bar_or(1 + qd, 64, need)) {
+        red[(s * 2 + hh) * 128 + rl] = got ? hm : __int_as_float(0x7FC00000);
+        named_bar_sync(1 + qd, 64);
+        const float other = red[(s * 2 + (1 - hh)) * 128 + rl];
+        if (!got || isnan(other)) { ok = false; break; }
+        const float mx = fmaxf(hm, other);
+        const float x = __fmul_rn(mx, c);
+        if (mx != kNegInf) {
+          if (M == kNegInf) {
+            M = x;
+          } else if (MX ? (x > __fadd_rn(M, p.delta)) : (__fsub_rn(x, M) > 8.0f)) {
+            rescale = true;
+            Mn = x;
+          }
         }
       }
       // fallback: O_aug row *= 2^(M - M') once the previous PV has landed.  tcgen05.ld/st
@@ -499,11 +523,8 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // ---- P~ for this half: codes into the consumed S columns, scales into SFP
       if constexpr (MX) {
         uint32_t pw[16];
-        constexpr int NWB = (FPV == F_E2M1 || FPV == F_EFQ) ? 4 : 8;
-        const uint32_t s0 = pgen_block<FPV, EXPM>(sv, bm0, c, M, p.efq_beta, pw);
-        const uint32_t s1 = pgen_block<FPV, EXPM>(sv + 32, bm1, c, M, p.efq_beta, pw + NWB);
+        const uint32_t sw = pgen_half<FPV, EXPM>(sv, bm0, bm1, c, M, p.efq_beta, pw);
         tmem_st_cols<C::P_COLS_HALF>(tl + C::T_S + 128 * s + 64 * hh, pw);
-        const uint32_t sw = s0 | (s1 << 8);
         TmemSt<1>::run(tl + C::T_SFP + 8 * s + 4 * hh + qd, &sw);
       } else {
         uint32_t pw[32];

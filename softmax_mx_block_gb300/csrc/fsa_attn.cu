@@ -25,11 +25,12 @@
 //   O = O_aug[:, :D] / l in fp32.
 //
 // CTA = one 128-row query tile of one (batch, head); 10 warps: warp 0 issues
-// TMA loads, warp 1 (one thread) issues tcgen05 MMAs and owns tensor memory,
-// warps 2..9 are two softmax warpgroups that split each key tile into halves
-// of 64 keys (thread = one row, one half).  S is double buffered in tensor
-// memory; P~ overwrites the consumed half of S and is read by the PV MMA
-// straight from tensor memory; O_aug stays in tensor memory until the end.
+// TMA loads, warp 1 issues the tcgen05 MMAs and owns tensor memory, warps 2..9
+// are the softmax warps, two per tensor-memory lane quadrant, which take
+// alternate key tiles (thread = one row, all 128 keys of the tile).  S is
+// double buffered in tensor memory and released as soon as a softmax warp holds
+// it in registers; P~ goes to buffers of its own, from which the PV MMA reads
+// it; O_aug stays in tensor memory until the end.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -153,34 +154,31 @@ __device__ __forceinline__ int block_exp(float bmax, float c, float M, float& nb
   return E;
 }
 
-// P codes of one 64-key half tile (raw scores sv[0..63] as two 32-key blocks,
-// masked = -inf) as packed words in out[] (16 words for one byte per code, 8 for
-// E2M1).  Returns the two scale bytes (block 0 in the low byte).
+// P codes of one 32-key block, in place: v[0..32) holds the raw scores (masked =
+// -inf) on entry and is clobbered.  Writes 8 packed words (one byte per code) or 4
+// (E2M1) to out[] and returns the scale byte E + 127.
 template <int FPV, int EXPM>
-__device__ __forceinline__ uint32_t pgen_half(const float* sv, float bm0, float bm1, float c, float M, int beta,
-                                              uint32_t* out) {
-  float nb0, nb1;
-  const int E0 = block_exp<FPV>(bm0, c, M, nb0);
-  const int E1 = block_exp<FPV>(bm1, c, M, nb1);
-  const uint64_t c2 = pk2(c, c), n0 = pk2(nb0, nb0), n1 = pk2(nb1, nb1);
-  float r[64];
+__device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, float M, int beta, uint32_t* out) {
+  float nb;
+  const int E = block_exp<FPV>(bmax, c, M, nb);
+  const uint64_t c2 = pk2(c, c), nb2 = pk2(nb, nb);
 #pragma unroll
-  for (int i = 0; i < 64; i += 2) upk2(ffma2(pk2(sv[i], sv[i + 1]), c2, i < 32 ? n0 : n1), r[i], r[i + 1]);
+  for (int i = 0; i < 32; i += 2) upk2(ffma2(pk2(v[i], v[i + 1]), c2, nb2), v[i], v[i + 1]);
   if constexpr (FPV == F_EFQ) {
     // k = clamp(rne(2 r + beta), 0, 7): fma onto the integer grid of 1.5*2^23, whose
     // low bits then hold k; nibble pairs combine by shift-add, bytes merge by permute
     const float magic = 12582912.0f;
     const uint64_t two2 = pk2(2.0f, 2.0f), kb2 = pk2(magic + (float)beta, magic + (float)beta);
-    uint32_t y[64];
+    uint32_t y[32];
 #pragma unroll
-    for (int i = 0; i < 64; i += 2) {
+    for (int i = 0; i < 32; i += 2) {
       float y0, y1;
-      upk2(ffma2(two2, pk2(r[i], r[i + 1]), kb2), y0, y1);
+      upk2(ffma2(two2, pk2(v[i], v[i + 1]), kb2), y0, y1);
       y[i] = __float_as_uint(fminf(fmaxf(y0, magic), magic + 7.0f));
       y[i + 1] = __float_as_uint(fminf(fmaxf(y1, magic), magic + 7.0f));
     }
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < 4; ++w) {
       const uint32_t* t = y + 8 * w;
       // low byte of (t1 << 4) + t0 is k0 | k1 << 4 (the magic's bits stay above bit 21)
       const uint32_t a01 = (t[1] << 4) + t[0], a23 = (t[3] << 4) + t[2];
@@ -188,35 +186,26 @@ __device__ __forceinline__ uint32_t pgen_half(const float* sv, float bm0, float 
       out[w] = prmt(prmt(a01, a23, 0x0040u), prmt(a45, a67, 0x0040u), 0x5410u);
     }
   } else {
-    exp2_block<EXPM>(r);
-    exp2_block<EXPM>(r + 32);
+    exp2_block<EXPM>(v);
     if constexpr (FPV == F_E4M3) {
 #pragma unroll
-      for (int w = 0; w < 16; ++w)
-        out[w] = pack_b16x2(cvt16_e4m3x2(r[4 * w], r[4 * w + 1]), cvt16_e4m3x2(r[4 * w + 2], r[4 * w + 3]));
+      for (int w = 0; w < 8; ++w)
+        out[w] = pack_b16x2(cvt16_e4m3x2(v[4 * w], v[4 * w + 1]), cvt16_e4m3x2(v[4 * w + 2], v[4 * w + 3]));
     } else if constexpr (FPV == F_E2M3) {
       // tensor memory holds 6-bit A operands one per byte (low 6 bits)
 #pragma unroll
-      for (int w = 0; w < 16; ++w)
-        out[w] = pack_b16x2(cvt16_e2m3x2(r[4 * w], r[4 * w + 1]), cvt16_e2m3x2(r[4 * w + 2], r[4 * w + 3]));
+      for (int w = 0; w < 8; ++w)
+        out[w] = pack_b16x2(cvt16_e2m3x2(v[4 * w], v[4 * w + 1]), cvt16_e2m3x2(v[4 * w + 2], v[4 * w + 3]));
     } else {
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const uint32_t b01 = cvt_e2m1x2(r[8 * w], r[8 * w + 1]), b23 = cvt_e2m1x2(r[8 * w + 2], r[8 * w + 3]);
-        const uint32_t b45 = cvt_e2m1x2(r[8 * w + 4], r[8 * w + 5]), b67 = cvt_e2m1x2(r[8 * w + 6], r[8 * w + 7]);
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t b01 = cvt_e2m1x2(v[8 * w], v[8 * w + 1]), b23 = cvt_e2m1x2(v[8 * w + 2], v[8 * w + 3]);
+        const uint32_t b45 = cvt_e2m1x2(v[8 * w + 4], v[8 * w + 5]), b67 = cvt_e2m1x2(v[8 * w + 6], v[8 * w + 7]);
         out[w] = prmt(prmt(b01, b23, 0x0040u), prmt(b45, b67, 0x0040u), 0x5410u);
       }
     }
   }
-  return (uint32_t)(E0 + 127) | ((uint32_t)(E1 + 127) << 8);
-}
-
-// bar.red.or over `nthreads` threads of named barrier `id`: true if any predicate is set.
-__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n barrier.red.or.pred q, %2, %3, p;\n"
-               " selp.b32 %0, 1, 0, q;\n}" : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
-  return r != 0;
+  return (uint32_t)(E + 127);
 }
 
 }  // namespace fsa
@@ -224,7 +213,7 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
 namespace fsa {
 
 template <int FQK, int FPV, int D, int EXPM>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(Cfg<FQK, FPV, D>::NTHREADS, 1)
 fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const KParams p) {
   using C = Cfg<FQK, FPV, D>;
@@ -252,12 +241,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 1 + C::NS;
-  uint64_t* v_full = bars + 1 + 2 * C::NS;
-  uint64_t* v_empty = bars + 1 + 3 * C::NS;
+  uint64_t* v_full = bars + 1 + C::NS;
+  uint64_t* pv_done = bars + 1 + 2 * C::NS;     // PV(j) -> slot j % NS
+  uint64_t* k_empty = bars + 1 + 3 * C::NS;    // S(j) done -> K slot j % NS
   uint64_t* s_full = bars + 1 + 4 * C::NS;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = s_full + 4;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_full + 4;
   uint64_t* drain = s_full + 6;
   uint64_t* stall = s_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
@@ -267,10 +256,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < C::NS; ++i) {
-      mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1);
-      mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1);
+      mbar_init(k_full + i, 1); mbar_init(v_full + i, 1); mbar_init(pv_done + i, 1); mbar_init(k_empty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) { mbar_init(s_full + i, 1); mbar_init(p_full + i, 8); mbar_init(pv_done + i, 1); }
+    for (int i = 0; i < 2; ++i) {
+      // one softmax warp per lane quadrant owns each tile
+      mbar_init(s_full + i, 1); mbar_init(s_free + i, 4); mbar_init(p_full + i, 4);
+    }
     mbar_init(drain, 1);
     mbar_init(stall, 1);
     *abort_flag = 0;
@@ -287,7 +278,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     else one4 = 0x22222222u;
     constexpr int ROWW = C::W_V / 4;                 // words per row per atom
     constexpr int PER_STAGE = C::NKA_V * 16 * ROWW;
-    for (int i = t; i < C::NS * PER_STAGE; i += 256) {
+    for (int i = t; i < C::NS * PER_STAGE; i += C::NTHREADS - 64) {
       const int st = i / PER_STAGE, rem = i % PER_STAGE;
       const int ka = rem / (16 * ROWW), r = (rem / ROWW) % 16, w = rem % ROWW;
       uint32_t val = 0u;
@@ -304,7 +295,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (MX) {
       uint32_t* one_atom = reinterpret_cast<uint32_t*>(sm + C::OFF_SFONE);
-      for (int i = t; i < 128; i += 256) one_atom[i] = 0x7F7F7F7Fu;
+      for (int i = t; i < 128; i += C::NTHREADS - 64) one_atom[i] = 0x7F7F7F7Fu;
     }
     fence_proxy_async_smem();
   }
@@ -318,7 +309,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 0) {
     // =============================================================== producer
     if (lane == 0 && nT > 0) {
-      int issued_k[C::NS] = {}, issued_v[C::NS] = {};
+      int nk = 0, nv = 0;                           // tiles whose K / V copies were started
       const int bhq = b * p.H + h, bhk = b * p.Hkv + kvh;
       mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
 #pragma unroll
@@ -327,113 +318,185 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
       for (int j = 0; j < nT; ++j) {
         const int st = j % C::NS;
-        const uint32_t ph = (j / C::NS) & 1;
-        if (!mbar_wait(k_empty + st, ph ^ 1, ac)) break;
+        // K slot st is free once S(j - NS) is done, V slot st once PV(j - NS) is
+        if (j >= C::NS && !mbar_wait(k_empty + st, ((j - C::NS) / C::NS) & 1, ac)) break;
         mbar_expect_tx(k_full + st, C::TILE_QK + (MX ? 512 : 0));
 #pragma unroll
         for (int ka = 0; ka < C::NKA_QK; ++ka)
           tma_load_3d(sK + st * C::TILE_QK + ka * 128 * C::W_QK, &tm_k, k_full + st, ka * C::W_QK, j * 128, bhk);
         if (MX) bulk_load(sm + C::OFF_SFK + st * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + st);
-        ++issued_k[st];
-        if (!mbar_wait(v_empty + st, ph ^ 1, ac)) break;
+        ++nk;
+        if (j >= C::NS && !mbar_wait(pv_done + st, ((j - C::NS) / C::NS) & 1, ac)) break;
         mbar_expect_tx(v_full + st, C::TILE_V_TMA + (MX ? 512 : 0));
 #pragma unroll
         for (int ka = 0; ka < C::NKA_V; ++ka)
           tma_load_3d(sV + st * C::TILE_V + ka * C::VATOM, &tm_v, v_full + st, j * C::RB_V + ka * C::W_V, 0, bhk);
         if (MX) bulk_load(sm + C::OFF_SFV + st * 512, p.sf_v + ((size_t)bhk * nkt + j) * 512, 512, v_full + st);
-        ++issued_v[st];
+        ++nv;
       }
       // every copy this thread started has landed before the CTA tears down
       mbar_wait_drain(q_full, 0, p.timeout_ns);
       for (int st = 0; st < C::NS; ++st) {
-        if (issued_k[st]) mbar_wait_drain(k_full + st, (issued_k[st] - 1) & 1, p.timeout_ns);
-        if (issued_v[st]) mbar_wait_drain(v_full + st, (issued_v[st] - 1) & 1, p.timeout_ns);
+        // copies started into slot st: (n - 1 - st) / NS + 1 of the first n tiles
+        if (st < nk) mbar_wait_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, p.timeout_ns);
+        if (st < nv) mbar_wait_drain(v_full + st, ((nv - 1 - st) / C::NS) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // =============================================================== MMA issuer
-    if (lane == 0 && nT > 0) {
+    // The warp runs converged; lane 0 polls the barriers and every tcgen05
+    // instruction is issued by the elected lane (the same lane throughout, so its
+    // commits cover all of them).  One warp issues both GEMMs: tcgen05 work from two
+    // issuing warps of one CTA was measured to serialise badly.
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool r = false;
+      if (lane == 0) r = mbar_wait<false>(bar, parity, ac);
+      return __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+    };
+    if (nT > 0) {
       const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
       constexpr uint32_t SWQ = swz_code(C::W_QK), SWV = swz_code(C::W_V);
       bool ok = true;
-      if (p.inject_stall) ok = mbar_wait(stall, 0, ac);        // nobody arrives: the wait must expire
-      ok = ok && mbar_wait(q_full, 0, ac);
+      if (p.inject_stall) {                                     // nobody arrives: the wait must expire
+        bool r = false;
+        if (lane == 0) r = mbar_wait(stall, 0, ac);
+        ok = __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+      }
+      ok = ok && wait_all(q_full, 0);
       if (ok) {
         tc_fence_after();
         if constexpr (MX) {
-          tc_cp_sf_atom(tbase + C::T_SFQ, smem_desc(smem_u32(sm + C::OFF_SFQ), 16, 128, 0));
+          if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFQ, smem_desc(smem_u32(sm + C::OFF_SFQ), 16, 128, 0));
           if constexpr (D == 128) {
-            tc_cp_sf_atom(tbase + C::T_SFV + 4, smem_desc(smem_u32(sm + C::OFF_SFONE), 16, 128, 0));
-            tc_cp_sf_atom(tbase + C::T_SFV + 12, smem_desc(smem_u32(sm + C::OFF_SFONE), 16, 128, 0));
+            const uint64_t one = smem_desc(smem_u32(sm + C::OFF_SFONE), 16, 128, 0);
+            if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFV + 4, one);
+            if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFV + 12, one);
           }
         }
       }
-      auto issue_pv = [&](int jj) -> bool {
+      auto issue_pv = [&](int jj) {
         const int s = jj & 1, st = jj % C::NS;
-        const uint32_t ph = (jj / C::NS) & 1;
-        if (!mbar_wait(p_full + s, (jj >> 1) & 1, ac)) return false;
-        if (!mbar_wait(v_full + st, ph, ac)) return false;
         tc_fence_after();
-        if constexpr (MX)
-          tc_cp_sf_atom(tbase + C::T_SFV + 8 * s, smem_desc(smem_u32(sm + C::OFF_SFV + st * 512), 16, 128, 0));
+        if constexpr (MX) {
+          const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFV + st * 512), 16, 128, 0);
+          if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFV + 8 * s, sfd);
+        }
 #pragma unroll
         for (int i = 0; i < C::PV_STEPS; ++i) {
-          const int hh = i / C::STEPS_PER_HALF, j2 = i % C::STEPS_PER_HALF;
-          const uint32_t a_tm = tbase + C::T_S + 128 * s + 64 * hh + 8 * j2;
+          // P~ of step i sits in columns [8i, 8i+8) of its P buffer; the scale word of
+          // each row (byte b = 32-key block b) is in column T_SFP + 4 s + lane quadrant
+          const uint32_t a_tm = tbase + C::T_P + C::P_COLS * (jj % C::NPB) + 8 * i;
+          const uint32_t sfa = tbase + C::T_SFP + 4 * s;
           const int ka = (i * 32) / C::W_V, off = (i * 32) % C::W_V;
           const uint64_t bd = smem_desc(sVa + st * C::TILE_V + ka * C::VATOM + off, 16, 8 * C::W_V, SWV);
           const uint32_t acc = (jj > 0 || i > 0) ? 1u : 0u;
-          if constexpr (KIND_PV == 0) {
-            mma_f16_ts(tbase + C::T_O, a_tm, bd, idesc_f16_bf16(C::N_PV), acc);
-          } else if constexpr (KIND_PV == 1) {
-            mma_mxf8f6f4_ts(tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, Fmt<FPV>::code, j2, i),
-                            tbase + C::T_SFP + 8 * s + 4 * hh, tbase + C::T_SFV + 8 * s, acc);
-          } else {
-            mma_mxf4_ts(tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, 1, 0, 2 * i),
-                        tbase + C::T_SFP + 8 * s + 4 * hh, tbase + C::T_SFV + 8 * s, acc);
+          if (elect_one()) {
+            if constexpr (KIND_PV == 0) {
+              mma_f16_ts(tbase + C::T_O, a_tm, bd, idesc_f16_bf16(C::N_PV), acc);
+            } else if constexpr (KIND_PV == 1) {
+              mma_mxf8f6f4_ts(tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, Fmt<FPV>::code, i, i), sfa,
+                              tbase + C::T_SFV + 8 * s, acc);
+            } else {
+              mma_mxf4_ts(tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, 1, 2 * i, 2 * i), sfa, tbase + C::T_SFV + 8 * s,
+                          acc);
+            }
           }
         }
-        tc_commit(pv_done + s);
-        tc_commit(v_empty + st);
-        return true;
+        if (elect_one()) tc_commit(pv_done + st);
       };
-      for (int j = 0; ok && j < nT; ++j) {
+      auto issue_s = [&](int j) {
         const int s = j & 1, st = j % C::NS;
-        const uint32_t ph = (j / C::NS) & 1;
-        if (!mbar_wait(k_full + st, ph, ac)) { ok = false; break; }
         tc_fence_after();
-        if constexpr (MX)
-          tc_cp_sf_atom(tbase + C::T_SFK + 4 * s, smem_desc(smem_u32(sm + C::OFF_SFK + st * 512), 16, 128, 0));
+        if constexpr (MX) {
+          const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFK + st * 512), 16, 128, 0);
+          if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFK + 4 * s, sfd);
+        }
 #pragma unroll
         for (int i = 0; i < C::QK_STEPS; ++i) {
           const int ka = (i * 32) / C::W_QK, off = (i * 32) % C::W_QK;
           const uint64_t ad = smem_desc(sQa + ka * 128 * C::W_QK + off, 16, 8 * C::W_QK, SWQ);
           const uint64_t bd = smem_desc(sKa + st * C::TILE_QK + ka * 128 * C::W_QK + off, 16, 8 * C::W_QK, SWQ);
           const uint32_t acc = i > 0 ? 1u : 0u;
-          if constexpr (KIND_QK == 0) {
-            mma_f16_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_f16_bf16(128), acc);
-          } else if constexpr (KIND_QK == 1) {
-            mma_mxf8f6f4_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, Fmt<FQK>::code, i, i),
-                            tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
-          } else {
-            mma_mxf4_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, 1, 2 * i, 2 * i),
-                        tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
+          if (elect_one()) {
+            if constexpr (KIND_QK == 0) {
+              mma_f16_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_f16_bf16(128), acc);
+            } else if constexpr (KIND_QK == 1) {
+              mma_mxf8f6f4_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, Fmt<FQK>::code, i, i),
+                              tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
+            } else {
+              mma_mxf4_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, 1, 2 * i, 2 * i),
+                          tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
+            }
           }
         }
-        tc_commit(s_full + s);
-        tc_commit(k_empty + st);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (elect_one()) tc_commit(s_full + s);
+        if (elect_one()) tc_commit(k_empty + st);
+      };
+      // Non-blocking scheduler: each round lane 0 tests the barriers of the next
+      // QK^T (K(jS) landed, S buffer loaded by its owners) and of the next PV (P~(jP)
+      // written, V(jP) landed) together, and whichever GEMM is ready is issued.  QK^T
+      // runs ahead of PV so that a softmax warp finds S(j) waiting when it is done
+      // with tile j-2; the round trips of the tests overlap.
+      int jS = 0, jP = 0;
+      uint32_t idle = 0;
+      uint64_t t0 = 0;
+      while (ok && jP < nT) {
+        int rdy = 0;
+        if (lane == 0) {
+          if (jS < nT && mbar_test(k_full + jS % C::NS, (jS / C::NS) & 1) &&
+              (jS < 2 || mbar_test(s_free + (jS & 1), ((jS - 2) >> 1) & 1)))
+            rdy |= 1;
+          if (jP < jS && mbar_test(p_full + (jP & 1), (jP >> 1) & 1) &&
+              mbar_test(v_full + jP % C::NS, (jP / C::NS) & 1))
+            rdy |= 2;
+        }
+        rdy = __shfl_sync(0xffffffffu, rdy, 0);
+        if (rdy & 1) issue_s(jS++);
+        if (rdy & 2) issue_pv(jP++);
+        if (rdy) {
+          idle = 0;
+          continue;
+        }
+        // nothing ready: park in a suspending try_wait on what most likely completes
+        // next (P~(jP) once QK^T has run ahead, else the next QK^T's inputs), so the
+        // warp takes no issue slots from the softmax warps of its scheduler
+        if (lane == 0) {
+          if (jP < jS && (jS >= nT || jS - jP >= 2)) mbar_try_wait(p_full + (jP & 1), (jP >> 1) & 1);
+          else if (jS < nT && !mbar_test(k_full + jS % C::NS, (jS / C::NS) & 1))
+            mbar_try_wait(k_full + jS % C::NS, (jS / C::NS) & 1);
+          else if (jS < nT && jS >= 2) mbar_try_wait(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
+        }
+        __syncwarp();
+        // bounded wait, abort check
+        if (++idle == 1) t0 = globaltimer_ns();
+        if ((idle & 7u) == 0) {
+          int stop = 0;
+          if (lane == 0) {
+            if (*ac.flag) stop = 1;
+            else if (globaltimer_ns() - t0 > ac.limit_ns) {
+              *ac.flag = 1;
+              if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
+              stop = 1;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
+        }
       }
-      if (ok) issue_pv(nT - 1);
-      // all MMAs and copies issued by this thread complete before tensor memory is freed
-      tc_commit(drain);
+      // all MMAs and copies issued by this warp complete before tensor memory is freed
+      if (elect_one()) tc_commit(drain);
       mbar_wait_drain(drain, 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
     // =============================================================== softmax / epilogue
-    const int hh = (warp - 2) >> 2;                 // key half of every tile
+    // The two warps of a tensor-memory lane quadrant take alternate key tiles: part pp
+    // owns the tiles j with j % 2 == pp, all 128 keys of its 32 rows (thread = row),
+    // and with them S buffer, P~ buffer and scale column pp.  The running maximum M
+    // passes between the two once per tile (shared memory plus a named-barrier
+    // handoff), so they work half a tile apart instead of in lockstep.
+    constexpr int NBLK = 4;                         // 32-key blocks per tile
+    const int pp = (warp - 2) >> 2;
     const int qd = warp & 3;                        // tensor-memory lane quadrant
     const int rl = 32 * qd + lane;                  // row within the tile
     const int row = q0 + rl;
@@ -442,122 +505,147 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     int lim = p.Sk - 1;
     if (p.causal) lim = min(lim, row + p.Sk - p.Sq);
     const float c = p.c;
+    const int bar_in = 1 + qd + 4 * pp, bar_out = 1 + qd + 4 * (1 - pp);
+    volatile float* m_slot = red + rl;              // M of this row after the latest tile
     float M = kNegInf;
     int nfb = 0, nvis = 0;
-    bool ok = true;
-    for (int j = 0; j < nT; ++j) {
-      const int s = j & 1;
-      // a failed wait (here or in the previous fallback) is exchanged with the partner
-      // warp below, so both warps of a row pair leave the loop at the same iteration
-      const bool got = __all_sync(0xffffffffu, ok && mbar_wait(s_full + s, (j >> 1) & 1, ac));
-      float sv[64];
-      float bm0 = kNegInf, bm1 = kNegInf;
+    bool ok = true;                                 // false once any wait failed: no more work
+    // lane 0 polls and broadcasts: 32 lanes polling one mbarrier serialise
+    auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool r = false;
+      if (lane == 0) r = mbar_wait<false>(bar, parity, ac);
+      return __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+    };
+    for (int j = pp; j < nT; j += 2) {
+      const int s = pp;
+      const bool got = ok && wait0(s_full + s, (j >> 1) & 1);
+      if (!got) ok = false;
+      float sv[128];
+      float bm[NBLK];
+#pragma unroll
+      for (int b = 0; b < NBLK; ++b) bm[b] = kNegInf;
       if (got) {
         tc_fence_after();
-        uint32_t raw[64];
-        tmem_ld_cols<64>(tl + C::T_S + 128 * s + 64 * hh, raw);
+        uint32_t raw[128];
+        tmem_ld_cols<128>(tl + C::T_S + 128 * s, raw);
         tc_wait_ld();
-        const int kbase = 128 * j + 64 * hh;
+        // S(j) is in registers: its buffer may take S(j+2)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free + s);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(raw[i]);
-        if (kbase + 63 > lim) {                     // only diagonal / tail tiles mask keys
+        for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(raw[i]);
+        if (128 * j + 127 > lim) {                  // only diagonal / tail tiles mask keys
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (kbase + i > lim) sv[i] = kNegInf;
+          for (int i = 0; i < 128; ++i)
+            if (128 * j + i > lim) sv[i] = kNegInf;
         }
-        bm0 = max32(sv);
-        bm1 = max32(sv + 32);
+#pragma unroll
+        for (int b = 0; b < NBLK; ++b) bm[b] = max32(sv + 32 * b);
       }
-      // The row's two halves agree on the tile maximum only when some row of the warp
-      // pair needs it: its first visible tile, a fallback (x > M + delta), or a failed
-      // wait.  The test per half is exact: rounding is monotone, so
-      // fp32(max(a,b)*c) > T  <=>  fp32(a*c) > T or fp32(b*c) > T.
-      const float hm = fmaxf(bm0, bm1);
-      const bool vis = 128 * j <= lim;               // first key of the tile visible to this row
-      const bool need = !got || (vis && (M == kNegInf ||
-                                         (MX ? (__fmul_rn(hm, c) > __fadd_rn(M, p.delta))
-                                             : (__fsub_rn(__fmul_rn(hm, c), M) > 8.0f))));
+      // M after tile j-1 comes from the other part (NaN: it has stopped working)
+      if (j > 0) {
+        named_bar_sync(bar_in, 64);
+        const float Mp = *m_slot;
+        if (isnan(Mp)) ok = false;
+        else M = Mp;
+      }
+      // first visible tile: M = x; later: fallback when x > fp32(M + delta)
+      const float hm = fmaxf(fmaxf(bm[0], bm[1]), fmaxf(bm[2], bm[3]));
+      if (128 * j <= lim) ++nvis;
       bool rescale = false;
       float Mn = M;
-      if (vis) ++nvis;
-      if (named_bar_or(1 + qd, 64, need)) {
-        red[(s * 2 + hh) * 128 + rl] = got ? hm : __int_as_float(0x7FC00000);
-        named_bar_sync(1 + qd, 64);
-        const float other = red[(s * 2 + (1 - hh)) * 128 + rl];
-        if (!got || isnan(other)) { ok = false; break; }
-        const float mx = fmaxf(hm, other);
-        const float x = __fmul_rn(mx, c);
-        if (mx != kNegInf) {
-          if (M == kNegInf) {
-            M = x;
-          } else if (MX ? (x > __fadd_rn(M, p.delta)) : (__fsub_rn(x, M) > 8.0f)) {
-            rescale = true;
-            Mn = x;
-          }
+      if (ok && hm != kNegInf) {
+        const float x = __fmul_rn(hm, c);
+        if (M == kNegInf) {
+          Mn = x;
+        } else if (MX ? (x > __fadd_rn(M, p.delta)) : (__fsub_rn(x, M) > 8.0f)) {
+          rescale = true;
+          Mn = x;
         }
       }
-      // fallback: O_aug row *= 2^(M - M') once the previous PV has landed.  tcgen05.ld/st
-      // are warp-collective, so the whole warp rescales when any of its rows falls
-      // back; the other rows multiply by exactly 1.
+      if (j + 1 < nT) {
+        *m_slot = ok ? Mn : __int_as_float(0x7FC00000);
+        named_bar_arrive(bar_out, 64);
+      }
+      // fallback: O_aug row *= 2^(M - M') once PV(j-1) has landed.  tcgen05.ld/st are
+      // warp-collective, so the whole warp rescales when any of its rows falls back;
+      // the other rows multiply by exactly 1.
       if (__any_sync(0xffffffffu, rescale)) {
         const float alpha = rescale ? ex2_approx(__fsub_rn(M, Mn)) : 1.0f;
-        const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, ac));
-        if (!pv_ok) ok = false;
+        if (wait0(pv_done + (j - 1) % C::NS, ((j - 1) / C::NS) & 1)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::N_PV; c0 += 16) {
+            uint32_t o[16];
+            TmemLd<16>::run(tl + C::T_O + c0, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), alpha));
+            TmemSt<16>::run(tl + C::T_O + c0, o);
+          }
+          tc_wait_st();
+        } else {
+          ok = false;
+        }
+        if (rescale) ++nfb;
+      }
+      M = Mn;
+      // P~ buffer j % NPB and scale column s were last read by PV(j - NPB)
+      if (ok && j >= C::NPB && !wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1)) ok = false;
+      if (ok) {
+        // ---- P~ of the tile into P buffer j % NPB, one 32-key block at a time
         tc_fence_after();
-        constexpr int HALF = C::N_PV / 2;             // 72 or 40 columns, in chunks of 8
+        const uint32_t tp = tl + C::T_P + C::P_COLS * (j % C::NPB);
+        if constexpr (MX) {
+          constexpr int WB = C::P_COLS / NBLK;       // words (columns) per block: 8, or 4 for E2M1
+          uint32_t sw = 0;
 #pragma unroll
-        for (int c0 = 0; c0 < HALF; c0 += 8) {
-          uint32_t o[8];
-          TmemLd<8>::run(tl + C::T_O + hh * HALF + c0, o);
-          tc_wait_ld();
+          for (int b = 0; b < NBLK; ++b) {
+            uint32_t pw[WB];
+            sw |= pgen_block<FPV, EXPM>(sv + 32 * b, bm[b], c, M, p.efq_beta, pw) << (8 * b);
+            tmem_st_cols<WB>(tp + WB * b, pw);
+          }
+          // A scales of the PV MMA: lane quadrant q reads column base + q
+          TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
+        } else {
+          {
+            const float nM = M == kNegInf ? 0.0f : -M;   // no visible key yet: every s is -inf, p = 0
+            const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), alpha));
-          TmemSt<8>::run(tl + C::T_O + hh * HALF + c0, o);
+            for (int b = 0; b < NBLK; ++b) {
+              uint32_t pw[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float a, bb;
+                upk2(ffma2(pk2(sv[32 * b + 2 * i], sv[32 * b + 2 * i + 1]), c2, nM2), a, bb);
+                pw[i] = cvt_bf16x2(ex2_approx(a), ex2_approx(bb));
+              }
+              tmem_st_cols<16>(tp + 16 * b, pw);
+            }
+          }
         }
         tc_wait_st();
-        if (rescale) {
-          M = Mn;
-          ++nfb;
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(p_full + s);
       }
-      // ---- P~ for this half: codes into the consumed S columns, scales into SFP
-      if constexpr (MX) {
-        uint32_t pw[16];
-        const uint32_t sw = pgen_half<FPV, EXPM>(sv, bm0, bm1, c, M, p.efq_beta, pw);
-        tmem_st_cols<C::P_COLS_HALF>(tl + C::T_S + 128 * s + 64 * hh, pw);
-        TmemSt<1>::run(tl + C::T_SFP + 8 * s + 4 * hh + qd, &sw);
-      } else {
-        uint32_t pw[32];
-        const float nM = M == kNegInf ? 0.0f : -M;   // no visible key yet: every s is -inf, p = 0
-        const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float a, bb;
-          upk2(ffma2(pk2(sv[2 * i], sv[2 * i + 1]), c2, nM2), a, bb);
-          pw[i] = cvt_bf16x2(ex2_approx(a), ex2_approx(bb));
-        }
-        tmem_st_cols<32>(tl + C::T_S + 128 * s + 64 * hh, pw);
-      }
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + s);
     }
-    // ---- epilogue: O = O_aug[:, :D] / l
-    float* orow = p.out + (((size_t)b * p.H + h) * p.Sq + (row_valid ? row : 0)) * D + hh * (D / 2);
-    const bool done = ok && nT > 0 &&
-                      __all_sync(0xffffffffu, mbar_wait(pv_done + ((nT - 1) & 1), ((nT - 1) >> 1) & 1, ac));
+    // ---- epilogue: O = O_aug[:, :D] / l, D/2 columns per part
+    constexpr int DP = D / 2;
+    float* orow = p.out + (((size_t)b * p.H + h) * p.Sq + (row_valid ? row : 0)) * D + DP * pp;
+    const bool done = ok && nT > 0 && wait0(pv_done + (nT - 1) % C::NS, ((nT - 1) / C::NS) & 1);
     if (done) {
       tc_fence_after();
       uint32_t lraw;
       TmemLd<1>::run(tl + C::T_O + D, &lraw);
-      uint32_t o[D / 2];
-      tmem_ld_cols<D / 2>(tl + C::T_O + hh * (D / 2), o);
+      uint32_t o[DP];
+      tmem_ld_cols<DP>(tl + C::T_O + DP * pp, o);
       tc_wait_ld();
       const float l = __uint_as_float(lraw);
       if (row_valid) {
 #pragma unroll
-        for (int i = 0; i < D / 2; i += 4) {
+        for (int i = 0; i < DP; i += 4) {
           float4 v;
           v.x = l > 0.f ? __fdiv_rn(__uint_as_float(o[i]), l) : 0.f;
           v.y = l > 0.f ? __fdiv_rn(__uint_as_float(o[i + 1]), l) : 0.f;
@@ -568,21 +656,24 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     } else if (nT == 0 && row_valid) {
 #pragma unroll
-      for (int i = 0; i < D / 2; i += 4) *reinterpret_cast<float4*>(orow + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < DP; i += 4) *reinterpret_cast<float4*>(orow + i) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (hh == 0) {
-      if (row_valid && p.row_fallbacks) p.row_fallbacks[((size_t)b * p.H + h) * p.Sq + row] = nfb;
-      unsigned long long f = row_valid ? (unsigned long long)nfb : 0ull;
-      unsigned long long v = row_valid ? (unsigned long long)nvis : 0ull;
+    // ---- statistics: each part counted the tiles it owns
+    int* nfb_other = reinterpret_cast<int*>(red) + 128 + rl;
+    if (pp == 1) *nfb_other = nfb;
+    named_bar_sync(9 + qd, 64);
+    if (pp == 0 && row_valid && p.row_fallbacks)
+      p.row_fallbacks[((size_t)b * p.H + h) * p.Sq + row] = nfb + *nfb_other;
+    unsigned long long f = row_valid ? (unsigned long long)nfb : 0ull;
+    unsigned long long v = row_valid ? (unsigned long long)nvis : 0ull;
 #pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) {
-        f += __shfl_xor_sync(0xffffffffu, f, o2);
-        v += __shfl_xor_sync(0xffffffffu, v, o2);
-      }
-      if (lane == 0 && p.stat_fallbacks) {
-        atomicAdd(p.stat_fallbacks, f);
-        atomicAdd(p.stat_row_tiles, v);
-      }
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      f += __shfl_xor_sync(0xffffffffu, f, o2);
+      v += __shfl_xor_sync(0xffffffffu, v, o2);
+    }
+    if (lane == 0 && p.stat_fallbacks) {
+      atomicAdd(p.stat_fallbacks, f);
+      atomicAdd(p.stat_row_tiles, v);
     }
   }
   // ---- teardown

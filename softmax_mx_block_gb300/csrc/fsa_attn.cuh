@@ -40,14 +40,19 @@ struct Cfg {
   static constexpr int W_V = RB_V < 128 ? RB_V : 128;
   static constexpr int NKA_V = RB_V / W_V;
   static constexpr int PV_STEPS = RB_V / 32;
-  static constexpr int STEPS_PER_HALF = PV_STEPS / 2;
   static constexpr int VATOM = N_PV * W_V;                          // bytes of one K-atom of the V tile
   static constexpr int TILE_V = NKA_V * VATOM;
   static constexpr int TILE_V_TMA = NKA_V * D * W_V;                // bytes TMA writes per tile
-  // ---- P in tensor memory: 64 keys per softmax half
-  static constexpr int P_COLS_HALF = 64 * Fmt<FPV>::bits2 / 16 / 4;
+  // ---- softmax: two warps per tensor-memory lane quadrant, taking alternate key
+  // tiles (thread = one row, all 128 keys of the tile)
+  static constexpr int NQ = 2;
+  static constexpr int NSW = 4 * NQ;                                // softmax warps
+  // ---- P~ in tensor memory, its own buffers (so S is free once loaded)
+  static constexpr int P_COLS = 128 * Fmt<FPV>::bits2 / 16 / 4;     // 32 (8-bit), 16 (E2M1), 64 (BF16)
+  static constexpr int NPB = MX ? 2 : 1;                            // P~ buffers
+  static_assert(P_COLS == 8 * PV_STEPS, "one PV step per 8 columns");
   // ---- pipeline
-  static constexpr int NS = MX ? 3 : 2;                             // K/V stages
+  static constexpr int NS = MX ? 4 : 2;                             // K/V stages
   static constexpr int SF_BYTES = 512;
   // ---- shared memory offsets (1024-aligned tiles)
   static constexpr int OFF_Q = 0;
@@ -58,22 +63,25 @@ struct Cfg {
   static constexpr int OFF_SFK = OFF_SFQ + SF_BYTES;
   static constexpr int OFF_SFV = OFF_SFK + NS * SF_BYTES;
   static constexpr int OFF_SFONE = OFF_SFV + NS * SF_BYTES;
-  static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // row-max exchange [parity][half][row] fp32
-  static constexpr int OFF_BAR = OFF_RED + 2 * 2 * 128 * 4;
-  static constexpr int NBAR = 1 + 4 * NS + 3 * 2 + 2;               // q, k/v full/empty, s/p/pv x2, drain, stall
+  static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // M handoff [row], fallback counts [row]
+  static constexpr int OFF_BAR = OFF_RED + 2 * 128 * 4;
+  static constexpr int NBAR = 1 + 4 * NS + 3 * 2 + 2;               // q, k/v full, pv done, k empty x NS, s full/free, p x2, drain, stall
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
   static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
   static_assert(SMEM <= 227 * 1024, "shared memory");
   // ---- tensor memory columns
-  static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256); P aliases its half of S
+  static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256)
   static constexpr uint32_t T_O = 256;        // [256, 256 + N_PV)
   static constexpr uint32_t T_SFQ = 400;
   static constexpr uint32_t T_SFK = 404;      // + 4 * parity
   static constexpr uint32_t T_SFV = 412;      // + 8 * parity (4 from the V atom, 4 constant)
-  static constexpr uint32_t T_SFP = 428;      // + 8 * parity + 4 * half
+  static constexpr uint32_t T_SFP = 428;      // + 4 * buffer + lane quadrant
+  static constexpr uint32_t T_P = 448;       // + P_COLS * buffer
   static_assert(T_O + N_PV <= T_SFQ, "tmem");
+  static_assert(!MX || T_SFP + 8 <= T_P, "tmem");
+  static_assert(T_P + NPB * P_COLS <= 512, "tmem");
   // ---- threads
-  static constexpr int NTHREADS = 320;        // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+  static constexpr int NTHREADS = 64 + 32 * NSW;   // warp 0 TMA, warp 1 MMA, then the softmax warps
 };
 
 struct KParams {

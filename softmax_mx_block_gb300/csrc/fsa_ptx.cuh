@@ -39,6 +39,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
                " selp.b32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               " selp.b32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
 // As above, but the thread may sleep up to `hint_ns` inside the instruction (it
 // resumes as soon as the phase completes), so a waiting warp issues few polls.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
@@ -57,11 +64,14 @@ struct AbortCtl {
 };
 
 // Wait for phase `parity` of `bar`; false if the limit passed or the CTA aborted.
+// SLEEP lets the thread doze inside each poll (few issue slots taken from the
+// warps it shares a scheduler with); the latency-critical waits poll without it.
+template <bool SLEEP = true>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const AbortCtl& ac) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (SLEEP ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
     if ((it & 7u) == 0) {
       if (*ac.flag) return false;
       if (globaltimer_ns() - t0 > ac.limit_ns) {
@@ -82,6 +92,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// One lane of a converged warp (the lowest active one) gets true.  The tcgen05
+// issuing warp runs converged and elects its issuing lane per instruction.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.b32 %0, 1, 0, p;\n}" : "=r"(e));
+  return e != 0;
+}
+
 // ---------------------------------------------------------------- TMA / bulk
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y, int z) {
   asm volatile(
@@ -98,6 +116,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Arrive on named barrier `id` without waiting (the producer side of a handoff).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------- tcgen05
@@ -198,6 +220,7 @@ template <int N> struct TmemLd;
     }                                                                                        \
   };
 FSA_TMEM_LD(1, "%0", "=r"(r[0]))
+FSA_TMEM_LD(4, "%0,%1,%2,%3", "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]))
 FSA_TMEM_LD(8, "%0,%1,%2,%3,%4,%5,%6,%7", "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
             "=r"(r[5]), "=r"(r[6]), "=r"(r[7]))
 FSA_TMEM_LD(16, "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15", "=r"(r[0]), "=r"(r[1]), "=r"(r[2]),
@@ -214,6 +237,7 @@ template <int N> struct TmemSt;
     }                                                                                        \
   };
 FSA_TMEM_ST(1, "%1", "r"(r[0]))
+FSA_TMEM_ST(4, "%1,%2,%3,%4", "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]))
 FSA_TMEM_ST(8, "%1,%2,%3,%4,%5,%6,%7,%8", "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
             "r"(r[6]), "r"(r[7]))
 FSA_TMEM_ST(16, "%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16", "r"(r[0]), "r"(r[1]), "r"(r[2]),

@@ -54,6 +54,11 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint64_t fadd2_rm(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -267,7 +272,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp >= 2) {
+  if (MX && warp >= 2) {
     // constant rows D..D+15 of every V stage (row D = ones, the rest zero) and the
     // scale atom that gives the ones row scale 2^0 in the upper tensor-memory columns
     const int t = threadIdx.x - 64;
@@ -510,6 +515,8 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float M = kNegInf;
     int nfb = 0, nvis = 0;
     bool ok = true;                                 // false once any wait failed: no more work
+    // BF16: the denominator is summed here, per part, relative to the part's latest M
+    float lsum = 0.0f, Ml = kNegInf;
     // lane 0 polls and broadcasts: 32 lanes polling one mbarrier serialise
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
       bool r = false;
@@ -591,6 +598,10 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (rescale) ++nfb;
       }
       M = Mn;
+      if constexpr (!MX) {
+        if (Ml != kNegInf && M != Ml) lsum *= ex2_approx(__fsub_rn(Ml, M));
+        Ml = M;
+      }
       // P~ buffer j % NPB and scale column s were last read by PV(j - NPB)
       if (ok && j >= C::NPB && !wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1)) ok = false;
       if (ok) {
@@ -612,6 +623,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           {
             const float nM = M == kNegInf ? 0.0f : -M;   // no visible key yet: every s is -inf, p = 0
             const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
+            uint64_t acc = pk2(0.0f, 0.0f);
 #pragma unroll
             for (int b = 0; b < NBLK; ++b) {
               uint32_t pw[16];
@@ -620,9 +632,14 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float a, bb;
                 upk2(ffma2(pk2(sv[32 * b + 2 * i], sv[32 * b + 2 * i + 1]), c2, nM2), a, bb);
                 pw[i] = cvt_bf16x2(ex2_approx(a), ex2_approx(bb));
+                // the denominator sums the rounded p that the PV MMA multiplies
+                acc = fadd2(acc, pk2(__uint_as_float(pw[i] << 16), __uint_as_float(pw[i] & 0xFFFF0000u)));
               }
               tmem_st_cols<16>(tp + 16 * b, pw);
             }
+            float a0, a1;
+            upk2(acc, a0, a1);
+            lsum += a0 + a1;
           }
         }
         tc_wait_st();
@@ -633,16 +650,28 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     // ---- epilogue: O = O_aug[:, :D] / l, D/2 columns per part
     constexpr int DP = D / 2;
+    float lb = 0.0f;                                 // BF16: l of the row from both parts
+    if constexpr (!MX) {
+      float* xl = red + 256 + 4 * rl;                // [row] {l, M} of each part
+      xl[2 * pp] = lsum;
+      xl[2 * pp + 1] = Ml;
+      named_bar_sync(9 + qd, 64);
+      const float l0 = xl[0], m0 = xl[1], l1 = xl[2], m1 = xl[3];
+      const float mf = fmaxf(m0, m1);
+      lb = (m0 != kNegInf ? l0 * ex2_approx(__fsub_rn(m0, mf)) : 0.0f) +
+           (m1 != kNegInf ? l1 * ex2_approx(__fsub_rn(m1, mf)) : 0.0f);
+      named_bar_sync(9 + qd, 64);                    // both have read before the slots are reused
+    }
     float* orow = p.out + (((size_t)b * p.H + h) * p.Sq + (row_valid ? row : 0)) * D + DP * pp;
     const bool done = ok && nT > 0 && wait0(pv_done + (nT - 1) % C::NS, ((nT - 1) / C::NS) & 1);
     if (done) {
       tc_fence_after();
-      uint32_t lraw;
-      TmemLd<1>::run(tl + C::T_O + D, &lraw);
+      uint32_t lraw = 0;
+      if constexpr (MX) TmemLd<1>::run(tl + C::T_O + D, &lraw);
       uint32_t o[DP];
       tmem_ld_cols<DP>(tl + C::T_O + DP * pp, o);
       tc_wait_ld();
-      const float l = __uint_as_float(lraw);
+      const float l = MX ? __uint_as_float(lraw) : lb;
       if (row_valid) {
 #pragma unroll
         for (int i = 0; i < DP; i += 4) {

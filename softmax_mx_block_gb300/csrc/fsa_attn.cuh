@@ -34,8 +34,9 @@ struct Cfg {
   static constexpr int NKA_QK = RB_QK / W_QK;                       // atoms along K
   static constexpr int QK_STEPS = RB_QK / 32;                       // 32 bytes of K per MMA
   static constexpr int TILE_QK = BM * RB_QK;                        // bytes of a 128-row tile
-  // ---- PV operands (V^T rows of 128 keys, plus 16 rows: ones row, zero rows)
-  static constexpr int N_PV = D + 16;
+  // ---- PV operands (V^T rows of 128 keys; the MX kernels add 16 rows, a ones row
+  // and zero rows, whose product column accumulates the denominator l)
+  static constexpr int N_PV = MX ? D + 16 : D;
   static constexpr int RB_V = BN * Fmt<FPV>::bits2 / 16;            // bytes per V^T row per key tile
   static constexpr int W_V = RB_V < 128 ? RB_V : 128;
   static constexpr int NKA_V = RB_V / W_V;
@@ -49,7 +50,7 @@ struct Cfg {
   static constexpr int NSW = 4 * NQ;                                // softmax warps
   // ---- P~ in tensor memory, its own buffers (so S is free once loaded)
   static constexpr int P_COLS = 128 * Fmt<FPV>::bits2 / 16 / 4;     // 32 (8-bit), 16 (E2M1), 64 (BF16)
-  static constexpr int NPB = MX ? 2 : 1;                            // P~ buffers
+  static constexpr int NPB = 2;                                     // P~ buffers
   static_assert(P_COLS == 8 * PV_STEPS, "one PV step per 8 columns");
   // ---- pipeline
   static constexpr int NS = MX ? 4 : 2;                             // K/V stages
@@ -63,8 +64,8 @@ struct Cfg {
   static constexpr int OFF_SFK = OFF_SFQ + SF_BYTES;
   static constexpr int OFF_SFV = OFF_SFK + NS * SF_BYTES;
   static constexpr int OFF_SFONE = OFF_SFV + NS * SF_BYTES;
-  static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // M handoff [row], fallback counts [row]
-  static constexpr int OFF_BAR = OFF_RED + 2 * 128 * 4;
+  static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // M handoff, fallback counts, BF16 {l, M} x 2
+  static constexpr int OFF_BAR = OFF_RED + (256 + 4 * 128) * 4;
   static constexpr int NBAR = 1 + 4 * NS + 3 * 2 + 2;               // q, k/v full, pv done, k empty x NS, s full/free, p x2, drain, stall
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
   static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
@@ -76,8 +77,8 @@ struct Cfg {
   static constexpr uint32_t T_SFK = 404;      // + 4 * parity
   static constexpr uint32_t T_SFV = 412;      // + 8 * parity (4 from the V atom, 4 constant)
   static constexpr uint32_t T_SFP = 428;      // + 4 * buffer + lane quadrant
-  static constexpr uint32_t T_P = 448;       // + P_COLS * buffer
-  static_assert(T_O + N_PV <= T_SFQ, "tmem");
+  static constexpr uint32_t T_P = MX ? 448 : T_O + D;   // + P_COLS * buffer (BF16: no scales)
+  static_assert(T_O + N_PV <= (MX ? T_SFQ : T_P), "tmem");
   static_assert(!MX || T_SFP + 8 <= T_P, "tmem");
   static_assert(T_P + NPB * P_COLS <= 512, "tmem");
   // ---- threads

@@ -575,68 +575,74 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         *m_slot = ok ? Mn : __int_as_float(0x7FC00000);
         named_bar_arrive(bar_out, 64);
       }
-      // fallback: O_aug row *= 2^(M - M') once PV(j-1) has landed.  tcgen05.ld/st are
-      // warp-collective, so the whole warp rescales when any of its rows falls back;
-      // the other rows multiply by exactly 1.
-      if (__any_sync(0xffffffffu, rescale)) {
-        const float alpha = rescale ? ex2_approx(__fsub_rn(M, Mn)) : 1.0f;
-        if (wait0(pv_done + (j - 1) % C::NS, ((j - 1) / C::NS) & 1)) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int c0 = 0; c0 < C::N_PV; c0 += 16) {
-            uint32_t o[16];
-            TmemLd<16>::run(tl + C::T_O + c0, o);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), alpha));
-            TmemSt<16>::run(tl + C::T_O + c0, o);
-          }
-          tc_wait_st();
-        } else {
-          ok = false;
-        }
-        if (rescale) ++nfb;
-      }
+      const float alpha = rescale ? ex2_approx(__fsub_rn(M, Mn)) : 1.0f;
+      if (rescale) ++nfb;
       M = Mn;
       if constexpr (!MX) {
         if (Ml != kNegInf && M != Ml) lsum *= ex2_approx(__fsub_rn(Ml, M));
         Ml = M;
       }
-      // P~ buffer j % NPB and scale column s were last read by PV(j - NPB)
-      if (ok && j >= C::NPB && !wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1)) ok = false;
       if (ok) {
-        // ---- P~ of the tile into P buffer j % NPB, one 32-key block at a time
-        tc_fence_after();
+        // ---- P~ of the tile in two halves of two 32-key blocks.  The first half is
+        // generated before waiting for the PVs that the rescale and the buffer reuse
+        // depend on, which gives them that much longer to finish.
+        constexpr int HW = C::P_COLS / 2;             // words (columns) per half
         const uint32_t tp = tl + C::T_P + C::P_COLS * (j % C::NPB);
-        if constexpr (MX) {
-          constexpr int WB = C::P_COLS / NBLK;       // words (columns) per block: 8, or 4 for E2M1
-          uint32_t sw = 0;
+        uint32_t sw = 0;
+        uint64_t acc = pk2(0.0f, 0.0f);               // BF16: sum of the rounded p
+        const float nM = M == kNegInf ? 0.0f : -M;    // BF16, no visible key yet: every s is -inf, p = 0
+        auto gen_half = [&](int hf, uint32_t* pw) {
+          if constexpr (MX) {
+            constexpr int WB = C::P_COLS / NBLK;       // words per block: 8, or 4 for E2M1
 #pragma unroll
-          for (int b = 0; b < NBLK; ++b) {
-            uint32_t pw[WB];
-            sw |= pgen_block<FPV, EXPM>(sv + 32 * b, bm[b], c, M, p.efq_beta, pw) << (8 * b);
-            tmem_st_cols<WB>(tp + WB * b, pw);
-          }
-          // A scales of the PV MMA: lane quadrant q reads column base + q
-          TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
-        } else {
-          {
-            const float nM = M == kNegInf ? 0.0f : -M;   // no visible key yet: every s is -inf, p = 0
+            for (int b = 0; b < 2; ++b)
+              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p.efq_beta, pw + WB * b)
+                    << (8 * (2 * hf + b));
+          } else {
             const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
-            uint64_t acc = pk2(0.0f, 0.0f);
 #pragma unroll
-            for (int b = 0; b < NBLK; ++b) {
-              uint32_t pw[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float a, bb;
-                upk2(ffma2(pk2(sv[32 * b + 2 * i], sv[32 * b + 2 * i + 1]), c2, nM2), a, bb);
-                pw[i] = cvt_bf16x2(ex2_approx(a), ex2_approx(bb));
-                // the denominator sums the rounded p that the PV MMA multiplies
-                acc = fadd2(acc, pk2(__uint_as_float(pw[i] << 16), __uint_as_float(pw[i] & 0xFFFF0000u)));
-              }
-              tmem_st_cols<16>(tp + 16 * b, pw);
+            for (int i = 0; i < 32; ++i) {
+              float a, bb;
+              upk2(ffma2(pk2(sv[64 * hf + 2 * i], sv[64 * hf + 2 * i + 1]), c2, nM2), a, bb);
+              pw[i] = cvt_bf16x2(ex2_approx(a), ex2_approx(bb));
+              // the denominator sums the rounded p that the PV MMA multiplies
+              acc = fadd2(acc, pk2(__uint_as_float(pw[i] << 16), __uint_as_float(pw[i] & 0xFFFF0000u)));
             }
+          }
+        };
+        uint32_t pw[HW];
+        if constexpr (MX) gen_half(0, pw);           // (BF16: too many registers to hold across)
+        // fallback: O_aug row *= 2^(M_old - M) once PV(j-1) has landed.  tcgen05.ld/st
+        // are warp-collective, so the whole warp rescales when any of its rows falls
+        // back; the other rows multiply by exactly 1.
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (wait0(pv_done + (j - 1) % C::NS, ((j - 1) / C::NS) & 1)) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < C::N_PV; c0 += 8) {
+              uint32_t o[8];
+              TmemLd<8>::run(tl + C::T_O + c0, o);
+              tc_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), alpha));
+              TmemSt<8>::run(tl + C::T_O + c0, o);
+            }
+            tc_wait_st();
+          } else {
+            ok = false;
+          }
+        }
+        // P~ buffer j % NPB and scale column s were last read by PV(j - NPB)
+        if (ok && j >= C::NPB && !wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1)) ok = false;
+        if (ok) {
+          tc_fence_after();
+          if constexpr (!MX) gen_half(0, pw);
+          tmem_st_cols<HW>(tp, pw);
+          gen_half(1, pw);
+          tmem_st_cols<HW>(tp + HW, pw);
+          // A scales of the PV MMA: lane quadrant q reads column base + q
+          if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
+          if constexpr (!MX) {
             float a0, a1;
             upk2(acc, a0, a1);
             lsum += a0 + a1;

@@ -233,7 +233,12 @@ def run_gpu(args, w: Workload, world):
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
-def run_oracle_sample(w: Workload, budget_s=15.0):
+# which key positions of a 32-key block the oracle takes through ex2 (bit set) for
+# each exp mode: 0 the cubic everywhere, 1 ex2 everywhere, 2 the cubic at 4k+3
+MUFU_MASK = {0: 0x00000000, 1: 0xFFFFFFFF, 2: 0x77777777}
+
+
+def run_oracle_sample(w: Workload, budget_s=15.0, exp_mode=1):
     """The oracle's step-by-step emulation on a bounded sample of query rows, timed on
     the host cores; returns (TFLOP/s-equivalent, description, threads)."""
     import oracle
@@ -247,7 +252,7 @@ def run_oracle_sample(w: Workload, budget_s=15.0):
     while done < len(rows_all):
         rows = np.sort(rows_all[done:done + n])
         t0 = time.perf_counter()
-        oracle.fsa_emulate(mx, wl.Sk, wl.causal, wl.scale, fp, rows, delta=8.0, mufu_mask=0x77777777)
+        oracle.fsa_emulate(mx, wl.Sk, wl.causal, wl.scale, fp, rows, delta=8.0, mufu_mask=MUFU_MASK[exp_mode])
         dt = time.perf_counter() - t0
         i = rows % wl.Sq
         vis = np.minimum(wl.Sk, i + 1 + wl.Sk - wl.Sq) if wl.causal else np.full(len(rows), wl.Sk)
@@ -271,8 +276,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="fsa", choices=["fsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--exp-mode", type=int, default=2, choices=[0, 1, 2],
-                    help="0 cubic, 1 ex2.approx, 2 split (default)")
+    ap.add_argument("--exp-mode", type=int, default=1, choices=[0, 1, 2],
+                    help="0 cubic, 1 ex2.approx (default, the library's), 2 split 3:1")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = WORKLOADS[args.workload]
@@ -287,7 +292,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        v, desc, threads = run_oracle_sample(w, budget_s=20.0)
+        v, desc, threads = run_oracle_sample(w, budget_s=20.0, exp_mode=args.exp_mode)
         line = {"metric": metric_name(), "value": v, "unit": "TFLOP/s", "impl": "reference", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, workloads.py)", "config": config,
@@ -329,7 +334,7 @@ def main():
         "clocks": r["clocks"],
     }
     if not args.no_cpu_baseline and world == 1:
-        v, desc, threads = run_oracle_sample(w, budget_s=15.0)
+        v, desc, threads = run_oracle_sample(w, budget_s=15.0, exp_mode=args.exp_mode)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
 

@@ -29,7 +29,8 @@
  *     are detected on the host before any launch; nothing is enqueued then.
  *   - Shapes: B batch, H query heads, Hkv key/value heads (H % Hkv == 0; query
  *     head h reads kv head h / (H/Hkv)), Sq queries, Sk keys, head dim D in
- *     {64, 128}.  Causal masking is bottom-right aligned: key j is visible to
+ *     {64, 128}; B*H <= 65535, Sq <= 65535*128, Sk <= 2^24 (else INVALID_ARG).
+ *     Causal masking is bottom-right aligned: key j is visible to
  *     query i iff j <= i + Sk - Sq.  A query with no visible key gets a zero
  *     output row.
  */
@@ -114,7 +115,9 @@ typedef struct {
   float    delta;        /* fallback margin in log2 units (default 8): a later tile falls back
                             only when its maximum exceeds the frozen one by more than delta;
                             per-block scales make a stale maximum cost no precision */
-  int32_t  exp_mode;     /* fsa_exp_mode (default FSA_EXP_SPLIT) */
+  int32_t  exp_mode;     /* fsa_exp_mode (default FSA_EXP_MUFU: on sm_103a the hardware exp2
+                            issues at twice the rate of earlier parts, and the cubic's
+                            extra FMA-pipe instructions cost more than they save) */
   int32_t  efq_beta;     /* integer offset of the EFQ rule code = rne(2 r + beta) (default 2) */
   uint32_t timeout_ms;   /* limit of each on-chip wait (0: 4000 ms) */
   int32_t* row_fallbacks;/* optional device int32 [B][H][Sq]: fallback count per row */

@@ -165,7 +165,7 @@ def read_stats(stats: torch.Tensor) -> dict:
 
 
 def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
-                      causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=None, exp_mode=FSA_EXP_SPLIT,
+                      causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=None, exp_mode=None,
                       efq_beta=2, timeout_ms=0, row_fallbacks: torch.Tensor | None = None, stats=None,
                       inject_stall=False, stream=None) -> torch.Tensor:
     """O [B,H,Sq,D] fp32 by the fused MX forward (fsa_attention_fwd_ex)."""
@@ -181,7 +181,9 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
     o = default_opts()
     if delta is not None:
         o.delta = float(delta)
-    o.exp_mode, o.efq_beta = int(exp_mode), int(efq_beta)
+    if exp_mode is not None:
+        o.exp_mode = int(exp_mode)
+    o.efq_beta = int(efq_beta)
     if timeout_ms:
         o.timeout_ms = int(timeout_ms)
     o.inject_stall = int(bool(inject_stall))

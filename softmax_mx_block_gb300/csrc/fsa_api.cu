@@ -61,7 +61,7 @@ int storage_fmt(int f) { return f == FSA_FMT_E2M1_EFQ ? FSA_FMT_E2M1 : f; }
 
 bool shape_ok(int B, int H, int Hkv, int Sq, int Sk, int D) {
   return B > 0 && H > 0 && Hkv > 0 && H % Hkv == 0 && Sq > 0 && Sk > 0 && (D == 64 || D == 128) &&
-         (int64_t)B * H <= 65535 && (int64_t)Sq <= (1 << 24) && (int64_t)Sk <= (1 << 24);
+         (int64_t)B * H <= 65535 && (int64_t)Sq <= 65535 * 128 && (int64_t)Sk <= (1 << 24);
 }
 
 using ImplFn = cudaError_t (*)(const AttnLaunch&);
@@ -101,7 +101,7 @@ void fsa_default_opts(fsa_opts* o) {
   if (!o) return;
   std::memset(o, 0, sizeof(*o));
   o->delta = 8.0f;
-  o->exp_mode = FSA_EXP_SPLIT;
+  o->exp_mode = FSA_EXP_MUFU;
   o->efq_beta = 2;
   o->timeout_ms = 4000;
 }

@@ -229,8 +229,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item: heavy causal tiles first
-  const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
+  // causal: (batch, head) on the fast grid axis and query tiles heaviest first on the
+  // slow one, so blocks are dispatched longest first; otherwise query tiles of one
+  // head run together and share its K/V in L2
+  const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.y) : (int)blockIdx.x;
+  const int h = p.causal ? (int)blockIdx.x % p.H : (int)blockIdx.y;
+  const int b = p.causal ? (int)blockIdx.x / p.H : (int)blockIdx.z;
   const int kvh = h / (p.H / p.Hkv);
   const int q0 = qt * 128;
   const int nkt = (p.Sk + 127) / 128;
@@ -727,7 +731,7 @@ static cudaError_t launch_one(const AttnLaunch& a) {
   auto kern = fsa_attn_kernel<FQK, FPV, D, EXPM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.p.n_qtiles, a.p.H, a.p.B);
+  const dim3 grid = a.p.causal ? dim3(a.p.H * a.p.B, a.p.n_qtiles, 1) : dim3(a.p.n_qtiles, a.p.H, a.p.B);
   kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.p);
   return cudaGetLastError();
 }

@@ -42,7 +42,7 @@ def test_sizes_and_status(lib):
         fsa.fsa_mx_sizes(1, 1, 128, 96, 0, "E4M3")
     assert fsa.status_string(fsa.FSA_ERR_TIMEOUT) == "on-chip wait timed out"
     o = fsa.default_opts()
-    assert (o.exp_mode, o.efq_beta, o.timeout_ms, o.delta) == (fsa.FSA_EXP_SPLIT, 2, 4000, 8.0)
+    assert (o.exp_mode, o.efq_beta, o.timeout_ms, o.delta) == (fsa.FSA_EXP_MUFU, 2, 4000, 8.0)
 
 
 def test_argument_checks_reject_before_launch(lib):

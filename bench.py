@@ -33,9 +33,9 @@ DEFAULT_WORKLOAD = "prefill"
 FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
 # nominal dense ratio of each block-scaled kind to BF16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s)
 KIND_RATIO = {"E4M3": 2.0, "E2M3": 2.0, "E2M1": 6.0, "E2M1_EFQ": 6.0}
-# DRAM bytes per attention launch from an ncu capture of the current kernel build,
-# by workload (profiles/); absent until captured.
-TRAFFIC = {}
+# DRAM bytes (read + write) per attention launch from an ncu capture of the current
+# kernel build, by workload (profiles/fsa_attn_e4m3_*.md); absent: not captured
+TRAFFIC = {"prefill": 26_634_240 + 14_210_304, "long_fp8_16k": 107_855_872 + 215_160_832}
 
 
 def metric_name():

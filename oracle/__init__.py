@@ -60,12 +60,13 @@ class MxOperands(ctypes.Structure):
 
 
 class FsaOpts(ctypes.Structure):
-    _fields_ = [("delta", ctypes.c_float), ("mufu_mask", ctypes.c_uint32), ("beta", ctypes.c_int)]
+    _fields_ = [("delta", ctypes.c_float), ("mufu_mask", ctypes.c_uint32), ("beta", ctypes.c_int),
+                ("s_perturb", ctypes.c_double)]
 
 
 class FsaDump(ctypes.Structure):
     _fields_ = [("s", ctypes.c_void_p), ("p_codes", ctypes.c_void_p), ("p_scales", ctypes.c_void_p),
-                ("m_frozen", ctypes.c_void_p)]
+                ("m_frozen", ctypes.c_void_p), ("amb", ctypes.c_void_p)]
 
 
 def lib():
@@ -219,10 +220,14 @@ def attn_floor(mx: MxInputs, Sk, causal, scale, fmt_p, rows, quantize_p=True, nt
 
 
 def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_mask=0, beta=2,
-                dump=False, nthreads=None):
+                dump=False, ambiguity=False, s_perturb=0.0, nthreads=None):
     """Step-by-step emulation of the fused MX forward.  fmt_p: 0/1/2 exp path, 3 EFQ.
 
-    Returns dict(out, fallbacks, tiles) and, with dump=True, s/p_codes/p_scales/m_frozen."""
+    Returns dict(out, fallbacks, tiles); with dump=True also s/p_codes/p_scales/m_frozen;
+    with ambiguity=True also amb [rows, D]: the bound on how far a kernel output may lie
+    from `out` through code, block-exponent and fallback decisions that fp32 leaves
+    undetermined (inf for a row whose fallback decision is undetermined).
+    s_perturb (tests only) scales every raw score by 1 + s_perturb."""
     B, H, Hkv, Sq, _, D = _shape(mx, Sk)
     rows = _rows(rows)
     n = len(rows)
@@ -233,14 +238,19 @@ def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_ma
     tv = np.zeros(n, np.int32)
     res = dict(out=out, fallbacks=fb, tiles=tv)
     d = None
+    if dump or ambiguity:
+        d = FsaDump(None, None, None, None, None)
     if dump:
         res.update(s=np.zeros((n, Skp), np.float32), p_codes=np.zeros((n, Skp), np.uint8),
                    p_scales=np.zeros((n, Skp // 32), np.uint8), m_frozen=np.zeros((n, ntiles), np.float32))
-        d = FsaDump(res["s"].ctypes.data, res["p_codes"].ctypes.data, res["p_scales"].ctypes.data,
-                    res["m_frozen"].ctypes.data)
+        d.s, d.p_codes, d.p_scales, d.m_frozen = (res["s"].ctypes.data, res["p_codes"].ctypes.data,
+                                                  res["p_scales"].ctypes.data, res["m_frozen"].ctypes.data)
+    if ambiguity:
+        res["amb"] = np.zeros((n, D), np.float64)
+        d.amb = res["amb"].ctypes.data
     g = _geom(B, H, Hkv, Sq, Sk, D, causal)
     ops = mx.struct()
-    opts = FsaOpts(float(delta), int(mufu_mask) & 0xFFFFFFFF, int(beta))
+    opts = FsaOpts(float(delta), int(mufu_mask) & 0xFFFFFFFF, int(beta), float(s_perturb))
     lib().orc_fsa_emulate(ctypes.byref(ops), ctypes.byref(g), ctypes.c_float(scale), ctypes.c_int(fmt_p),
                           ctypes.byref(opts), _p(rows), ctypes.c_int64(n), _p(out), _p(fb), _p(tv),
                           ctypes.byref(d) if d is not None else None, ctypes.c_int(nthreads or nthreads_default()))

@@ -500,6 +500,7 @@ typedef struct {
   float delta;        /* fallback margin, log2 units: fall back when x > M + delta */
   uint32_t mufu_mask; /* per position in a 32-block: 1 = hardware exp2 model */
   int beta;           /* EFQ affine offset (default 2) */
+  double s_perturb;   /* test knob: raw scores are fp32(dot * (1 + s_perturb)); 0 normally */
 } orc_fsa_opts;
 
 typedef struct {      /* optional per-row dumps, NULL to skip */
@@ -507,7 +508,24 @@ typedef struct {      /* optional per-row dumps, NULL to skip */
   uint8_t* p_codes;   /* [nrows][Skp] P codes */
   uint8_t* p_scales;  /* [nrows][Skp/32] P scale bytes */
   float* m_frozen;    /* [nrows][ntiles] M after the tile's max step (NaN if skipped) */
+  double* amb;        /* [nrows][D] bound on |O_kernel - O| from undetermined decisions (below) */
 } orc_fsa_dump;
+
+/* Decisions the kernel takes in fp32 that this emulation cannot reproduce bit for
+ * bit: the tensor core's fp32 score (its internal accumulation order is not
+ * specified; modelled here as within AMB_S = 2^-21 of the sum of the absolute
+ * 32-element block dot products, i.e. a few ulps of the largest partial sum), and
+ * the hardware exp2 (within AMB_X = 2^-21 relative of 2^r).  A P code is
+ * undetermined when the interval of inputs those uncertainties allow maps to more
+ * than one code; a block exponent when its floor can go either way; a row when its
+ * fallback test can.  For each undetermined code (or whole block) the possible
+ * change dp of its value is added into B = sum dp and A_d = sum dp |v_jd|; a
+ * fallback's factor 2^(M - M') carries the relative error of M, M' and the exp2
+ * into everything accumulated before it; with
+ * o the emulated output, |O_kernel_d - o_d| <= (A_d + B |o_d|) / (l - B), which is
+ * written to amb (infinite for a row with an undetermined fallback). */
+#define AMB_S 4.76837158203125e-07   /* 2^-21 */
+#define AMB_X 4.76837158203125e-07   /* 2^-21 */
 
 static float exp2_model(float r, int use_hw, const float* pc) {
   if (use_hw) return (float)exp2((double)r);
@@ -558,28 +576,59 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
         float M = -INFINITY;
         int M_set = 0;
         float s[128];
-        double pt[128];
+        double pt[128], ds[128];                 /* ds: score uncertainty (ambiguity bound) */
+        double* A = NULL;                        /* ambiguity accumulators, when asked for */
+        double Bsum = 0.0, dM = 0.0;
+        int undetermined = 0, jM = -1;           /* jM: key whose score set M */
+        if (dump && dump->amb) {
+          A = dump->amb + n * D;
+          for (int d = 0; d < D; ++d) A[d] = 0.0;
+        }
         for (int t = 0; t * BN < nk; ++t) {
           int j0 = t * BN, j1 = j0 + BN < nk ? j0 + BN : nk;   /* visible keys of this tile */
           ++tv;
           float mx = -INFINITY;
+          int jmx = j0;
           for (int j = j0; j < j1; ++j) {
-            double acc = 0.0;
-            for (int d = 0; d < D; ++d) acc += qh[d] * kv.kh[(int64_t)j * D + d];
-            s[j - j0] = (float)acc;
-            if (s[j - j0] > mx) mx = s[j - j0];
+            double acc = 0.0, aabs = 0.0;
+            for (int d0 = 0; d0 < D; d0 += 32) {
+              double blk = 0.0;
+              for (int d = d0; d < d0 + 32; ++d) blk += qh[d] * kv.kh[(int64_t)j * D + d];
+              acc += blk;
+              aabs += fabs(blk);
+            }
+            s[j - j0] = (float)(acc * (1.0 + opt->s_perturb));
+            ds[j - j0] = AMB_S * aabs + (opt->s_perturb != 0.0 ? fabs((double)s[j - j0] * opt->s_perturb) : 0.0);
+            if (s[j - j0] > mx) { mx = s[j - j0]; jmx = j; }
           }
           float x = mx * c;
+          /* uncertainty of x (fp32 product of an uncertain score) */
+          const double dx = (double)c * ds[jmx - j0] + 1.2e-7 * fabs((double)x);
           if (!M_set) {
             M = x;
             M_set = 1;
-          } else if (x > M + opt->delta) {
-            float Mn = x;
-            double alpha = exp2((double)(M - Mn));
-            for (int d = 0; d < D; ++d) o[d] *= alpha;
-            l *= alpha;
-            M = Mn;
-            ++fb;
+            dM = dx;
+            jM = jmx;
+          } else {
+            const double thr = (double)(M + opt->delta);
+            if (A && fabs((double)x - thr) <= dx + dM + 1.2e-7 * fabs(thr)) undetermined = 1;
+            if (x > M + opt->delta) {
+              float Mn = x;
+              double alpha = exp2((double)(M - Mn));
+              for (int d = 0; d < D; ++d) o[d] *= alpha;
+              l *= alpha;
+              if (A) {
+                /* alpha itself is uncertain (M, M' and the kernel's exp2): everything
+                   accumulated so far carries that relative error */
+                const double ra = 0.6931471805599453 * (dM + dx) + AMB_X;
+                for (int d = 0; d < D; ++d) A[d] = A[d] * alpha + ra * fabs(o[d]);
+                Bsum = Bsum * alpha + ra * l;
+              }
+              M = Mn;
+              dM = dx;
+              jM = jmx;
+              ++fb;
+            }
           }
           if (dump && dump->m_frozen) dump->m_frozen[n * ntiles + t] = M;
           for (int jb = j0; jb < j1; jb += 32) {
@@ -592,9 +641,22 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
             if (E > 127) E = 127;
             float bE = M + (float)E;
             double sc = ldexp(1.0, E);
+            int blk_undet = 0;
+            if (A && smax != -INFINITY) {
+              int jsm = jb;
+              for (int j = jb; j < je; ++j) if (s[j - j0] == smax) { jsm = j; break; }
+              /* the block holding the score that set M has tmax = 0 exactly on both sides */
+              if (jM >= jb && jM < je && s[jM - j0] == smax) jsm = -1;
+              if (jsm >= 0) {
+                const double dt = (double)c * ds[jsm - j0] + dM + 1.2e-7 * (fabs((double)(smax * c)) + fabs((double)M));
+                const int Elo = (int)floor((double)tmax - dt), Ehi = (int)floor((double)tmax + dt);
+                if (Elo != Ehi && Ehi - emax > -127 && Elo - emax < 127) blk_undet = 1;
+              }
+            }
             for (int j = jb; j < je; ++j) {
               float r = fmaf(s[j - j0], c, -bE);
               uint32_t code;
+              int hw = (opt->mufu_mask >> (j % 32)) & 1;
               if (efq) {
                 double y = 2.0 * (double)r + (double)opt->beta;   /* exact */
                 double kk = nearbyint(y);                         /* ties to even */
@@ -602,10 +664,37 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
                 if (kk > 7.0) kk = 7.0;
                 code = (uint32_t)kk;
               } else {
-                int hw = (opt->mufu_mask >> (j % 32)) & 1;
                 code = orc_encode(efmt, (double)exp2_model(r, hw, pc));
               }
               pt[j - j0] = orc_decode(efmt, code) * sc;
+              if (A && s[j - j0] != -INFINITY) {
+                double dp = 0.0;
+                if (blk_undet) {
+                  /* requantised one exponent step finer or coarser */
+                  dp = 0.25 * pt[j - j0] + orc_decode(efmt, 1) * sc * 2.0;
+                } else {
+                  const double dr = (double)c * ds[j - j0] + dM + 1.2e-7 * (fabs((double)s[j - j0] * c) + fabs((double)bE));
+                  const double rlo = (double)r - dr, rhi = (double)r + dr;
+                  uint32_t clo, chi;
+                  if (efq) {
+                    double klo = nearbyint(2.0 * rlo + opt->beta), khi = nearbyint(2.0 * rhi + opt->beta);
+                    klo = klo < 0.0 ? 0.0 : (klo > 7.0 ? 7.0 : klo);
+                    khi = khi < 0.0 ? 0.0 : (khi > 7.0 ? 7.0 : khi);
+                    clo = (uint32_t)klo; chi = (uint32_t)khi;
+                  } else if (hw) {
+                    clo = orc_encode(efmt, exp2(rlo) * (1.0 - AMB_X));
+                    chi = orc_encode(efmt, exp2(rhi) * (1.0 + AMB_X));
+                  } else {
+                    clo = orc_encode(efmt, (double)exp2_model((float)rlo, 0, pc) * (1.0 - 1e-7));
+                    chi = orc_encode(efmt, (double)exp2_model((float)rhi, 0, pc) * (1.0 + 1e-7));
+                  }
+                  if (clo != chi) dp = fabs(orc_decode(efmt, chi) - orc_decode(efmt, clo)) * sc;
+                }
+                if (dp > 0.0) {
+                  Bsum += dp;
+                  for (int d = 0; d < D; ++d) A[d] += dp * fabs(kv.vh[(int64_t)d * kv.nk + j]);
+                }
+              }
               if (dump && dump->p_codes) dump->p_codes[n * Skp + j] = (uint8_t)code;
             }
             if (dump && dump->p_scales) dump->p_scales[n * (Skp / 32) + jb / 32] = (uint8_t)(E + 127);
@@ -620,6 +709,13 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
           }
         }
         for (int d = 0; d < D; ++d) o[d] = l > 0.0 ? o[d] / l : 0.0;
+        if (A) {
+          for (int d = 0; d < D; ++d) {
+            const double den = l - Bsum;
+            A[d] = undetermined ? INFINITY
+                                : (Bsum == 0.0 ? 0.0 : (den > 0.0 ? (A[d] + Bsum * fabs(o[d])) / den : INFINITY));
+          }
+        }
       }
       if (fallbacks) fallbacks[n] = fb;
       if (tiles_visited) tiles_visited[n] = tv;

@@ -1,0 +1,70 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times
+(library default options: hardware exp2 for every element, fallback margin 8), on
+256 sampled query rows per head that the oracle computes one by one.
+
+The tensor core's fp32 scores and the hardware exp2 differ from the emulation in
+the last bits, so a P code whose rounding decision lies within that uncertainty of
+a boundary may land on either side (measured: one code in a few rows per 8192 at
+16K keys).  The oracle reports, per row and column, how far such undetermined
+decisions can move the output (`amb`); the check is |O - O_emu| <= 2e-3 * rms +
+amb, element by element, and rows whose fallback decision is itself undetermined
+(amb infinite) must be under 1% of the sample."""
+import numpy as np
+import pytest
+
+import oracle
+from workloads import WORKLOADS, generate, sample_rows
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from test_gpu_attention import FMT, TOL_EMU, oracle_mx, rel_err, run_bf16, run_mx  # noqa: E402
+
+MUFU_ALL = 0xFFFFFFFF            # every key position through the hardware exp2 (the default mode)
+CASES = ["prefill", "long_fp8_16k", "long_efq_16k", "video_dit", "adversarial.L0", "adversarial.L1"]
+
+
+def _workload(name):
+    base, _, layer = name.partition(".L")
+    w = WORKLOADS[base]
+    return w.layer(int(layer)) if w.layers > 1 else w
+
+
+@pytest.mark.parametrize("name", CASES)
+def test_full_size_sampled_rows(name):
+    w = _workload(name)
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    gpu = run_mx(w, q, k, v, exp_mode=None, delta=None, row_fb=True)
+    assert gpu["stats"]["status"] == 0
+    fq, fp = FMT[w.fmt_qk], FMT[w.fmt_pv]
+    mx = oracle.MxInputs.from_bf16(q, k, v, fq, 2 if fp == 3 else fp)
+    orc = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=8.0, mufu_mask=MUFU_ALL, ambiguity=True)
+    emu, amb = orc["out"], orc["amb"]
+    o = gpu["out"][rows]
+    undetermined = np.isinf(amb).any(axis=1)
+    assert np.mean(undetermined) < 0.01
+    tol = TOL_EMU * np.sqrt(np.mean(emu ** 2))
+    excess = (np.abs(o - emu) - amb - tol)[~undetermined]
+    assert np.all(excess <= 0.0), f"{name}: |O-O_emu| exceeds 2e-3*rms + amb by {excess.max():.3e}"
+    # the fallback decision compares fp32 scores; rare one-ulp ties may differ
+    assert np.mean(gpu["row_fallbacks"][rows] != orc["fallbacks"]) < 0.01
+    assert gpu["stats"]["fallback_events"] == int(gpu["row_fallbacks"].sum())
+    # error against fp64 exact attention within the operand-quantisation floor, on
+    # every eighth sampled row (the exact and floor oracles cost as much again)
+    sub = rows[::8]
+    fl = oracle_mx(w, q, k, v, sub, MUFU_ALL, delta=8.0, with_floor=True)
+    ratio = 2.0 if w.fmt_pv == "E2M1_EFQ" else 1.1
+    e_gpu, e_floor = rel_err(gpu["out"][sub], fl["exact"]), rel_err(fl["floor"], fl["exact"])
+    assert e_gpu <= ratio * e_floor, f"{name}: error {e_gpu:.4f} vs floor {e_floor:.4f}"
+
+
+def test_bf16_full_size_sampled_rows():
+    w = WORKLOADS["prefill"]
+    q, k, v = generate(w)
+    rows = sample_rows(w)
+    out, st = run_bf16(w, q, k, v)
+    emu = oracle.bf16_emulate(q, k, v, w.causal, w.scale, rows)["out"]
+    o = out[rows]
+    assert np.abs(o - emu).max() / np.sqrt(np.mean(emu ** 2)) < 5e-3
+    assert st["status"] == 0

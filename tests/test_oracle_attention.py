@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from workloads import to_bf16_bits, bf16_bits_to_f32
+from workloads import WORKLOADS, Workload, bf16_bits_to_f32, generate, sample_rows, small, to_bf16_bits
 
 
 def bf(x):
@@ -254,3 +254,29 @@ def test_bf16_emulate_pins():
     kk[0, 0, 200] = 8.0 * bf16_bits_to_f32(q)[0, 0, 250]
     r = oracle.bf16_emulate(q, bf(kk), v, False, 0.125, rows)
     assert r["rescales"][250] == 1
+
+
+@pytest.mark.parametrize("fq,fp,mufu", [(0, 0, 0xFFFFFFFF), (0, 0, 0), (2, 3, 0), (1, 2, 0x77777777)])
+def test_emulate_ambiguity_bound_covers_score_perturbations(fq, fp, mufu):
+    """amb bounds how far the output can move when the fp32 scores move within the
+    modelled uncertainty: rerun the emulation with every score scaled by 1 +- 2^-21
+    and 1 +- 2^-22 (coherently, inside the per-score interval) and check each change
+    against the unperturbed bound.  The case is large enough that codes do flip."""
+    w = small(WORKLOADS["prefill"], 1024, H=4, Hkv=2)
+    w = Workload(w.name, w.B, w.H, w.Hkv, w.Sq, w.Sk, w.D, w.causal, ["E4M3", "E2M3", "E2M1"][fq],
+                 ["E4M3", "E2M3", "E2M1", "E2M1_EFQ"][fp], w.seed, w.kind)
+    q, k, v = generate(w)
+    fv = 2 if fp == 3 else fp
+    mx = oracle.MxInputs.from_bf16(q, k, v, fq, fv)
+    rows = np.arange(w.B * w.H * w.Sq)
+    base = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=8.0, mufu_mask=mufu, ambiguity=True)
+    amb = base["amb"]
+    assert np.all(amb >= 0.0)
+    assert np.mean(np.isinf(amb).any(axis=1)) < 0.01
+    moved = 0
+    for eps in (2.0 ** -21, -2.0 ** -21, 2.0 ** -22, -2.0 ** -22):
+        pert = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=8.0, mufu_mask=mufu, s_perturb=eps)
+        diff = np.abs(pert["out"] - base["out"])
+        moved += int(np.sum(diff.max(axis=1) > 1e-12))
+        assert np.all(diff <= amb * (1 + 1e-9) + 1e-12), f"eps {eps}: {np.max(diff - amb):.3e}"
+    assert moved > 0

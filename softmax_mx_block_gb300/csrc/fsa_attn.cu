@@ -359,28 +359,22 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // commits cover all of them).  One warp issues both GEMMs: tcgen05 work from two
     // issuing warps of one CTA was measured to serialise badly.
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      bool r = false;
-      if (lane == 0) r = mbar_wait<false>(bar, parity, ac);
-      return __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+      return __all_sync(0xffffffffu, mbar_wait<false>(bar, parity, ac));
     };
     if (nT > 0) {
       const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
       constexpr uint32_t SWQ = swz_code(C::W_QK), SWV = swz_code(C::W_V);
       bool ok = true;
-      if (p.inject_stall) {                                     // nobody arrives: the wait must expire
-        bool r = false;
-        if (lane == 0) r = mbar_wait(stall, 0, ac);
-        ok = __shfl_sync(0xffffffffu, (int)r, 0) != 0;
-      }
+      if (p.inject_stall) ok = __all_sync(0xffffffffu, mbar_wait(stall, 0, ac));   // nobody arrives: must expire
       ok = ok && wait_all(q_full, 0);
       if (ok) {
         tc_fence_after();
         if constexpr (MX) {
-          if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFQ, smem_desc(smem_u32(sm + C::OFF_SFQ), 16, 128, 0));
+          tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFQ, smem_desc(smem_u32(sm + C::OFF_SFQ), 16, 128, 0));
           if constexpr (D == 128) {
             const uint64_t one = smem_desc(smem_u32(sm + C::OFF_SFONE), 16, 128, 0);
-            if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFV + 4, one);
-            if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFV + 12, one);
+            tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 4, one);
+            tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 12, one);
           }
         }
       }
@@ -389,7 +383,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
         if constexpr (MX) {
           const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFV + st * 512), 16, 128, 0);
-          if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFV + 8 * s, sfd);
+          tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 8 * s, sfd);
         }
 #pragma unroll
         for (int i = 0; i < C::PV_STEPS; ++i) {
@@ -400,26 +394,25 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int ka = (i * 32) / C::W_V, off = (i * 32) % C::W_V;
           const uint64_t bd = smem_desc(sVa + st * C::TILE_V + ka * C::VATOM + off, 16, 8 * C::W_V, SWV);
           const uint32_t acc = (jj > 0 || i > 0) ? 1u : 0u;
-          if (elect_one()) {
-            if constexpr (KIND_PV == 0) {
-              mma_f16_ts(tbase + C::T_O, a_tm, bd, idesc_f16_bf16(C::N_PV), acc);
-            } else if constexpr (KIND_PV == 1) {
-              mma_mxf8f6f4_ts(tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, Fmt<FPV>::code, i, i), sfa,
+          const uint32_t e = elect_u32();
+          if constexpr (KIND_PV == 0) {
+            mma_f16_ts_p(e, tbase + C::T_O, a_tm, bd, idesc_f16_bf16(C::N_PV), acc);
+          } else if constexpr (KIND_PV == 1) {
+            mma_mxf8f6f4_ts_p(e, tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, Fmt<FPV>::code, i, i), sfa,
                               tbase + C::T_SFV + 8 * s, acc);
-            } else {
-              mma_mxf4_ts(tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, 1, 2 * i, 2 * i), sfa, tbase + C::T_SFV + 8 * s,
-                          acc);
-            }
+          } else {
+            mma_mxf4_ts_p(e, tbase + C::T_O, a_tm, bd, idesc_bs(C::N_PV, 1, 2 * i, 2 * i), sfa,
+                          tbase + C::T_SFV + 8 * s, acc);
           }
         }
-        if (elect_one()) tc_commit(pv_done + st);
+        tc_commit_p(elect_u32(), pv_done + st);
       };
       auto issue_s = [&](int j) {
         const int s = j & 1, st = j % C::NS;
         tc_fence_after();
         if constexpr (MX) {
           const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFK + st * 512), 16, 128, 0);
-          if (elect_one()) tc_cp_sf_atom(tbase + C::T_SFK + 4 * s, sfd);
+          tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFK + 4 * s, sfd);
         }
 #pragma unroll
         for (int i = 0; i < C::QK_STEPS; ++i) {
@@ -427,20 +420,19 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const uint64_t ad = smem_desc(sQa + ka * 128 * C::W_QK + off, 16, 8 * C::W_QK, SWQ);
           const uint64_t bd = smem_desc(sKa + st * C::TILE_QK + ka * 128 * C::W_QK + off, 16, 8 * C::W_QK, SWQ);
           const uint32_t acc = i > 0 ? 1u : 0u;
-          if (elect_one()) {
-            if constexpr (KIND_QK == 0) {
-              mma_f16_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_f16_bf16(128), acc);
-            } else if constexpr (KIND_QK == 1) {
-              mma_mxf8f6f4_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, Fmt<FQK>::code, i, i),
+          const uint32_t e = elect_u32();
+          if constexpr (KIND_QK == 0) {
+            mma_f16_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_f16_bf16(128), acc);
+          } else if constexpr (KIND_QK == 1) {
+            mma_mxf8f6f4_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, Fmt<FQK>::code, i, i),
                               tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
-            } else {
-              mma_mxf4_ss(tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, 1, 2 * i, 2 * i),
+          } else {
+            mma_mxf4_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, 1, 2 * i, 2 * i),
                           tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
-            }
           }
         }
-        if (elect_one()) tc_commit(s_full + s);
-        if (elect_one()) tc_commit(k_empty + st);
+        tc_commit_p(elect_u32(), s_full + s);
+        tc_commit_p(elect_u32(), k_empty + st);
       };
       // Non-blocking scheduler: each round lane 0 tests the barriers of the next
       // QK^T (K(jS) landed, S buffer loaded by its owners) and of the next PV (P~(jP)
@@ -451,49 +443,39 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t idle = 0;
       uint64_t t0 = 0;
       while (ok && jP < nT) {
-        int rdy = 0;
-        if (lane == 0) {
-          if (jS < nT && mbar_test(k_full + jS % C::NS, (jS / C::NS) & 1) &&
-              (jS < 2 || mbar_test(s_free + (jS & 1), ((jS - 2) >> 1) & 1)))
-            rdy |= 1;
-          if (jP < jS && mbar_test(p_full + (jP & 1), (jP >> 1) & 1) &&
-              mbar_test(v_full + jP % C::NS, (jP / C::NS) & 1))
-            rdy |= 2;
-        }
-        rdy = __shfl_sync(0xffffffffu, rdy, 0);
-        if (rdy & 1) issue_s(jS++);
-        if (rdy & 2) issue_pv(jP++);
-        if (rdy) {
+        // every lane tests (all four tests in flight together), the votes agree
+        const bool tk = jS < nT && mbar_test(k_full + jS % C::NS, (jS / C::NS) & 1);
+        const bool tf = jS < 2 || mbar_test(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
+        const bool tp = jP < jS && mbar_test(p_full + (jP & 1), (jP >> 1) & 1);
+        const bool tv = mbar_test(v_full + jP % C::NS, (jP / C::NS) & 1);
+        const bool rs = __all_sync(0xffffffffu, tk && tf), rp = __all_sync(0xffffffffu, tp && tv);
+        if (rs) issue_s(jS++);
+        if (rp) issue_pv(jP++);
+        if (rs || rp) {
           idle = 0;
           continue;
         }
         // nothing ready: park in a suspending try_wait on what most likely completes
         // next (P~(jP) once QK^T has run ahead, else the next QK^T's inputs), so the
         // warp takes no issue slots from the softmax warps of its scheduler
-        if (lane == 0) {
-          if (jP < jS && (jS >= nT || jS - jP >= 2)) mbar_try_wait(p_full + (jP & 1), (jP >> 1) & 1);
-          else if (jS < nT && !mbar_test(k_full + jS % C::NS, (jS / C::NS) & 1))
-            mbar_try_wait(k_full + jS % C::NS, (jS / C::NS) & 1);
-          else if (jS < nT && jS >= 2) mbar_try_wait(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
-        }
+        if (jP < jS && (jS >= nT || jS - jP >= 2)) mbar_try_wait(p_full + (jP & 1), (jP >> 1) & 1);
+        else if (jS < nT && !tk) mbar_try_wait(k_full + jS % C::NS, (jS / C::NS) & 1);
+        else if (jS < nT && jS >= 2) mbar_try_wait(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
         __syncwarp();
         // bounded wait, abort check
         if (++idle == 1) t0 = globaltimer_ns();
         if ((idle & 7u) == 0) {
-          int stop = 0;
-          if (lane == 0) {
-            if (*ac.flag) stop = 1;
-            else if (globaltimer_ns() - t0 > ac.limit_ns) {
-              *ac.flag = 1;
-              if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
-              stop = 1;
-            }
+          bool stop = *ac.flag != 0;
+          if (!stop && globaltimer_ns() - t0 > ac.limit_ns) {
+            *ac.flag = 1;
+            if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
+            stop = true;
           }
-          if (__shfl_sync(0xffffffffu, stop, 0)) ok = false;
+          if (__any_sync(0xffffffffu, stop)) ok = false;
         }
       }
       // all MMAs and copies issued by this warp complete before tensor memory is freed
-      if (elect_one()) tc_commit(drain);
+      tc_commit_p(elect_u32(), drain);
       mbar_wait_drain(drain, 0, p.timeout_ns);
     }
     __syncwarp();
@@ -521,11 +503,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     bool ok = true;                                 // false once any wait failed: no more work
     // BF16: the denominator is summed here, per part, relative to the part's latest M
     float lsum = 0.0f, Ml = kNegInf;
-    // lane 0 polls and broadcasts: 32 lanes polling one mbarrier serialise
+    // every lane polls; the vote keeps the warp uniform
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
-      bool r = false;
-      if (lane == 0) r = mbar_wait<false>(bar, parity, ac);
-      return __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+      return __all_sync(0xffffffffu, mbar_wait<false>(bar, parity, ac));
     };
     for (int j = pp; j < nT; j += 2) {
       const int s = pp;
@@ -543,7 +523,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // S(j) is in registers: its buffer may take S(j+2)
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_free + s);
+        mbar_arrive_elect(s_free + s);
 #pragma unroll
         for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(raw[i]);
         if (128 * j + 127 > lim) {                  // only diagonal / tail tiles mask keys
@@ -655,7 +635,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(p_full + s);
+        if (ok) mbar_arrive_elect(p_full + s);
       }
     }
     // ---- epilogue: O = O_aug[:, :D] / l, D/2 columns per part

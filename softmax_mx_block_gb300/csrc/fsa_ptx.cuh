@@ -100,6 +100,19 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
+// 1 in the elected lane of a converged warp, else 0 (a value for the predicated
+// forms below, so no branch diverges the warp)
+__device__ __forceinline__ uint32_t elect_u32() {
+  uint32_t e;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.b32 %0, 1, 0, p;\n}" : "=r"(e));
+  return e;
+}
+// mbarrier arrive by the elected lane only (whole warp converged)
+__device__ __forceinline__ void mbar_arrive_elect(uint64_t* bar) {
+  asm volatile("{\n .reg .pred e;\n .reg .b64 st;\n elect.sync _|e, 0xffffffff;\n"
+               " @e mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA / bulk
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y, int z) {
   asm volatile(
@@ -188,6 +201,52 @@ __device__ __forceinline__ void mma_mxf4_ts(uint32_t d, uint32_t a_tmem, uint64_
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
                "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n}"
                ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
+
+// Predicated forms: issued only where e != 0 (the warp stays converged).
+__device__ __forceinline__ void tc_commit_p(uint32_t e, uint64_t* bar) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
+               "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}"
+               ::"r"(smem_u32(bar)), "r"(e) : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf_atom_p(uint32_t e, uint32_t taddr, uint64_t sdesc) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+               "@q tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}" ::"r"(taddr), "l"(sdesc), "r"(e) : "memory");
+}
+__device__ __forceinline__ void mma_f16_ss_p(uint32_t e, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(e) : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_p(uint32_t e, uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(e) : "memory");
+}
+__device__ __forceinline__ void mma_mxf8f6f4_ss_p(uint32_t e, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                  uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
+}
+__device__ __forceinline__ void mma_mxf8f6f4_ts_p(uint32_t e, uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                  uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
+}
+__device__ __forceinline__ void mma_mxf4_ss_p(uint32_t e, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
+}
+__device__ __forceinline__ void mma_mxf4_ts_p(uint32_t e, uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
 }
 
 // Shared-memory matrix descriptor: start address, stride between 8-row core

@@ -662,14 +662,19 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_ld_cols<DP>(tl + C::T_O + DP * pp, o);
       tc_wait_ld();
       const float l = MX ? __uint_as_float(lraw) : lb;
+      // fp32 normalisation: one correctly rounded reciprocal of l per row, then products
+      // (within 1.5 ulp of the quotient).  A row with no visible key has l = 0 (or
+      // NaN: its residuals are -inf + inf) and gets zeros.
+      const bool lpos = l > 0.f;
+      const float rinv = lpos ? __frcp_rn(l) : 0.f;
       if (row_valid) {
 #pragma unroll
         for (int i = 0; i < DP; i += 4) {
           float4 v;
-          v.x = l > 0.f ? __fdiv_rn(__uint_as_float(o[i]), l) : 0.f;
-          v.y = l > 0.f ? __fdiv_rn(__uint_as_float(o[i + 1]), l) : 0.f;
-          v.z = l > 0.f ? __fdiv_rn(__uint_as_float(o[i + 2]), l) : 0.f;
-          v.w = l > 0.f ? __fdiv_rn(__uint_as_float(o[i + 3]), l) : 0.f;
+          v.x = lpos ? __fmul_rn(__uint_as_float(o[i]), rinv) : 0.f;
+          v.y = lpos ? __fmul_rn(__uint_as_float(o[i + 1]), rinv) : 0.f;
+          v.z = lpos ? __fmul_rn(__uint_as_float(o[i + 2]), rinv) : 0.f;
+          v.w = lpos ? __fmul_rn(__uint_as_float(o[i + 3]), rinv) : 0.f;
           *reinterpret_cast<float4*>(orow + i) = v;
         }
       }

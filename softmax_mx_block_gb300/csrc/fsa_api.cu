@@ -50,6 +50,20 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of the fp32 output O [planes][rows][D]: boxes of 32 rows x 32 floats
+// (128 bytes), 128B swizzle, written by TMA stores from the kernel's epilogue.
+bool make_tmap_out(CUtensorMap* m, float* base, uint64_t D, uint64_t rows, uint64_t planes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {D, rows, planes};
+  const cuuint64_t strides[2] = {D * 4, D * 4 * rows};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // storage bits per element * 2, as the kernels store them
 int bits2_of(int fmt) { return fmt == FSA_FMT_E2M1 || fmt == FSA_FMT_E2M1_EFQ ? 8 : 16; }
 
@@ -193,7 +207,8 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
   const uint32_t wv = rbv_tile < 128 ? rbv_tile : 128;
   if (!make_tmap(&a.tq, q->codes, rbq, Sq, (uint64_t)B * H, wq, 128) ||
       !make_tmap(&a.tk, k->codes, rbq, Sk, (uint64_t)B * Hkv, wq, 128) ||
-      !make_tmap(&a.tv, v->codes, rbv_total, D, (uint64_t)B * Hkv, wv, D))
+      !make_tmap(&a.tv, v->codes, rbv_total, D, (uint64_t)B * Hkv, wv, D) ||
+      !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H))
     return FSA_ERR_LAUNCH;
   fill_common(a.p, B, H, Hkv, Sq, Sk, causal, scale, &o, stats);
   a.p.sf_q = q->scales; a.p.sf_k = k->scales; a.p.sf_v = v->scales;
@@ -223,7 +238,8 @@ int fsa_attention_fwd_bf16(const void* q, const void* k, const void* vt, float* 
   const uint64_t Sp = (uint64_t)(Sk + 127) / 128 * 128;
   if (!make_tmap(&a.tq, q, 2 * D, Sq, (uint64_t)B * H, 128, 128) ||
       !make_tmap(&a.tk, k, 2 * D, Sk, (uint64_t)B * Hkv, 128, 128) ||
-      !make_tmap(&a.tv, vt, 2 * Sp, D, (uint64_t)B * Hkv, 128, D))
+      !make_tmap(&a.tv, vt, 2 * Sp, D, (uint64_t)B * Hkv, 128, D) ||
+      !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H))
     return FSA_ERR_LAUNCH;
   fill_common(a.p, B, H, Hkv, Sq, Sk, causal, scale, &o, stats);
   a.p.out = out;

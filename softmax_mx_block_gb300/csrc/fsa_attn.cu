@@ -220,7 +220,8 @@ namespace fsa {
 template <int FQK, int FPV, int D, int EXPM>
 __global__ void __launch_bounds__(Cfg<FQK, FPV, D>::NTHREADS, 1)
 fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const KParams p) {
   using C = Cfg<FQK, FPV, D>;
   constexpr int KIND_QK = Fmt<FQK>::kind, KIND_PV = Fmt<FPV>::kind;
   constexpr bool MX = C::MX;
@@ -652,35 +653,55 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
            (m1 != kNegInf ? l1 * ex2_approx(__fsub_rn(m1, mf)) : 0.0f);
       named_bar_sync(9 + qd, 64);                    // both have read before the slots are reused
     }
-    float* orow = p.out + (((size_t)b * p.H + h) * p.Sq + (row_valid ? row : 0)) * D + DP * pp;
+    // O rows go out through shared memory and TMA: each warp writes its 32 rows x DP
+    // columns as 32x32 fp32 boxes (128B swizzle) into the K/V ring, which no copy or
+    // MMA uses any more, and one lane stores them (rows past Sq are clipped).
+    constexpr int NBOX = DP / 32;                    // boxes per warp
     const bool done = ok && nT > 0 && wait0(pv_done + (nT - 1) % C::NS, ((nT - 1) / C::NS) & 1);
-    if (done) {
-      tc_fence_after();
-      uint32_t lraw = 0;
-      if constexpr (MX) TmemLd<1>::run(tl + C::T_O + D, &lraw);
+    if (done || nT == 0) {
       uint32_t o[DP];
-      tmem_ld_cols<DP>(tl + C::T_O + DP * pp, o);
-      tc_wait_ld();
-      const float l = MX ? __uint_as_float(lraw) : lb;
+      float l = 0.f;
+      if (done) {
+        tc_fence_after();
+        uint32_t lraw = 0;
+        if constexpr (MX) TmemLd<1>::run(tl + C::T_O + D, &lraw);
+        tmem_ld_cols<DP>(tl + C::T_O + DP * pp, o);
+        tc_wait_ld();
+        l = MX ? __uint_as_float(lraw) : lb;
+      }
       // fp32 normalisation: one correctly rounded reciprocal of l per row, then products
       // (within 1.5 ulp of the quotient).  A row with no visible key has l = 0 (or
       // NaN: its residuals are -inf + inf) and gets zeros.
       const bool lpos = l > 0.f;
       const float rinv = lpos ? __frcp_rn(l) : 0.f;
-      if (row_valid) {
+      fence_proxy_async_smem();                      // the ring was last written by TMA loads
 #pragma unroll
-        for (int i = 0; i < DP; i += 4) {
+      for (int t = 0; t < NBOX; ++t) {
+        uint8_t* box = sm + C::OFF_OSTAGE + (qd * (D / 32) + (DP * pp) / 32 + t) * 4096;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
           float4 v;
-          v.x = lpos ? __fmul_rn(__uint_as_float(o[i]), rinv) : 0.f;
-          v.y = lpos ? __fmul_rn(__uint_as_float(o[i + 1]), rinv) : 0.f;
-          v.z = lpos ? __fmul_rn(__uint_as_float(o[i + 2]), rinv) : 0.f;
-          v.w = lpos ? __fmul_rn(__uint_as_float(o[i + 3]), rinv) : 0.f;
-          *reinterpret_cast<float4*>(orow + i) = v;
+          const uint32_t* src = o + 32 * t + 4 * ch;
+          v.x = lpos ? __fmul_rn(__uint_as_float(src[0]), rinv) : 0.f;
+          v.y = lpos ? __fmul_rn(__uint_as_float(src[1]), rinv) : 0.f;
+          v.z = lpos ? __fmul_rn(__uint_as_float(src[2]), rinv) : 0.f;
+          v.w = lpos ? __fmul_rn(__uint_as_float(src[3]), rinv) : 0.f;
+          // 128B swizzle: 16-byte chunk ch of row `lane` sits at chunk ch ^ (lane % 8)
+          *reinterpret_cast<float4*>(box + lane * 128 + ((ch ^ (lane & 7)) << 4)) = v;
         }
       }
-    } else if (nT == 0 && row_valid) {
+      fence_proxy_async_smem();                      // generic writes -> TMA reads
+      __syncwarp();
+      if (lane == 0) {
+        const int bh = b * p.H + h;
 #pragma unroll
-      for (int i = 0; i < DP; i += 4) *reinterpret_cast<float4*>(orow + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t = 0; t < NBOX; ++t)
+          tma_store_3d(&tm_o, sm + C::OFF_OSTAGE + (qd * (D / 32) + (DP * pp) / 32 + t) * 4096,
+                       DP * pp + 32 * t, q0 + 32 * qd, bh);
+        bulk_commit_group();
+        bulk_wait_all();                             // before the CTA (and its shared memory) ends
+      }
+      __syncwarp();
     }
     // ---- statistics: each part counted the tiles it owns
     int* nfb_other = reinterpret_cast<int*>(red) + 128 + rl;
@@ -717,7 +738,7 @@ static cudaError_t launch_one(const AttnLaunch& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid = a.p.causal ? dim3(a.p.H * a.p.B, a.p.n_qtiles, 1) : dim3(a.p.n_qtiles, a.p.H, a.p.B);
-  kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.p);
+  kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.to, a.p);
   return cudaGetLastError();
 }
 

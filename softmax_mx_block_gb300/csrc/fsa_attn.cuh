@@ -70,6 +70,9 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
   static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  // the epilogue stages O (128 rows x D fp32, 32x32 boxes) in the K/V ring, free by then
+  static constexpr int OFF_OSTAGE = OFF_K;
+  static_assert(OFF_K + 128 * D * 4 <= OFF_SF, "O staging fits the K/V ring");
   // ---- tensor memory columns
   static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256)
   static constexpr uint32_t T_O = 256;        // [256, 256 + N_PV)

@@ -7,7 +7,7 @@
 namespace fsa {
 
 struct AttnLaunch {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;   // Q, K, V^T codes; fp32 output
   KParams p;
   int D;
   int exp_mode;          // 0 poly, 1 MUFU, 2 split (ignored for EFQ and BF16)

@@ -35,7 +35,7 @@ FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
 KIND_RATIO = {"E4M3": 2.0, "E2M3": 2.0, "E2M1": 6.0, "E2M1_EFQ": 6.0}
 # DRAM bytes (read + write) per attention launch from an ncu capture of the current
 # kernel build, by workload (profiles/fsa_attn_e4m3_*.md); absent: not captured
-TRAFFIC = {"prefill": 26_401_280 + 13_305_344, "long_fp8_16k": 106_589_184 + 215_014_144}
+TRAFFIC = {"prefill": 26_019_072 + 10_541_824, "long_fp8_16k": 106_343_168 + 212_194_560}
 
 
 def metric_name():

@@ -318,38 +318,46 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == 0) {
     // =============================================================== producer
-    if (lane == 0 && nT > 0) {
-      int nk = 0, nv = 0;                           // tiles whose K / V copies were started
+    // Lane 0 loads Q and the K tiles, lane 1 the V tiles: a K tile waits only for
+    // its own ring slot, never behind a V slot that a late PV still holds.
+    if (lane < 2 && nT > 0) {
       const int bhq = b * p.H + h, bhk = b * p.Hkv + kvh;
-      mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
-#pragma unroll
-      for (int ka = 0; ka < C::NKA_QK; ++ka)
-        tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
-      if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
-      for (int j = 0; j < nT; ++j) {
-        const int st = j % C::NS;
-        // K slot st is free once S(j - NS) is done, V slot st once PV(j - NS) is
-        if (j >= C::NS && !mbar_wait(k_empty + st, ((j - C::NS) / C::NS) & 1, ac)) break;
-        mbar_expect_tx(k_full + st, C::TILE_QK + (MX ? 512 : 0));
+      if (lane == 0) {
+        // Q, then K(j) as soon as K slot j % NS is free (S(j - NS) done)
+        int nk = 0;
+        mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
 #pragma unroll
         for (int ka = 0; ka < C::NKA_QK; ++ka)
-          tma_load_3d(sK + st * C::TILE_QK + ka * 128 * C::W_QK, &tm_k, k_full + st, ka * C::W_QK, j * 128, bhk);
-        if (MX) bulk_load(sm + C::OFF_SFK + st * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + st);
-        ++nk;
-        if (j >= C::NS && !mbar_wait(pv_done + st, ((j - C::NS) / C::NS) & 1, ac)) break;
-        mbar_expect_tx(v_full + st, C::TILE_V_TMA + (MX ? 512 : 0));
+          tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
+        if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
+        for (int j = 0; j < nT; ++j) {
+          const int st = j % C::NS;
+          if (j >= C::NS && !mbar_wait(k_empty + st, ((j - C::NS) / C::NS) & 1, ac)) break;
+          mbar_expect_tx(k_full + st, C::TILE_QK + (MX ? 512 : 0));
 #pragma unroll
-        for (int ka = 0; ka < C::NKA_V; ++ka)
-          tma_load_3d(sV + st * C::TILE_V + ka * C::VATOM, &tm_v, v_full + st, j * C::RB_V + ka * C::W_V, 0, bhk);
-        if (MX) bulk_load(sm + C::OFF_SFV + st * 512, p.sf_v + ((size_t)bhk * nkt + j) * 512, 512, v_full + st);
-        ++nv;
-      }
-      // every copy this thread started has landed before the CTA tears down
-      mbar_wait_drain(q_full, 0, p.timeout_ns);
-      for (int st = 0; st < C::NS; ++st) {
-        // copies started into slot st: (n - 1 - st) / NS + 1 of the first n tiles
-        if (st < nk) mbar_wait_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, p.timeout_ns);
-        if (st < nv) mbar_wait_drain(v_full + st, ((nv - 1 - st) / C::NS) & 1, p.timeout_ns);
+          for (int ka = 0; ka < C::NKA_QK; ++ka)
+            tma_load_3d(sK + st * C::TILE_QK + ka * 128 * C::W_QK, &tm_k, k_full + st, ka * C::W_QK, j * 128, bhk);
+          if (MX) bulk_load(sm + C::OFF_SFK + st * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + st);
+          ++nk;
+        }
+        mbar_wait_drain(q_full, 0, p.timeout_ns);
+        for (int st = 0; st < C::NS && st < nk; ++st)
+          mbar_wait_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, p.timeout_ns);
+      } else {
+        // V(j) as soon as V slot j % NS is free (PV(j - NS) done)
+        int nv = 0;
+        for (int j = 0; j < nT; ++j) {
+          const int st = j % C::NS;
+          if (j >= C::NS && !mbar_wait(pv_done + st, ((j - C::NS) / C::NS) & 1, ac)) break;
+          mbar_expect_tx(v_full + st, C::TILE_V_TMA + (MX ? 512 : 0));
+#pragma unroll
+          for (int ka = 0; ka < C::NKA_V; ++ka)
+            tma_load_3d(sV + st * C::TILE_V + ka * C::VATOM, &tm_v, v_full + st, j * C::RB_V + ka * C::W_V, 0, bhk);
+          if (MX) bulk_load(sm + C::OFF_SFV + st * 512, p.sf_v + ((size_t)bhk * nkt + j) * 512, 512, v_full + st);
+          ++nv;
+        }
+        for (int st = 0; st < C::NS && st < nv; ++st)
+          mbar_wait_drain(v_full + st, ((nv - 1 - st) / C::NS) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -457,11 +465,18 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           continue;
         }
         // nothing ready: park in a suspending try_wait on what most likely completes
-        // next (P~(jP) once QK^T has run ahead, else the next QK^T's inputs), so the
-        // warp takes no issue slots from the softmax warps of its scheduler
-        if (jP < jS && (jS >= nT || jS - jP >= 2)) mbar_try_wait(p_full + (jP & 1), (jP >> 1) & 1);
-        else if (jS < nT && !tk) mbar_try_wait(k_full + jS % C::NS, (jS / C::NS) & 1);
-        else if (jS < nT && jS >= 2) mbar_try_wait(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
+        // next, so the warp takes no issue slots from the softmax warps of its
+        // scheduler.  The owners of tile j release S(j) when they load it, early in
+        // the tile, and write P~(j) at its end; the other part's tiles are half a tile
+        // behind.  So the release of S(jS-2) comes before P~(jP) unless PV lags QK^T
+        // by four tiles or more.
+        if (jS < nT && jS - jP <= 3) {
+          if (!tk) mbar_try_wait(k_full + jS % C::NS, (jS / C::NS) & 1);
+          else if (jS >= 2) mbar_try_wait(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
+        } else if (jP < jS) {
+          if (!tp) mbar_try_wait(p_full + (jP & 1), (jP >> 1) & 1);
+          else mbar_try_wait(v_full + jP % C::NS, (jP / C::NS) & 1);
+        }
         __syncwarp();
         // bounded wait, abort check
         if (++idle == 1) t0 = globaltimer_ns();
@@ -601,7 +616,10 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // are warp-collective, so the whole warp rescales when any of its rows falls
         // back; the other rows multiply by exactly 1.
         if (__any_sync(0xffffffffu, rescale)) {
-          if (wait0(pv_done + (j - 1) % C::NS, ((j - 1) / C::NS) & 1)) {
+          // PV(j-2) first: with two PV barriers (BF16) PV(j-1) shares its barrier with
+          // PV(j-3), and its parity only identifies PV(j-1) once PV(j-3) has completed
+          const bool prev = j < C::NPB || wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1);
+          if (prev && wait0(pv_done + (j - 1) % C::NS, ((j - 1) / C::NS) & 1)) {
             tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < C::N_PV; c0 += 8) {
@@ -657,7 +675,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // columns as 32x32 fp32 boxes (128B swizzle) into the K/V ring, which no copy or
     // MMA uses any more, and one lane stores them (rows past Sq are clipped).
     constexpr int NBOX = DP / 32;                    // boxes per warp
-    const bool done = ok && nT > 0 && wait0(pv_done + (nT - 1) % C::NS, ((nT - 1) / C::NS) & 1);
+    // PV(nT-2) before PV(nT-1), for the same parity reason as the rescale wait
+    const bool done = ok && nT > 0 && (nT < 2 || wait0(pv_done + (nT - 2) % C::NS, ((nT - 2) / C::NS) & 1)) &&
+                      wait0(pv_done + (nT - 1) % C::NS, ((nT - 1) / C::NS) & 1);
     if (done || nT == 0) {
       uint32_t o[DP];
       float l = 0.f;

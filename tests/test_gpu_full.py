@@ -68,3 +68,25 @@ def test_bf16_full_size_sampled_rows():
     o = out[rows]
     assert np.abs(o - emu).max() / np.sqrt(np.mean(emu ** 2)) < 5e-3
     assert st["status"] == 0
+
+
+@pytest.mark.parametrize("name", ["prefill", "long_fp8_16k.bf16", "long_efq_16k"])
+def test_repeated_launches_bit_identical(name):
+    """Every output element is a fixed sequence of fp32 operations, so three launches
+    on the same inputs agree bit for bit.  A read of tensor memory or shared memory
+    before the MMA or copy that fills it finishes (a barrier phase taken for the wrong
+    one) shows up as a difference here even where the error is small."""
+    base, _, kind = name.partition(".")
+    w = WORKLOADS[base]
+    q, k, v = generate(w)
+    outs = []
+    for _ in range(3):
+        if kind == "bf16":
+            out, st = run_bf16(w, q, k, v)
+        else:
+            gpu = run_mx(w, q, k, v, exp_mode=None, delta=None)
+            out, st = gpu["out"], gpu["stats"]
+        assert st["status"] == 0
+        outs.append(out)
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)), f"{name}: launches differ"

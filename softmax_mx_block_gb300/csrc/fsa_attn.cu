@@ -276,6 +276,27 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(stall, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    if (nT > 0) {
+      // the first loads overlap the rest of the setup (tensor memory, constant rows)
+      const int bhq = b * p.H + h, bhk = b * p.Hkv + kvh;
+      mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
+#pragma unroll
+      for (int ka = 0; ka < C::NKA_QK; ++ka)
+        tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
+      if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
+      for (int j = 0; j < C::NS && j < nT; ++j) {
+        mbar_expect_tx(k_full + j, C::TILE_QK + (MX ? 512 : 0));
+#pragma unroll
+        for (int ka = 0; ka < C::NKA_QK; ++ka)
+          tma_load_3d(sK + j * C::TILE_QK + ka * 128 * C::W_QK, &tm_k, k_full + j, ka * C::W_QK, j * 128, bhk);
+        if (MX) bulk_load(sm + C::OFF_SFK + j * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + j);
+        mbar_expect_tx(v_full + j, C::TILE_V_TMA + (MX ? 512 : 0));
+#pragma unroll
+        for (int ka = 0; ka < C::NKA_V; ++ka)
+          tma_load_3d(sV + j * C::TILE_V + ka * C::VATOM, &tm_v, v_full + j, j * C::RB_V + ka * C::W_V, 0, bhk);
+        if (MX) bulk_load(sm + C::OFF_SFV + j * 512, p.sf_v + ((size_t)bhk * nkt + j) * 512, 512, v_full + j);
+      }
+    }
   }
   if (MX && warp >= 2) {
     // constant rows D..D+15 of every V stage (row D = ones, the rest zero) and the
@@ -321,16 +342,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // Lane 0 loads Q and the K tiles, lane 1 the V tiles: a K tile waits only for
     // its own ring slot, never behind a V slot that a late PV still holds.
     if (lane < 2 && nT > 0) {
-      const int bhq = b * p.H + h, bhk = b * p.Hkv + kvh;
+      const int bhk = b * p.Hkv + kvh;
       if (lane == 0) {
-        // Q, then K(j) as soon as K slot j % NS is free (S(j - NS) done)
-        int nk = 0;
-        mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
-#pragma unroll
-        for (int ka = 0; ka < C::NKA_QK; ++ka)
-          tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
-        if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
-        for (int j = 0; j < nT; ++j) {
+        // K(j) as soon as K slot j % NS is free (S(j - NS) done); Q and the first
+        // NS tiles were requested during the setup
+        int nk = min(C::NS, nT);
+        for (int j = nk; j < nT; ++j) {
           const int st = j % C::NS;
           if (j >= C::NS && !mbar_wait(k_empty + st, ((j - C::NS) / C::NS) & 1, ac)) break;
           mbar_expect_tx(k_full + st, C::TILE_QK + (MX ? 512 : 0));
@@ -345,8 +362,8 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mbar_wait_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, p.timeout_ns);
       } else {
         // V(j) as soon as V slot j % NS is free (PV(j - NS) done)
-        int nv = 0;
-        for (int j = 0; j < nT; ++j) {
+        int nv = min(C::NS, nT);
+        for (int j = nv; j < nT; ++j) {
           const int st = j % C::NS;
           if (j >= C::NS && !mbar_wait(pv_done + st, ((j - C::NS) / C::NS) & 1, ac)) break;
           mbar_expect_tx(v_full + st, C::TILE_V_TMA + (MX ? 512 : 0));

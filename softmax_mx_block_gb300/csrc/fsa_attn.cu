@@ -227,7 +227,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   constexpr bool MX = C::MX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the warp index (and below the tensor-memory base) through a lane-0 shuffle, which
+  // the compiler knows to be warp-uniform: addresses derived from them stay uniform
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
 
   // ---- work item: heavy causal tiles first
   // causal: (batch, head) on the fast grid axis and query tiles heaviest first on the
@@ -334,7 +336,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *tmem_slot;
+  const uint32_t tbase = __shfl_sync(0xffffffffu, *tmem_slot, 0);
   const AbortCtl ac{abort_flag, p.status, p.timeout_ns};
 
   if (warp == 0) {
@@ -536,8 +538,10 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     bool ok = true;                                 // false once any wait failed: no more work
     // BF16: the denominator is summed here, per part, relative to the part's latest M
     float lsum = 0.0f, Ml = kNegInf;
-    // every lane polls; the vote keeps the warp uniform
+    // every lane polls; the vote keeps the warp uniform.  The common case (phase
+    // already complete) is one try_wait per lane and one vote, with no loop
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
       return __all_sync(0xffffffffu, mbar_wait<false>(bar, parity, ac));
     };
     for (int j = pp; j < nT; j += 2) {

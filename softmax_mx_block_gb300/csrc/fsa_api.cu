@@ -99,6 +99,7 @@ void fill_common(fsa::KParams& p, int B, int H, int Hkv, int Sq, int Sk, int cau
   p.c = (float)((double)scale * 1.4426950408889634073599246810018921);   // log2(e)
   p.delta = o->delta;
   p.efq_beta = o->efq_beta;
+  p.efq_fast = (o->efq_beta <= 2 && o->delta <= 120.0f) ? 1 : 0;
   p.timeout_ns = (uint64_t)(o->timeout_ms ? o->timeout_ms : 4000u) * 1000000ull;
   p.row_fallbacks = o->row_fallbacks;
   p.stat_fallbacks = stats ? &stats->fallback_events : nullptr;

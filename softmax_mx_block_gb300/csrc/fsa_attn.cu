@@ -174,13 +174,19 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
     // low bits then hold k; nibble pairs combine by shift-add, bytes merge by permute
     const float magic = 12582912.0f;
     const uint64_t two2 = pk2(2.0f, 2.0f), kb2 = pk2(magic + (float)beta, magic + (float)beta);
+    // EXPM 1: beta <= 2 and a fallback margin delta <= 120, so E = floor(tmax) - 2 <=
+    // 125 is never clamped from above, r < 3 (up to rounding), 2 r + beta < 8.5 and a
+    // rounded code is at most 8: clamp below only, then turn the nibbles equal to 8
+    // into 7 on the packed word (8 - 1; no nibble of 0..7 has bit 3 set).
+    // EXPM 0: any beta and delta, both sides clamped.
+    constexpr bool one_sided = EXPM == 1;
     uint32_t y[32];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       float y0, y1;
       upk2(ffma2(two2, pk2(v[i], v[i + 1]), kb2), y0, y1);
-      y[i] = __float_as_uint(fminf(fmaxf(y0, magic), magic + 7.0f));
-      y[i + 1] = __float_as_uint(fminf(fmaxf(y1, magic), magic + 7.0f));
+      y[i] = __float_as_uint(one_sided ? fmaxf(y0, magic) : fminf(fmaxf(y0, magic), magic + 7.0f));
+      y[i + 1] = __float_as_uint(one_sided ? fmaxf(y1, magic) : fminf(fmaxf(y1, magic), magic + 7.0f));
     }
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -188,7 +194,8 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
       // low byte of (t1 << 4) + t0 is k0 | k1 << 4 (the magic's bits stay above bit 21)
       const uint32_t a01 = (t[1] << 4) + t[0], a23 = (t[3] << 4) + t[2];
       const uint32_t a45 = (t[5] << 4) + t[4], a67 = (t[7] << 4) + t[6];
-      out[w] = prmt(prmt(a01, a23, 0x0040u), prmt(a45, a67, 0x0040u), 0x5410u);
+      const uint32_t wv = prmt(prmt(a01, a23, 0x0040u), prmt(a45, a67, 0x0040u), 0x5410u);
+      out[w] = one_sided ? wv - ((wv >> 3) & 0x11111111u) : wv;
     }
   } else {
     exp2_block<EXPM>(v);
@@ -786,6 +793,10 @@ static cudaError_t launch_one(const AttnLaunch& a) {
 template <int FQK, int FPV>
 cudaError_t launch_attn_impl(const AttnLaunch& a) {
   constexpr bool efq_or_bf16 = FPV == F_EFQ || FPV == F_BF16;
+  if constexpr (FPV == F_EFQ) {             // EFQ: the exp-mode slot selects the clamp (see pgen_block)
+    if (a.D == 64) return a.p.efq_fast ? launch_one<FQK, FPV, 64, 1>(a) : launch_one<FQK, FPV, 64, 0>(a);
+    return a.p.efq_fast ? launch_one<FQK, FPV, 128, 1>(a) : launch_one<FQK, FPV, 128, 0>(a);
+  }
   if (a.D == 64) {
     if constexpr (efq_or_bf16) return launch_one<FQK, FPV, 64, 1>(a);
     else {

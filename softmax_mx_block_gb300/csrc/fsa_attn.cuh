@@ -93,6 +93,7 @@ struct KParams {
   float c;                // fp32(scale * log2 e)
   float delta;
   int efq_beta;
+  int efq_fast;           // EFQ codes cannot exceed 8 (beta <= 2, delta <= 120): one-sided clamp
   uint64_t timeout_ns;
   const uint8_t* sf_q;    // [B*H][ceil(Sq/128)][512]
   const uint8_t* sf_k;    // [B*Hkv][ceil(Sk/128)][512]

@@ -202,3 +202,23 @@ def test_bf16_transpose_v():
     assert got.shape == (2, 3, 64, 256)
     np.testing.assert_array_equal(got[..., :200], np.swapaxes(v, 2, 3))
     assert not got[..., 200:].any()
+
+
+@pytest.mark.parametrize("beta,delta", [(2, 8.0), (0, 8.0), (-3, 8.0), (2, 120.0), (3, 8.0), (5, 50.0), (2, 200.0)])
+def test_efq_offset_and_margin(beta, delta):
+    """EFQ codes rne(2 r + beta) clamped to [0, 7], for offsets and fallback margins on
+    both sides of the kernel's one-sided-clamp condition (beta <= 2, delta <= 120),
+    on inputs with planted keys that lift late tiles far above the frozen maximum."""
+    w = Workload("efq_beta", 1, 4, 2, 512, 1024, 128, False, "E2M1", "E2M1_EFQ", 11, "planted")
+    q, k, v = generate(w)
+    rows = sample_rows(w, per_head=128)
+    gpu = run_mx(w, q, k, v, exp_mode=None, delta=delta, efq_beta=beta)
+    assert gpu["stats"]["status"] == 0
+    mx = oracle.MxInputs.from_bf16(q, k, v, FMT[w.fmt_qk], 2)
+    orc = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, 3, rows, delta=delta, beta=beta, ambiguity=True)
+    emu, amb = orc["out"], orc["amb"]
+    undetermined = np.isinf(amb).any(axis=1)
+    assert np.mean(undetermined) < 0.01
+    tol = TOL_EMU * np.sqrt(np.mean(emu ** 2))
+    excess = (np.abs(gpu["out"][rows] - emu) - amb - tol)[~undetermined]
+    assert np.all(excess <= 0.0), f"beta {beta} delta {delta}: exceeds by {excess.max():.3e}"

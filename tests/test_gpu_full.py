@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 from test_gpu_attention import FMT, TOL_EMU, oracle_mx, rel_err, run_bf16, run_mx  # noqa: E402
 
 MUFU_ALL = 0xFFFFFFFF            # every key position through the hardware exp2 (the default mode)
-CASES = ["prefill", "long_fp8_16k", "long_efq_16k", "video_dit", "adversarial.L0", "adversarial.L1"]
+CASES = ["prefill", "long_fp8_16k", "long_efq_16k", "long_fp8_64k", "long_efq_64k", "long_efq_128k", "video_dit",
+         "adversarial.L0", "adversarial.L1"]
 
 
 def _workload(name):

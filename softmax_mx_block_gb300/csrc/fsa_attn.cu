@@ -562,7 +562,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (got) {
         tc_fence_after();
         uint32_t raw[128];
-        tmem_ld_cols<128>(tl + C::T_S + 128 * s, raw);
+        float bmr[NBLK];                              // block maxima, from the load itself
+#pragma unroll
+        for (int b = 0; b < NBLK; ++b) tmem_ld32_max(tl + C::T_S + 128 * s + 32 * b, raw + 32 * b, bmr[b]);
         tc_wait_ld();
         // S(j) is in registers: its buffer may take S(j+2)
         tc_fence_before();
@@ -574,9 +576,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (128 * j + i > lim) sv[i] = kNegInf;
-        }
 #pragma unroll
-        for (int b = 0; b < NBLK; ++b) bm[b] = max32(sv + 32 * b);
+          for (int b = 0; b < NBLK; ++b) bm[b] = max32(sv + 32 * b);
+        } else {
+#pragma unroll
+          for (int b = 0; b < NBLK; ++b) bm[b] = bmr[b];
+        }
       }
       // M after tile j-1 comes from the other part (NaN: it has stopped working)
       if (j > 0) {

@@ -123,8 +123,20 @@ typedef struct {
   int32_t* row_fallbacks;/* optional device int32 [B][H][Sq]: fallback count per row */
   int32_t  inject_stall; /* test hook: 1 makes the MMA warp wait on a barrier nobody
                             arrives on, so the bounded wait expires (status TIMEOUT) */
-  int32_t  reserved[3];
+  int32_t  schedule;     /* fsa_schedule (default FSA_SCHED_AUTO); the result does not
+                            depend on it: both schedules compute bit-identical outputs */
+  int32_t  reserved[2];
 } fsa_opts;
+
+typedef enum {
+  FSA_SCHED_AUTO = 0,        /* persistent when query tiles average at most 32 key tiles
+                                (short causal prefill), else one CTA per query tile; the
+                                BF16 entry point always takes one CTA per query tile */
+  FSA_SCHED_PER_TILE = 1,    /* one CTA per 128-row query tile */
+  FSA_SCHED_PERSISTENT = 2   /* one CTA per SM, each walking a list of query tiles: a CTA's
+                                setup, first loads, pipeline fill and drain are paid once
+                                per SM instead of once per query tile */
+} fsa_schedule;
 
 typedef struct {                      /* device memory, zeroed by the caller */
   unsigned long long fallback_events; /* (row, tile) pairs whose score beat the frozen max */

@@ -39,7 +39,7 @@ class fsa_mx_tensor(ctypes.Structure):
 class fsa_opts(ctypes.Structure):
     _fields_ = [("delta", ctypes.c_float), ("exp_mode", ctypes.c_int32), ("efq_beta", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_uint32), ("row_fallbacks", ctypes.c_void_p), ("inject_stall", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("schedule", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
 
 STATS_BYTES = 24      # fsa_stats: u64 fallback_events, u64 row_tiles, i32 status, i32 reserved
@@ -167,7 +167,7 @@ def read_stats(stats: torch.Tensor) -> dict:
 def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
                       causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=None, exp_mode=None,
                       efq_beta=2, timeout_ms=0, row_fallbacks: torch.Tensor | None = None, stats=None,
-                      inject_stall=False, stream=None) -> torch.Tensor:
+                      inject_stall=False, schedule=None, stream=None) -> torch.Tensor:
     """O [B,H,Sq,D] fp32 by the fused MX forward (fsa_attention_fwd_ex)."""
     B, H, Sq, D = q.B, q.H, q.S, q.D
     Hkv = k.H if Hkv is None else Hkv
@@ -187,6 +187,8 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
     if timeout_ms:
         o.timeout_ms = int(timeout_ms)
     o.inject_stall = int(bool(inject_stall))
+    if schedule is not None:
+        o.schedule = int(schedule)
     if row_fallbacks is not None:
         _need_cuda(row_fallbacks, "row_fallbacks", torch.int32)
         o.row_fallbacks = row_fallbacks.data_ptr()

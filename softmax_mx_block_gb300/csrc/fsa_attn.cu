@@ -781,6 +781,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
+}  // namespace fsa
+
+#include "fsa_attn_persistent.cuh"
+
+namespace fsa {
+
 // ----------------------------------------------------------------------------- host launch
 template <int FQK, int FPV, int D, int EXPM>
 static cudaError_t launch_one(const AttnLaunch& a) {
@@ -795,26 +801,51 @@ static cudaError_t launch_one(const AttnLaunch& a) {
   return cudaGetLastError();
 }
 
+// Persistent schedule: one CTA per SM (no more CTAs than query tiles), enough CTAs
+// that none takes more than MAX_ITEMS query tiles.
+template <int FQK, int FPV, int D, int EXPM>
+static cudaError_t launch_persistent(const AttnLaunch& a) {
+  using C = Cfg<FQK, FPV, D, true>;
+  constexpr int smem = (C::SMEM > 116 * 1024 ? C::SMEM : 116 * 1024);
+  auto kern = fsa_attn_persistent_kernel<FQK, FPV, D, EXPM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, n_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  int grid = a.p.n_items < n_sm ? a.p.n_items : n_sm;
+  const int need = (a.p.n_items + C::MAX_ITEMS - 1) / C::MAX_ITEMS;
+  if (grid < need) grid = need;
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.to, a.p);
+  return cudaGetLastError();
+}
+
+template <int FQK, int FPV, int D, int EXPM>
+static cudaError_t launch_sched(const AttnLaunch& a) {
+  return a.persistent ? launch_persistent<FQK, FPV, D, EXPM>(a) : launch_one<FQK, FPV, D, EXPM>(a);
+}
+
 template <int FQK, int FPV>
 cudaError_t launch_attn_impl(const AttnLaunch& a) {
   constexpr bool efq_or_bf16 = FPV == F_EFQ || FPV == F_BF16;
   if constexpr (FPV == F_EFQ) {             // EFQ: the exp-mode slot selects the clamp (see pgen_block)
-    if (a.D == 64) return a.p.efq_fast ? launch_one<FQK, FPV, 64, 1>(a) : launch_one<FQK, FPV, 64, 0>(a);
-    return a.p.efq_fast ? launch_one<FQK, FPV, 128, 1>(a) : launch_one<FQK, FPV, 128, 0>(a);
+    if (a.D == 64) return a.p.efq_fast ? launch_sched<FQK, FPV, 64, 1>(a) : launch_sched<FQK, FPV, 64, 0>(a);
+    return a.p.efq_fast ? launch_sched<FQK, FPV, 128, 1>(a) : launch_sched<FQK, FPV, 128, 0>(a);
   }
   if (a.D == 64) {
-    if constexpr (efq_or_bf16) return launch_one<FQK, FPV, 64, 1>(a);
+    if constexpr (efq_or_bf16) return launch_sched<FQK, FPV, 64, 1>(a);
     else {
-      if (a.exp_mode == 0) return launch_one<FQK, FPV, 64, 0>(a);
-      if (a.exp_mode == 1) return launch_one<FQK, FPV, 64, 1>(a);
-      return launch_one<FQK, FPV, 64, 2>(a);
+      if (a.exp_mode == 0) return launch_sched<FQK, FPV, 64, 0>(a);
+      if (a.exp_mode == 1) return launch_sched<FQK, FPV, 64, 1>(a);
+      return launch_sched<FQK, FPV, 64, 2>(a);
     }
   }
-  if constexpr (efq_or_bf16) return launch_one<FQK, FPV, 128, 1>(a);
+  if constexpr (efq_or_bf16) return launch_sched<FQK, FPV, 128, 1>(a);
   else {
-    if (a.exp_mode == 0) return launch_one<FQK, FPV, 128, 0>(a);
-    if (a.exp_mode == 1) return launch_one<FQK, FPV, 128, 1>(a);
-    return launch_one<FQK, FPV, 128, 2>(a);
+    if (a.exp_mode == 0) return launch_sched<FQK, FPV, 128, 0>(a);
+    if (a.exp_mode == 1) return launch_sched<FQK, FPV, 128, 1>(a);
+    return launch_sched<FQK, FPV, 128, 2>(a);
   }
 }
 

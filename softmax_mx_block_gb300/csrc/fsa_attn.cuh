@@ -21,7 +21,9 @@ template <> struct Fmt<F_EFQ>  { static constexpr int kind = 2, bits2 = 8, code 
 
 __host__ __device__ constexpr int swz_code(int width) { return width == 128 ? 2 : (width == 64 ? 4 : 6); }
 
-template <int FQK, int FPV, int D_>
+// PERSIST: the persistent schedule (one CTA per SM walking a list of query tiles),
+// which adds a second Q buffer, an output staging area and the list.
+template <int FQK, int FPV, int D_, bool PERSIST = false>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int BM = 128, BN = 128;
@@ -56,23 +58,31 @@ struct Cfg {
   static constexpr int NS = MX ? 4 : 2;                             // K/V stages
   static constexpr int SF_BYTES = 512;
   // ---- shared memory offsets (1024-aligned tiles)
+  static constexpr int NQB = PERSIST ? 2 : 1;                       // Q buffers
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE_QK;
+  static constexpr int OFF_K = OFF_Q + NQB * TILE_QK;
   static constexpr int OFF_V = OFF_K + NS * TILE_QK;
   static constexpr int OFF_SF = (OFF_V + NS * TILE_V + 1023) / 1024 * 1024;
   static constexpr int OFF_SFQ = OFF_SF;
-  static constexpr int OFF_SFK = OFF_SFQ + SF_BYTES;
+  static constexpr int OFF_SFK = OFF_SFQ + NQB * SF_BYTES;
   static constexpr int OFF_SFV = OFF_SFK + NS * SF_BYTES;
   static constexpr int OFF_SFONE = OFF_SFV + NS * SF_BYTES;
   static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // M handoff, fallback counts, BF16 {l, M} x 2
   static constexpr int OFF_BAR = OFF_RED + (256 + 4 * 128) * 4;
-  static constexpr int NBAR = 1 + 4 * NS + 3 * 2 + 2;               // q, k/v full, pv done, k empty x NS, s full/free, p x2, drain, stall
+  // q full (+ q empty x2 when persistent), k/v full, pv done, k empty x NS, s full/free,
+  // p full x2, (o free,) drain, stall
+  static constexpr int NBAR = PERSIST ? 4 + 4 * NS + 3 * 2 + 3 : 1 + 4 * NS + 3 * 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;                 // + alignment slack
+  // output staging: one CTA per query tile stages O (128 rows x D fp32, 32x32 boxes)
+  // in the K/V ring, free by then; the persistent schedule has one 32-row x 16-column
+  // fp32 box (64B swizzle) per softmax warp
+  static constexpr int OFF_OSTAGE = PERSIST ? (OFF_MISC + 64 + 1023) / 1024 * 1024 : OFF_K;
+  static_assert(PERSIST || OFF_K + 128 * D * 4 <= OFF_SF, "O staging fits the K/V ring");
+  // persistent: the CTA's query tiles in processing order (at most MAX_ITEMS)
+  static constexpr int MAX_ITEMS = 256;
+  static constexpr int OFF_ITEMS = OFF_OSTAGE + NSW * 2048;
+  static constexpr int SMEM = PERSIST ? OFF_ITEMS + MAX_ITEMS * 16 + 1024 : OFF_MISC + 64 + 1024;   // + alignment slack
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  // the epilogue stages O (128 rows x D fp32, 32x32 boxes) in the K/V ring, free by then
-  static constexpr int OFF_OSTAGE = OFF_K;
-  static_assert(OFF_K + 128 * D * 4 <= OFF_SF, "O staging fits the K/V ring");
   // ---- tensor memory columns
   static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256)
   static constexpr uint32_t T_O = 256;        // [256, 256 + N_PV)
@@ -80,9 +90,10 @@ struct Cfg {
   static constexpr uint32_t T_SFK = 404;      // + 4 * parity
   static constexpr uint32_t T_SFV = 412;      // + 8 * parity (4 from the V atom, 4 constant)
   static constexpr uint32_t T_SFP = 428;      // + 4 * buffer + lane quadrant
+  static constexpr uint32_t T_SFQ1 = 436;     // persistent: scale atom of the second Q buffer
   static constexpr uint32_t T_P = MX ? 448 : T_O + D;   // + P_COLS * buffer (BF16: no scales)
   static_assert(T_O + N_PV <= (MX ? T_SFQ : T_P), "tmem");
-  static_assert(!MX || T_SFP + 8 <= T_P, "tmem");
+  static_assert(!MX || T_SFQ1 + 4 <= T_P, "tmem");
   static_assert(T_P + NPB * P_COLS <= 512, "tmem");
   // ---- threads
   static constexpr int NTHREADS = 64 + 32 * NSW;   // warp 0 TMA, warp 1 MMA, then the softmax warps
@@ -90,6 +101,7 @@ struct Cfg {
 
 struct KParams {
   int B, H, Hkv, Sq, Sk, n_qtiles, causal;
+  int n_items;            // query tiles over all (batch, head): B * H * n_qtiles
   float c;                // fp32(scale * log2 e)
   float delta;
   int efq_beta;

@@ -7,10 +7,11 @@
 namespace fsa {
 
 struct AttnLaunch {
-  CUtensorMap tq, tk, tv, to;   // Q, K, V^T codes; fp32 output
+  CUtensorMap tq, tk, tv, to;   // Q, K, V^T codes; fp32 output (32x32 boxes, or 16x32 when persistent)
   KParams p;
   int D;
   int exp_mode;          // 0 poly, 1 MUFU, 2 split (ignored for EFQ and BF16)
+  int persistent;        // 1: the persistent schedule (tq..to built for it), 0: one CTA per query tile
   cudaStream_t stream;
 };
 

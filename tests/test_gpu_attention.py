@@ -158,13 +158,14 @@ def test_default_margin(name):
     assert np.mean(gpu["row_fallbacks"][rows] != orc["fallbacks"]) < 0.01
 
 
-def test_inject_stall_times_out_and_context_survives():
+@pytest.mark.parametrize("schedule", [1, 2])
+def test_inject_stall_times_out_and_context_survives(schedule):
     fsa = _fsa()
     w = WORKLOADS["tiny"]
     q, k, v = generate(w)
-    gpu = run_mx(w, q, k, v, inject_stall=True, timeout_ms=50)
+    gpu = run_mx(w, q, k, v, inject_stall=True, timeout_ms=50, schedule=schedule)
     assert gpu["stats"]["status"] == fsa.FSA_ERR_TIMEOUT
-    again = run_mx(w, q, k, v)
+    again = run_mx(w, q, k, v, schedule=schedule)
     assert again["stats"]["status"] == 0 and np.isfinite(again["out"]).all()
 
 
@@ -222,3 +223,44 @@ def test_efq_offset_and_margin(beta, delta):
     tol = TOL_EMU * np.sqrt(np.mean(emu ** 2))
     excess = (np.abs(gpu["out"][rows] - emu) - amb - tol)[~undetermined]
     assert np.all(excess <= 0.0), f"beta {beta} delta {delta}: exceeds by {excess.max():.3e}"
+
+
+SCHED_CASES = [
+    Workload("sched_ragged", 1, 4, 2, 300, 700, 128, False, "E4M3", "E4M3", 21),
+    Workload("sched_causal_d64", 2, 4, 1, 640, 640, 64, True, "E2M3", "E2M1", 22),
+    Workload("sched_no_keys", 1, 3, 3, 700, 300, 128, True, "E2M1", "E2M1_EFQ", 23),   # query tiles without key tiles
+    Workload("sched_planted", 1, 2, 2, 1024, 1024, 128, True, "E4M3", "E4M3", 24, "planted"),
+]
+
+
+@pytest.mark.parametrize("w", SCHED_CASES, ids=lambda w: w.name)
+def test_schedules_bit_identical(w):
+    """One CTA per query tile and the persistent schedule run the same arithmetic per
+    key tile: outputs, per-row fallback counts and statistics agree bit for bit."""
+    q, k, v = generate(w)
+    res = [run_mx(w, q, k, v, exp_mode=None, delta=None, row_fb=True, schedule=s) for s in (1, 2)]
+    for r in res:
+        assert r["stats"]["status"] == 0
+    assert np.array_equal(res[0]["out"].view(np.uint32), res[1]["out"].view(np.uint32))
+    assert np.array_equal(res[0]["row_fallbacks"], res[1]["row_fallbacks"])
+    assert res[0]["stats"] == res[1]["stats"]
+
+
+def test_persistent_more_query_tiles_than_one_wave():
+    """More than 256 query tiles per SM: the persistent launch takes enough CTAs that
+    none walks more than 256, and still matches one CTA per query tile bit for bit."""
+    fsa = _fsa()
+    g = torch.Generator(device="cuda").manual_seed(5)
+    B, H, Hkv, S, Sk, D = 4, 80, 1, 16384, 256, 64          # 40960 query tiles
+    x = lambda *shape: torch.randn(*shape, generator=g, device="cuda").to(torch.bfloat16)
+    q, k, v = x(B, H, S, D), x(B, Hkv, Sk, D), x(B, Hkv, Sk, D)
+    mq = fsa.fsa_mx_quantize(q, fsa.FSA_MX_ROWS, 0)
+    mk = fsa.fsa_mx_quantize(k, fsa.FSA_MX_ROWS, 0)
+    mv = fsa.fsa_mx_quantize(v, fsa.FSA_MX_COLS_T, 0)
+    outs = []
+    for s in (1, 2):
+        st = fsa.new_stats()
+        outs.append(fsa.fsa_attention_fwd(mq, mk, mv, fmt_qk=0, fmt_pv=0, stats=st, schedule=s))
+        torch.cuda.synchronize()
+        assert fsa.read_stats(st)["status"] == 0
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))

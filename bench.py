@@ -35,7 +35,7 @@ FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
 KIND_RATIO = {"E4M3": 2.0, "E2M3": 2.0, "E2M1": 6.0, "E2M1_EFQ": 6.0}
 # DRAM bytes (read + write) per attention launch from an ncu capture of the current
 # kernel build, by workload (profiles/fsa_attn_e4m3_*.md); absent: not captured
-TRAFFIC = {"prefill": 26_019_840 + 10_496_512, "long_fp8_16k": 105_641_984 + 212_161_536}
+TRAFFIC = {"prefill": 26_028_288 + 14_892_032, "long_fp8_16k": 105_790_976 + 212_229_120}
 
 
 def metric_name():

@@ -5,6 +5,9 @@ MX quantisation of Q, K and V (fsa_mx_quantize) and the fused attention
 forward (fsa_attention_fwd_ex).  The metric is attention forward TFLOP/s
 (4*B*H*Sq*Sk*D per layer, halved for causal).  Inputs are resident in HBM when
 the timed region starts; L2 is flushed (a 512 MB write) between timed steps.
+The three quantisation launches of a step are captured once as a CUDA graph and
+replayed (--no-graph: launched eagerly); the attention launch is bracketed by
+CUDA events of its own.  The end-to-end figure makes every call eagerly.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -141,12 +144,22 @@ def run_gpu(args, w: Workload, world):
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     attn_ev = []
 
-    def step(record=False):
-        for wl, (qd, kd, vd), (mq, mk, mv, out) in zip(layers, inputs, bufs):
+    def quantise(i):
+        wl, (qd, kd, vd), (mq, mk, mv, _) = layers[i], inputs[i], bufs[i]
+        fq, fp = FMT[wl.fmt_qk], FMT[wl.fmt_pv]
+        fsa.fsa_mx_quantize(qd, 0, fq, out=mq)
+        fsa.fsa_mx_quantize(kd, 0, fq, out=mk)
+        fsa.fsa_mx_quantize(vd, 1, 2 if fp == 3 else fp, out=mv)
+
+    qgraphs = []          # per layer: the three quantisation launches as one CUDA graph
+
+    def step(record=False, eager=False):
+        for i, (wl, (mq, mk, mv, out)) in enumerate(zip(layers, bufs)):
             fq, fp = FMT[wl.fmt_qk], FMT[wl.fmt_pv]
-            fsa.fsa_mx_quantize(qd, 0, fq, out=mq)
-            fsa.fsa_mx_quantize(kd, 0, fq, out=mk)
-            fsa.fsa_mx_quantize(vd, 1, 2 if fp == 3 else fp, out=mv)
+            if qgraphs and not eager:
+                qgraphs[i].replay()
+            else:
+                quantise(i)
             if record:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -164,6 +177,22 @@ def run_gpu(args, w: Workload, world):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    launch_mode = "eager"
+    if not args.no_graph:
+        # the same library calls, captured once and replayed: no host launch overhead
+        try:
+            for i in range(len(layers)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                    quantise(i)
+                qgraphs.append(g)
+            step()
+            torch.cuda.synchronize()
+            launch_mode = "quantisation from a CUDA graph, attention eager"
+        except Exception as e:  # capture unsupported: stay eager and say so
+            qgraphs.clear()
+            torch.cuda.synchronize()
+            launch_mode = f"eager (graph capture failed: {type(e).__name__})"
     stats.zero_()
     try:
         bus = torch.cuda.get_device_properties(dev).pci_bus_id
@@ -198,7 +227,7 @@ def run_gpu(args, w: Workload, world):
         for hs, ds in zip(host, inputs):
             for h_, d_ in zip(hs, ds):
                 d_.copy_(h_, non_blocking=True)
-        step()
+        step(eager=True)                      # every call through the public API
         for oh, b in zip(out_host, bufs):
             oh.copy_(b[3], non_blocking=True)
         e1.record(stream)
@@ -228,7 +257,7 @@ def run_gpu(args, w: Workload, world):
         t = torch.tensor([ms, e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms, e2e_ms = float(t[0]), float(t[1])
-    return dict(ms=ms, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks, stats=st,
+    return dict(ms=ms, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks, stats=st, launch_mode=launch_mode,
                 launches=args.steps * 4 * len(layers), bf16_ms=statistics.mean(bf_ms))
 
 
@@ -279,6 +308,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="fsa", choices=["fsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the quantisation eagerly (no CUDA graph)")
     ap.add_argument("--exp-mode", type=int, default=1, choices=[0, 1, 2],
                     help="0 cubic, 1 ex2.approx (default, the library's), 2 split 3:1")
     args = ap.parse_args()
@@ -313,6 +343,7 @@ def main():
         torch.distributed.destroy_process_group()
     if rank != 0:
         return
+    config["launch"] = r["launch_mode"]
     value = flops_per_step * world / (r["ms"] * 1e-3) / 1e12
     attn_tflops = flops_per_step / w.layers / (r["attn_ms"] * 1e-3) / 1e12
     peak, src = peak_for(w)

@@ -99,8 +99,11 @@ int fsa_mx_sizes(int B, int H, int S, int D, int layout, int fmt, size_t* codes_
 
 /* Quantise x_bf16 [B][H][S][D] (device, 16-byte aligned) into out->codes /
  * out->scales with the given layout and element format.  The shape, layout
- * and format fields of *out are written by the call.  Cited: MXFP8/6/4 GEMM
- * operands ("Fused-Softmax for efficient quantized attention", abstract). */
+ * and format fields of *out are written by the call.  One kernel launch on
+ * `stream`, which writes every byte of both buffers; nothing is allocated and
+ * nothing synchronises, so the call may be captured in a CUDA graph.  Cited:
+ * MXFP8/6/4 GEMM operands ("Fused-Softmax for efficient quantized
+ * attention", abstract). */
 int fsa_mx_quantize(const void* x_bf16, int B, int H, int S, int D, int layout, int fmt,
                     fsa_mx_tensor* out, void* stream);
 

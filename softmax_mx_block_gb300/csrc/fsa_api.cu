@@ -186,10 +186,9 @@ int fsa_mx_quantize(const void* x, int B, int H, int S, int D, int layout, int f
   if (!aligned16(x) || !aligned16(out->codes) || !aligned16(out->scales)) return FSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   out->fmt = fmt; out->layout = layout; out->B = B; out->H = H; out->S = S; out->D = D;
-  // unused scale slots hold 2^0 (0x7F); the kernels overwrite every used slot
-  cudaError_t e = cudaMemsetAsync(out->scales, 0x7F, sb, s);
-  if (e != cudaSuccess) return FSA_ERR_LAUNCH;
-  if (layout == FSA_MX_ROWS) e = fsa::launch_mx_quant_rows(x, (int64_t)B * H * S, S, D, fmt, out->codes, out->scales, s);
+  // the kernels write every byte of codes and scales (unused scale slots: 2^0, 0x7F)
+  cudaError_t e;
+  if (layout == FSA_MX_ROWS) e = fsa::launch_mx_quant_rows(x, B * H, S, D, fmt, out->codes, out->scales, s);
   else e = fsa::launch_mx_quant_cols(x, B * H, S, D, fmt, out->codes, out->scales, s);
   return launch_status(e);
 }

@@ -20,7 +20,7 @@ struct AttnLaunch {
 template <int FQK, int FPV>
 cudaError_t launch_attn_impl(const AttnLaunch& a);
 
-cudaError_t launch_mx_quant_rows(const void* x, int64_t R, int S, int D, int fmt, void* codes, void* scales,
+cudaError_t launch_mx_quant_rows(const void* x, int BH, int S, int D, int fmt, void* codes, void* scales,
                                  cudaStream_t st);
 cudaError_t launch_mx_quant_cols(const void* x, int BH, int S, int D, int fmt, void* codes, void* scales,
                                  cudaStream_t st);

@@ -37,153 +37,199 @@ __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
   else return cvt_e2m1x2(lo, hi);
 }
 
-// --------------------------------------------------------------------------
-// Rows layout (Q, K): one thread per 8 consecutive elements; 4 lanes = 1 block.
-// x: [R][D] bf16 (R = B*H*S), codes: [R][row_bytes], scales: 128x4 atoms.
+// Codes of one 32-element block held by one thread, v[0..32): 8 words (E4M3:
+// one code per byte; E2M3: two 16-code groups of 12 packed bytes and 4 zero
+// bytes) or 4 words (E2M1, two codes per byte, even index in the low nibble).
+// Returns the scale byte (0xFF and NaN / zero codes for a non-finite block).
 template <int FMT>
-__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __restrict__ x, int64_t R, int S, int D,
-                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+__device__ __forceinline__ uint32_t quant_block32(const float* v, uint32_t* w) {
   constexpr int emax = FMT == 0 ? 8 : 2;
-  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;    // chunk id
-  const int chunks_per_row = D / 8;
-  const int64_t row = g / chunks_per_row;
-  const bool active = row < R;
-  const int c = (int)(g - row * chunks_per_row);
-  float v[8];
   float amax = 0.f;
   bool nonfinite = false;
-  if (active) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(x + row * D + 8 * c);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = bf16_to_f32((uint16_t)(w[i] & 0xFFFF));
-      v[2 * i + 1] = bf16_to_f32((uint16_t)(w[i] >> 16));
-    }
+  for (int i = 0; i < 32; ++i) {
+    const float a = fabsf(v[i]);
+    nonfinite |= !(a <= 3.4e38f);
+    amax = fmaxf(amax, a);
+  }
+  const uint32_t sbyte = nonfinite ? 0xFFu : block_scale_byte(amax, emax);
+  const float mul = nonfinite ? 1.0f : pow2_neg((int)sbyte - 127);
+  uint32_t q[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float a = fabsf(v[i]);
-      nonfinite |= !(a <= 3.4e38f);
-      amax = fmaxf(amax, a);
+  for (int i = 0; i < 16; ++i)
+    q[i] = nonfinite ? (FMT == 0 ? 0x7F7Fu : 0u) : cvt_pair<FMT>(__fmul_rn(v[2 * i], mul), __fmul_rn(v[2 * i + 1], mul));
+  if constexpr (FMT == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = q[2 * i] | (q[2 * i + 1] << 16);
+  } else if constexpr (FMT == 1) {
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const uint32_t g[4] = {q[8 * gi] | (q[8 * gi + 1] << 16), q[8 * gi + 2] | (q[8 * gi + 3] << 16),
+                             q[8 * gi + 4] | (q[8 * gi + 5] << 16), q[8 * gi + 6] | (q[8 * gi + 7] << 16)};
+      pack6x16(g, w + 4 * gi);
+      w[4 * gi + 3] = 0u;
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int i = 0; i < 4; ++i) w[i] = q[4 * i] | (q[4 * i + 1] << 8) | (q[4 * i + 2] << 16) | (q[4 * i + 3] << 24);
   }
-  // 4-lane group reduction (groups are lane-aligned: D/8 chunks per row is a multiple of 4)
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  int nf = nonfinite;
-  nf |= __shfl_xor_sync(0xffffffffu, nf, 1);
-  nf |= __shfl_xor_sync(0xffffffffu, nf, 2);
-  const uint32_t sbyte = nf ? 0xFFu : block_scale_byte(amax, emax);
-  const float mul = nf ? 1.0f : pow2_neg((int)sbyte - 127);
-  uint32_t q[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (nf) q[i] = FMT == 0 ? 0x7F7Fu : 0u;
-    else q[i] = cvt_pair<FMT>(__fmul_rn(v[2 * i], mul), __fmul_rn(v[2 * i + 1], mul));
-  }
-  if (FMT == 1) {
-    // 16-element groups: the even chunk packs its and its neighbour's codes
-    uint32_t w[4] = {q[0] | (q[1] << 16), q[2] | (q[3] << 16), 0u, 0u};
-    w[2] = __shfl_down_sync(0xffffffffu, w[0], 1);
-    w[3] = __shfl_down_sync(0xffffffffu, w[1], 1);
-    if (active && (c & 1) == 0) {
-      uint32_t o[3];
-      pack6x16(w, o);
-      *reinterpret_cast<uint4*>(codes + row * D + 8 * c) = make_uint4(o[0], o[1], o[2], 0u);
-    }
-  } else if (active) {
-    if (FMT == 0) {
-      *reinterpret_cast<uint2*>(codes + row * D + 8 * c) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-    } else {
-      *reinterpret_cast<uint32_t*>(codes + row * (D / 2) + 4 * c) =
-          q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
-    }
-  }
-  if (active && (c & 3) == 0) {
-    const int64_t bh = row / S;
-    const int s = (int)(row - bh * S);
-    const int kb = c >> 2;
-    const int64_t atom = bh * ((S + 127) / 128) + s / 128;
-    const int rr = s & 127;
-    scales[atom * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + kb] = (uint8_t)sbyte;
-  }
+  return sbyte;
 }
 
 // --------------------------------------------------------------------------
-// Transposed layout (V): one CTA per (128-key tile, b*h); the tile is staged
-// in shared memory, each thread quantises (d, key block) columns.
-// x: [BH][S][D] bf16; codes: [BH][D][Sp] elements; scales: [BH][Sp/128] atoms.
-template <int FMT>
-__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const uint16_t* __restrict__ x, int S, int D, int Sp,
+// Rows layout (Q, K): one CTA per (128-row tile, b*h), 256 threads.  Chunk =
+// 8 consecutive elements of a row, 4 chunks = one 32-element block; thread t
+// takes chunks t, t + 256, ... of the tile, all loads issued before any
+// arithmetic.  The tile's 512-byte scale atom is assembled in shared memory
+// (unused slots 0x7F) and written whole.
+// x: [BH][S][D] bf16, codes: [BH*S][row bytes], scales: [BH][ceil(S/128)][512].
+template <int FMT, int D>
+__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __restrict__ x, int S,
                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   constexpr int emax = FMT == 0 ? 8 : 2;
-  extern __shared__ __align__(16) uint16_t tile[];        // [128][D]
-  const int t = blockIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int s0 = t * 128;
-  const uint16_t* src = x + (bh * S) * (int64_t)D;
-  const int nvec = 128 * D / 8;
-  for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
-    const int s = (i * 8) / D, d = (i * 8) % D;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (s0 + s < S) val = *reinterpret_cast<const uint4*>(src + (int64_t)(s0 + s) * D + d);
-    *reinterpret_cast<uint4*>(tile + s * D + d) = val;
+  constexpr int CPR = D / 8;                       // chunks per row
+  constexpr int NCH = 128 * CPR / 256;             // chunks per thread
+  constexpr int RB = FMT == 2 ? D / 2 : D;         // code bytes per row
+  __shared__ __align__(16) uint8_t atom[512];
+  const int t = threadIdx.x;
+  const int ntiles = (S + 127) / 128;
+  const int64_t bh = blockIdx.x / ntiles;          // one grid axis: no limit on B*H
+  const int s0 = (int)(blockIdx.x % ntiles) * 128;
+  const int nrows = min(128, S - s0);
+  const uint16_t* src = x + ((int64_t)bh * S + s0) * D;
+  uint8_t* dst = codes + ((int64_t)bh * S + s0) * RB;
+  if (t < 128) reinterpret_cast<uint32_t*>(atom)[t] = 0x7F7F7F7Fu;
+  uint4 raw[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int ch = t + 256 * i;
+    raw[i] = ch / CPR < nrows ? *reinterpret_cast<const uint4*>(src + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
-  const int npairs = D * 4;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int d = p % D, kb = p / D;
-    const int k0 = 32 * kb;
-    const int64_t code_elem = ((bh * D + d) * (int64_t)Sp) + s0 + k0;
-    uint32_t sbyte;
-    uint32_t q[16];
-    if (s0 + k0 >= S) {                         // block wholly past the sequence end
-      sbyte = 0x7Fu;
+  __syncthreads();                                 // atom initialised before the scale bytes land
 #pragma unroll
-      for (int i = 0; i < 16; ++i) q[i] = 0u;
-    } else {
-      float v[32];
-      float amax = 0.f;
-      bool nonfinite = false;
+  for (int i = 0; i < NCH; ++i) {
+    const int ch = t + 256 * i, r = ch / CPR, c = ch % CPR;
+    const bool active = r < nrows;
+    const uint32_t wr[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float v[8];
+    float amax = 0.f;
+    bool nonfinite = false;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = bf16_to_f32(tile[(k0 + i) * D + d]);
-        const float a = fabsf(v[i]);
-        nonfinite |= !(a <= 3.4e38f);
-        amax = fmaxf(amax, a);
-      }
-      sbyte = nonfinite ? 0xFFu : block_scale_byte(amax, emax);
-      const float mul = nonfinite ? 1.0f : pow2_neg((int)sbyte - 127);
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        q[i] = nonfinite ? (FMT == 0 ? 0x7F7Fu : 0u) : cvt_pair<FMT>(__fmul_rn(v[2 * i], mul), __fmul_rn(v[2 * i + 1], mul));
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = bf16_to_f32((uint16_t)(wr[e] & 0xFFFF));
+      v[2 * e + 1] = bf16_to_f32((uint16_t)(wr[e] >> 16));
     }
-    if (FMT == 0) {
-      uint4* dst = reinterpret_cast<uint4*>(codes + code_elem);
-      dst[0] = make_uint4(q[0] | (q[1] << 16), q[2] | (q[3] << 16), q[4] | (q[5] << 16), q[6] | (q[7] << 16));
-      dst[1] = make_uint4(q[8] | (q[9] << 16), q[10] | (q[11] << 16), q[12] | (q[13] << 16), q[14] | (q[15] << 16));
-    } else if (FMT == 1) {
-      uint4* dst = reinterpret_cast<uint4*>(codes + code_elem);
 #pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
-        const uint32_t w[4] = {q[8 * gi] | (q[8 * gi + 1] << 16), q[8 * gi + 2] | (q[8 * gi + 3] << 16),
-                               q[8 * gi + 4] | (q[8 * gi + 5] << 16), q[8 * gi + 6] | (q[8 * gi + 7] << 16)};
+    for (int e = 0; e < 8; ++e) {
+      const float a = fabsf(v[e]);
+      nonfinite |= !(a <= 3.4e38f);
+      amax = fmaxf(amax, a);
+    }
+    // 4-lane group reduction (groups are lane-aligned: CPR and 256 are multiples of 4)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int nf = nonfinite;
+    nf |= __shfl_xor_sync(0xffffffffu, nf, 1);
+    nf |= __shfl_xor_sync(0xffffffffu, nf, 2);
+    const uint32_t sbyte = nf ? 0xFFu : block_scale_byte(amax, emax);
+    const float mul = nf ? 1.0f : pow2_neg((int)sbyte - 127);
+    uint32_t q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (nf) q[e] = FMT == 0 ? 0x7F7Fu : 0u;
+      else q[e] = cvt_pair<FMT>(__fmul_rn(v[2 * e], mul), __fmul_rn(v[2 * e + 1], mul));
+    }
+    if constexpr (FMT == 1) {
+      // 16-element groups: the even chunk packs its and its neighbour's codes
+      uint32_t w[4] = {q[0] | (q[1] << 16), q[2] | (q[3] << 16), 0u, 0u};
+      w[2] = __shfl_down_sync(0xffffffffu, w[0], 1);
+      w[3] = __shfl_down_sync(0xffffffffu, w[1], 1);
+      if (active && (c & 1) == 0) {
         uint32_t o[3];
         pack6x16(w, o);
-        dst[gi] = make_uint4(o[0], o[1], o[2], 0u);
+        *reinterpret_cast<uint4*>(dst + r * RB + 8 * c) = make_uint4(o[0], o[1], o[2], 0u);
       }
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(codes + code_elem / 2);
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = q[4 * i] | (q[4 * i + 1] << 8) | (q[4 * i + 2] << 16) | (q[4 * i + 3] << 24);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (active) {
+      if constexpr (FMT == 0)
+        *reinterpret_cast<uint2*>(dst + r * RB + 8 * c) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+      else
+        *reinterpret_cast<uint32_t*>(dst + r * RB + 4 * c) = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
     }
-    if (d < 128) scales[(bh * (Sp / 128) + t) * 512 + (d & 31) * 16 + (d >> 5) * 4 + kb] = (uint8_t)sbyte;
+    if (active && (c & 3) == 0) atom[(r & 31) * 16 + (r >> 5) * 4 + (c >> 2)] = (uint8_t)sbyte;
   }
+  __syncthreads();
+  if (t < 32)
+    reinterpret_cast<uint4*>(scales + (int64_t)blockIdx.x * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
+}
+
+// --------------------------------------------------------------------------
+// Transposed layout (V): one CTA per (128-key tile, b*h), 256 threads.  The
+// tile is loaded into shared memory (all loads issued first); then each thread
+// quantises two adjacent columns d, d+1 over one 32-key block, and the scale
+// atom (rows d >= D and blocks past the sequence: 0x7F) is written whole.
+// x: [BH][S][D] bf16; codes: [BH][D][Sp] elements; scales: [BH][Sp/128][512].
+template <int FMT, int D>
+__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const uint16_t* __restrict__ x, int S, int Sp,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  constexpr int NV = 128 * D / 8 / 256;            // 16-byte vectors per thread
+  constexpr int DW = D / 2;                        // 32-bit words per tile row
+  __shared__ __align__(16) uint32_t tile[128 * DW];
+  __shared__ __align__(16) uint8_t atom[512];
+  const int t = threadIdx.x;
+  const int ntiles = Sp / 128;
+  const int64_t bh = blockIdx.x / ntiles;
+  const int s0 = (int)(blockIdx.x % ntiles) * 128;
+  const int nrows = min(128, S - s0);
+  const uint16_t* src = x + ((int64_t)bh * S + s0) * D;
+  uint4 raw[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int vi = t + 256 * i;
+    raw[i] = (vi * 8) / D < nrows ? *reinterpret_cast<const uint4*>(src + 8 * vi) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < NV; ++i) reinterpret_cast<uint4*>(tile)[t + 256 * i] = raw[i];
+  if (t < 128) reinterpret_cast<uint32_t*>(atom)[t] = 0x7F7F7F7Fu;
+  __syncthreads();
+  if (t < DW * 4) {
+    const int d2 = t % DW, kb = t / DW;
+    const int d = 2 * d2, k0 = 32 * kb;
+    uint32_t w0[8], w1[8];
+    uint32_t sb0 = 0x7Fu, sb1 = 0x7Fu;
+    if (s0 + k0 < S) {                             // else: block wholly past the sequence end, zero codes
+      float v0[32], v1[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t pr = tile[(k0 + i) * DW + d2];
+        v0[i] = bf16_to_f32((uint16_t)(pr & 0xFFFF));
+        v1[i] = bf16_to_f32((uint16_t)(pr >> 16));
+      }
+      sb0 = quant_block32<FMT>(v0, w0);
+      sb1 = quant_block32<FMT>(v1, w1);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w0[i] = w1[i] = 0u;
+    }
+    const int64_t e0 = ((bh * D + d) * (int64_t)Sp) + s0 + k0;   // element index of column d's block
+    if constexpr (FMT == 2) {
+      uint4* p0 = reinterpret_cast<uint4*>(codes + e0 / 2);
+      uint4* p1 = reinterpret_cast<uint4*>(codes + (e0 + Sp) / 2);
+      p0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+      p1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    } else {
+      uint4* p0 = reinterpret_cast<uint4*>(codes + e0);
+      uint4* p1 = reinterpret_cast<uint4*>(codes + e0 + Sp);
+      p0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+      p0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+      p1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+      p1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+    }
+    atom[(d & 31) * 16 + (d >> 5) * 4 + kb] = (uint8_t)sb0;
+    atom[((d + 1) & 31) * 16 + ((d + 1) >> 5) * 4 + kb] = (uint8_t)sb1;
+  }
+  __syncthreads();
+  if (t < 32)
+    reinterpret_cast<uint4*>(scales + (int64_t)blockIdx.x * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
 }
 
 // V [BH][S][D] bf16 -> V^T [BH][D][Sp] bf16 (zero padded), one CTA per 128-key tile.
@@ -214,36 +260,49 @@ __global__ void __launch_bounds__(256) transpose_v_kernel(const uint16_t* __rest
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_mx_quant_rows(const void* x, int64_t R, int S, int D, int fmt, void* codes, void* scales,
+template <int FMT>
+static cudaError_t quant_rows_d(const uint16_t* x, int BH, int S, int D, uint8_t* c, uint8_t* s, cudaStream_t st) {
+  const int64_t n = ((int64_t)S + 127) / 128 * BH;                   // (b*h, tile), tile fastest
+  if (n > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  const unsigned grid = (unsigned)n;
+  if (D == 128) mx_quant_rows_kernel<FMT, 128><<<grid, 256, 0, st>>>(x, S, c, s);
+  else mx_quant_rows_kernel<FMT, 64><<<grid, 256, 0, st>>>(x, S, c, s);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t quant_cols_d(const uint16_t* x, int BH, int S, int D, uint8_t* c, uint8_t* s, cudaStream_t st) {
+  const int Sp = (S + 127) / 128 * 128;
+  const int64_t n = (int64_t)Sp / 128 * BH;
+  if (n > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  const unsigned grid = (unsigned)n;
+  if (D == 128) mx_quant_cols_kernel<FMT, 128><<<grid, 256, 0, st>>>(x, S, Sp, c, s);
+  else mx_quant_cols_kernel<FMT, 64><<<grid, 256, 0, st>>>(x, S, Sp, c, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quant_rows(const void* x, int BH, int S, int D, int fmt, void* codes, void* scales,
                                  cudaStream_t st) {
-  const int64_t chunks = R * (D / 8);
-  const int threads = 256;
-  const int64_t blocks = (chunks + threads - 1) / threads;
   auto* xs = static_cast<const uint16_t*>(x);
   auto* c = static_cast<uint8_t*>(codes);
   auto* s = static_cast<uint8_t*>(scales);
   switch (fmt) {
-    case 0: mx_quant_rows_kernel<0><<<(unsigned)blocks, threads, 0, st>>>(xs, R, S, D, c, s); break;
-    case 1: mx_quant_rows_kernel<1><<<(unsigned)blocks, threads, 0, st>>>(xs, R, S, D, c, s); break;
-    default: mx_quant_rows_kernel<2><<<(unsigned)blocks, threads, 0, st>>>(xs, R, S, D, c, s); break;
+    case 0: return quant_rows_d<0>(xs, BH, S, D, c, s, st);
+    case 1: return quant_rows_d<1>(xs, BH, S, D, c, s, st);
+    default: return quant_rows_d<2>(xs, BH, S, D, c, s, st);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quant_cols(const void* x, int BH, int S, int D, int fmt, void* codes, void* scales,
                                  cudaStream_t st) {
-  const int Sp = (S + 127) / 128 * 128;
-  dim3 grid(Sp / 128, BH);
-  const size_t smem = (size_t)128 * D * 2;
   auto* xs = static_cast<const uint16_t*>(x);
   auto* c = static_cast<uint8_t*>(codes);
   auto* s = static_cast<uint8_t*>(scales);
   switch (fmt) {
-    case 0: mx_quant_cols_kernel<0><<<grid, 256, smem, st>>>(xs, S, D, Sp, c, s); break;
-    case 1: mx_quant_cols_kernel<1><<<grid, 256, smem, st>>>(xs, S, D, Sp, c, s); break;
-    default: mx_quant_cols_kernel<2><<<grid, 256, smem, st>>>(xs, S, D, Sp, c, s); break;
+    case 0: return quant_cols_d<0>(xs, BH, S, D, c, s, st);
+    case 1: return quant_cols_d<1>(xs, BH, S, D, c, s, st);
+    default: return quant_cols_d<2>(xs, BH, S, D, c, s, st);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_transpose_v(const void* v, void* vt, int BH, int S, int D, cudaStream_t st) {

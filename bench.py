@@ -1,11 +1,11 @@
 """Benchmark of the fused MX attention forward on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-MX quantisation of Q, K and V (fsa_mx_quantize) and the fused attention
-forward (fsa_attention_fwd_ex).  The metric is attention forward TFLOP/s
+MX quantisation of Q, K and V (fsa_mx_quantize_qkv, one launch) and the fused
+attention forward (fsa_attention_fwd_ex).  The metric is attention forward TFLOP/s
 (4*B*H*Sq*Sk*D per layer, halved for causal).  Inputs are resident in HBM when
 the timed region starts; L2 is flushed (a 512 MB write) between timed steps.
-The three quantisation launches of a step are captured once as a CUDA graph and
+The quantisation launch of a step is captured once as a CUDA graph and
 replayed (--no-graph: launched eagerly); the attention launch is bracketed by
 CUDA events of its own.  The end-to-end figure makes every call eagerly.
 
@@ -147,11 +147,9 @@ def run_gpu(args, w: Workload, world):
     def quantise(i):
         wl, (qd, kd, vd), (mq, mk, mv, _) = layers[i], inputs[i], bufs[i]
         fq, fp = FMT[wl.fmt_qk], FMT[wl.fmt_pv]
-        fsa.fsa_mx_quantize(qd, 0, fq, out=mq)
-        fsa.fsa_mx_quantize(kd, 0, fq, out=mk)
-        fsa.fsa_mx_quantize(vd, 1, 2 if fp == 3 else fp, out=mv)
+        fsa.fsa_mx_quantize_qkv(qd, kd, vd, fq, 2 if fp == 3 else fp, out=(mq, mk, mv))
 
-    qgraphs = []          # per layer: the three quantisation launches as one CUDA graph
+    qgraphs = []          # per layer: the quantisation launch captured as a CUDA graph
 
     def step(record=False, eager=False):
         for i, (wl, (mq, mk, mv, out)) in enumerate(zip(layers, bufs)):
@@ -258,7 +256,7 @@ def run_gpu(args, w: Workload, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms, e2e_ms = float(t[0]), float(t[1])
     return dict(ms=ms, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks, stats=st, launch_mode=launch_mode,
-                launches=args.steps * 4 * len(layers), bf16_ms=statistics.mean(bf_ms))
+                launches=args.steps * 2 * len(layers), bf16_ms=statistics.mean(bf_ms))
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm

@@ -107,6 +107,18 @@ int fsa_mx_sizes(int B, int H, int S, int D, int layout, int fmt, size_t* codes_
 int fsa_mx_quantize(const void* x_bf16, int B, int H, int S, int D, int layout, int fmt,
                     fsa_mx_tensor* out, void* stream);
 
+/* The operands of one attention call in one kernel launch: q [B][H][Sq][D]
+ * and k [B][Hkv][Sk][D] into FSA_MX_ROWS tensors of format fmt_qk, v
+ * [B][Hkv][Sk][D] into an FSA_MX_COLS_T tensor of format fmt_v (E2M1 for an
+ * EFQ P~ V product).  Codes and scales are identical to three
+ * fsa_mx_quantize calls; argument checks, field writes and launch behaviour
+ * are the same as there.  Errors: FSA_ERR_INVALID_ARG (null or misaligned
+ * pointer, bad shape), FSA_ERR_UNSUPPORTED_FMT (E2M1_EFQ as a storage
+ * format), FSA_ERR_LAUNCH. */
+int fsa_mx_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16, int B, int H, int Hkv,
+                        int Sq, int Sk, int D, int fmt_qk, int fmt_v, fsa_mx_tensor* q_out,
+                        fsa_mx_tensor* k_out, fsa_mx_tensor* v_out, void* stream);
+
 /* ------------------------------------------------------ options and stats */
 typedef enum {
   FSA_EXP_POLY = 0,   /* cubic interpolant of 2^f on the FMA pipe for every element */

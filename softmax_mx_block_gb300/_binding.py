@@ -64,6 +64,8 @@ def load(build_if_missing: bool = True):
             vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             L.fsa_mx_sizes.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
             L.fsa_mx_quantize.argtypes = [vp, i, i, i, i, i, i, ctypes.POINTER(fsa_mx_tensor), vp]
+            L.fsa_mx_quantize_qkv.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i] + \
+                [ctypes.POINTER(fsa_mx_tensor)] * 3 + [vp]
             L.fsa_attention_fwd.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + [vp, i, i, i, i, i, i, i, f, i, i, vp]
             L.fsa_attention_fwd_ex.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + \
                 [vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, vp]
@@ -73,8 +75,8 @@ def load(build_if_missing: bool = True):
             L.fsa_default_opts.restype = None
             L.fsa_status_string.argtypes = [i]
             L.fsa_status_string.restype = ctypes.c_char_p
-            for n in ("fsa_mx_sizes", "fsa_mx_quantize", "fsa_attention_fwd", "fsa_attention_fwd_ex",
-                      "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version"):
+            for n in ("fsa_mx_sizes", "fsa_mx_quantize", "fsa_mx_quantize_qkv", "fsa_attention_fwd",
+                      "fsa_attention_fwd_ex", "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version"):
                 getattr(L, n).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -143,6 +145,28 @@ def fsa_mx_quantize(x: torch.Tensor, layout, fmt, out: MxTensor | None = None, s
     st = out.struct()
     _check(load().fsa_mx_quantize(ctypes.c_void_p(x.data_ptr()), B, H, S, D, int(layout), fmt, ctypes.byref(st),
                                   _stream(stream)), "fsa_mx_quantize")
+    return out
+
+
+def fsa_mx_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt_qk, fmt_v,
+                        out: tuple | None = None, stream=None) -> tuple:
+    """Q, K (FSA_MX_ROWS, fmt_qk) and V (FSA_MX_COLS_T, fmt_v) of one attention call in one launch."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_cuda(t, n, torch.bfloat16)
+    B, H, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Sk, D) or tuple(v.shape) != (B, Hkv, Sk, D):
+        raise FsaError(FSA_ERR_INVALID_ARG, "q, k, v shapes")
+    fmt_qk, fmt_v = _fmt(fmt_qk), _fmt(fmt_v)
+    if out is None:
+        out = (empty_mx(B, H, Sq, D, FSA_MX_ROWS, fmt_qk, q.device),
+               empty_mx(B, Hkv, Sk, D, FSA_MX_ROWS, fmt_qk, q.device),
+               empty_mx(B, Hkv, Sk, D, FSA_MX_COLS_T, fmt_v, q.device))
+    sq, sk, sv = (o.struct() for o in out)
+    _check(load().fsa_mx_quantize_qkv(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                      ctypes.c_void_p(v.data_ptr()), B, H, Hkv, Sq, Sk, D, fmt_qk, fmt_v,
+                                      ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv), _stream(stream)),
+           "fsa_mx_quantize_qkv")
     return out
 
 

@@ -193,6 +193,31 @@ int fsa_mx_quantize(const void* x, int B, int H, int S, int D, int layout, int f
   return launch_status(e);
 }
 
+int fsa_mx_quantize_qkv(const void* q, const void* k, const void* v, int B, int H, int Hkv, int Sq, int Sk, int D,
+                        int fmt_qk, int fmt_v, fsa_mx_tensor* q_out, fsa_mx_tensor* k_out, fsa_mx_tensor* v_out,
+                        void* stream) {
+  size_t cb, sb;
+  if (!q || !k || !v || !q_out || !k_out || !v_out) return FSA_ERR_INVALID_ARG;
+  if (fmt_qk == FSA_FMT_E2M1_EFQ || fmt_v == FSA_FMT_E2M1_EFQ) return FSA_ERR_UNSUPPORTED_FMT;
+  int st;
+  if ((st = fsa_mx_sizes(B, H, Sq, D, FSA_MX_ROWS, fmt_qk, &cb, &sb)) != FSA_OK) return st;
+  if ((st = fsa_mx_sizes(B, Hkv, Sk, D, FSA_MX_ROWS, fmt_qk, &cb, &sb)) != FSA_OK) return st;
+  if ((st = fsa_mx_sizes(B, Hkv, Sk, D, FSA_MX_COLS_T, fmt_v, &cb, &sb)) != FSA_OK) return st;
+  const fsa_mx_tensor* outs[3] = {q_out, k_out, v_out};
+  for (const fsa_mx_tensor* o : outs)
+    if (!o->codes || !o->scales || !aligned16(o->codes) || !aligned16(o->scales)) return FSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FSA_ERR_INVALID_ARG;
+  auto set = [&](fsa_mx_tensor* o, int fmt, int layout, int h, int S) {
+    o->fmt = fmt; o->layout = layout; o->B = B; o->H = h; o->S = S; o->D = D;
+  };
+  set(q_out, fmt_qk, FSA_MX_ROWS, H, Sq);
+  set(k_out, fmt_qk, FSA_MX_ROWS, Hkv, Sk);
+  set(v_out, fmt_v, FSA_MX_COLS_T, Hkv, Sk);
+  return launch_status(fsa::launch_mx_quant_qkv(q, k, v, B * H, B * Hkv, Sq, Sk, D, fmt_qk, fmt_v, q_out->codes,
+                                                q_out->scales, k_out->codes, k_out->scales, v_out->codes,
+                                                v_out->scales, static_cast<cudaStream_t>(stream)));
+}
+
 int fsa_bf16_transpose_v(const void* v, void* vt, int B, int Hkv, int S, int D, void* stream) {
   if (!v || !vt || B <= 0 || Hkv <= 0 || S <= 0 || (D != 64 && D != 128) || !aligned16(v) || !aligned16(vt))
     return FSA_ERR_INVALID_ARG;

@@ -24,6 +24,9 @@ cudaError_t launch_mx_quant_rows(const void* x, int BH, int S, int D, int fmt, v
                                  cudaStream_t st);
 cudaError_t launch_mx_quant_cols(const void* x, int BH, int S, int D, int fmt, void* codes, void* scales,
                                  cudaStream_t st);
+cudaError_t launch_mx_quant_qkv(const void* q, const void* k, const void* v, int BHq, int BHk, int Sq, int Sk, int D,
+                                int fqk, int fv, void* cq, void* sq, void* ck, void* sk, void* cv, void* sv,
+                                cudaStream_t st);
 cudaError_t launch_transpose_v(const void* v, void* vt, int BH, int S, int D, cudaStream_t st);
 
 }  // namespace fsa

@@ -83,18 +83,18 @@ __device__ __forceinline__ uint32_t quant_block32(const float* v, uint32_t* w) {
 // arithmetic.  The tile's 512-byte scale atom is assembled in shared memory
 // (unused slots 0x7F) and written whole.
 // x: [BH][S][D] bf16, codes: [BH*S][row bytes], scales: [BH][ceil(S/128)][512].
+// tile_id = b*h * ceil(S/128) + tile; atom: 512 bytes of shared memory.
 template <int FMT, int D>
-__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __restrict__ x, int S,
-                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+__device__ __forceinline__ void quant_rows_tile(const uint16_t* __restrict__ x, int S, uint8_t* __restrict__ codes,
+                                                uint8_t* __restrict__ scales, int64_t tile_id, uint8_t* atom) {
   constexpr int emax = FMT == 0 ? 8 : 2;
   constexpr int CPR = D / 8;                       // chunks per row
   constexpr int NCH = 128 * CPR / 256;             // chunks per thread
   constexpr int RB = FMT == 2 ? D / 2 : D;         // code bytes per row
-  __shared__ __align__(16) uint8_t atom[512];
   const int t = threadIdx.x;
   const int ntiles = (S + 127) / 128;
-  const int64_t bh = blockIdx.x / ntiles;          // one grid axis: no limit on B*H
-  const int s0 = (int)(blockIdx.x % ntiles) * 128;
+  const int64_t bh = tile_id / ntiles;             // one grid axis: no limit on B*H
+  const int s0 = (int)(tile_id % ntiles) * 128;
   const int nrows = min(128, S - s0);
   const uint16_t* src = x + ((int64_t)bh * S + s0) * D;
   uint8_t* dst = codes + ((int64_t)bh * S + s0) * RB;
@@ -158,8 +158,14 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __re
     if (active && (c & 3) == 0) atom[(r & 31) * 16 + (r >> 5) * 4 + (c >> 2)] = (uint8_t)sbyte;
   }
   __syncthreads();
-  if (t < 32)
-    reinterpret_cast<uint4*>(scales + (int64_t)blockIdx.x * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
+  if (t < 32) reinterpret_cast<uint4*>(scales + tile_id * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
+}
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __restrict__ x, int S,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  __shared__ __align__(16) uint8_t atom[512];
+  quant_rows_tile<FMT, D>(x, S, codes, scales, blockIdx.x, atom);
 }
 
 // --------------------------------------------------------------------------
@@ -168,17 +174,17 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __re
 // quantises two adjacent columns d, d+1 over one 32-key block, and the scale
 // atom (rows d >= D and blocks past the sequence: 0x7F) is written whole.
 // x: [BH][S][D] bf16; codes: [BH][D][Sp] elements; scales: [BH][Sp/128][512].
+// tile_id = b*h * (Sp/128) + tile; tile: 128 x D bf16 of shared memory; atom: 512 bytes.
 template <int FMT, int D>
-__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const uint16_t* __restrict__ x, int S, int Sp,
-                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+__device__ __forceinline__ void quant_cols_tile(const uint16_t* __restrict__ x, int S, int Sp,
+                                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                int64_t tile_id, uint32_t* tile, uint8_t* atom) {
   constexpr int NV = 128 * D / 8 / 256;            // 16-byte vectors per thread
   constexpr int DW = D / 2;                        // 32-bit words per tile row
-  __shared__ __align__(16) uint32_t tile[128 * DW];
-  __shared__ __align__(16) uint8_t atom[512];
   const int t = threadIdx.x;
   const int ntiles = Sp / 128;
-  const int64_t bh = blockIdx.x / ntiles;
-  const int s0 = (int)(blockIdx.x % ntiles) * 128;
+  const int64_t bh = tile_id / ntiles;
+  const int s0 = (int)(tile_id % ntiles) * 128;
   const int nrows = min(128, S - s0);
   const uint16_t* src = x + ((int64_t)bh * S + s0) * D;
   uint4 raw[NV];
@@ -228,8 +234,38 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const uint16_t* __re
     atom[((d + 1) & 31) * 16 + ((d + 1) >> 5) * 4 + kb] = (uint8_t)sb1;
   }
   __syncthreads();
-  if (t < 32)
-    reinterpret_cast<uint4*>(scales + (int64_t)blockIdx.x * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
+  if (t < 32) reinterpret_cast<uint4*>(scales + tile_id * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
+}
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(256) mx_quant_cols_kernel(const uint16_t* __restrict__ x, int S, int Sp,
+                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  __shared__ __align__(16) uint32_t tile[128 * D / 2];
+  __shared__ __align__(16) uint8_t atom[512];
+  quant_cols_tile<FMT, D>(x, S, Sp, codes, scales, blockIdx.x, tile, atom);
+}
+
+// --------------------------------------------------------------------------
+// Q, K and V of one attention call in one launch: CTAs [0, nq) take the tiles
+// of Q, [nq, nq + nk) those of K (rows layout), the rest those of V
+// (transposed layout).  The same codes and scales as three separate launches,
+// without two kernel boundaries between them.
+struct QkvArgs {
+  const uint16_t* x[3];
+  uint8_t* codes[3];
+  uint8_t* scales[3];
+  int Sq, Sk, Spv;
+  int64_t nq, nk;
+};
+
+template <int FQK, int FV, int D>
+__global__ void __launch_bounds__(256) mx_quant_qkv_kernel(const QkvArgs a) {
+  __shared__ __align__(16) uint32_t tile[128 * D / 2];
+  __shared__ __align__(16) uint8_t atom[512];
+  const int64_t b = blockIdx.x;                    // block-uniform branch
+  if (b < a.nq) quant_rows_tile<FQK, D>(a.x[0], a.Sq, a.codes[0], a.scales[0], b, atom);
+  else if (b < a.nq + a.nk) quant_rows_tile<FQK, D>(a.x[1], a.Sk, a.codes[1], a.scales[1], b - a.nq, atom);
+  else quant_cols_tile<FV, D>(a.x[2], a.Sk, a.Spv, a.codes[2], a.scales[2], b - a.nq - a.nk, tile, atom);
 }
 
 // V [BH][S][D] bf16 -> V^T [BH][D][Sp] bf16 (zero padded), one CTA per 128-key tile.
@@ -302,6 +338,46 @@ cudaError_t launch_mx_quant_cols(const void* x, int BH, int S, int D, int fmt, v
     case 0: return quant_cols_d<0>(xs, BH, S, D, c, s, st);
     case 1: return quant_cols_d<1>(xs, BH, S, D, c, s, st);
     default: return quant_cols_d<2>(xs, BH, S, D, c, s, st);
+  }
+}
+
+template <int FQK, int FV>
+static cudaError_t quant_qkv_d(const QkvArgs& a, int64_t n, int D, cudaStream_t st) {
+  if (D == 128) mx_quant_qkv_kernel<FQK, FV, 128><<<(unsigned)n, 256, 0, st>>>(a);
+  else mx_quant_qkv_kernel<FQK, FV, 64><<<(unsigned)n, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int FQK>
+static cudaError_t quant_qkv_fv(const QkvArgs& a, int64_t n, int D, int fv, cudaStream_t st) {
+  switch (fv) {
+    case 0: return quant_qkv_d<FQK, 0>(a, n, D, st);
+    case 1: return quant_qkv_d<FQK, 1>(a, n, D, st);
+    default: return quant_qkv_d<FQK, 2>(a, n, D, st);
+  }
+}
+
+cudaError_t launch_mx_quant_qkv(const void* q, const void* k, const void* v, int BHq, int BHk, int Sq, int Sk, int D,
+                                int fqk, int fv, void* cq, void* sq, void* ck, void* sk, void* cv, void* sv,
+                                cudaStream_t st) {
+  QkvArgs a;
+  a.x[0] = static_cast<const uint16_t*>(q);
+  a.x[1] = static_cast<const uint16_t*>(k);
+  a.x[2] = static_cast<const uint16_t*>(v);
+  a.codes[0] = static_cast<uint8_t*>(cq); a.scales[0] = static_cast<uint8_t*>(sq);
+  a.codes[1] = static_cast<uint8_t*>(ck); a.scales[1] = static_cast<uint8_t*>(sk);
+  a.codes[2] = static_cast<uint8_t*>(cv); a.scales[2] = static_cast<uint8_t*>(sv);
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.Spv = (Sk + 127) / 128 * 128;
+  a.nq = ((int64_t)Sq + 127) / 128 * BHq;
+  a.nk = ((int64_t)Sk + 127) / 128 * BHk;
+  const int64_t n = a.nq + a.nk + (int64_t)a.Spv / 128 * BHk;
+  if (n > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  switch (fqk) {
+    case 0: return quant_qkv_fv<0>(a, n, D, fv, st);
+    case 1: return quant_qkv_fv<1>(a, n, D, fv, st);
+    default: return quant_qkv_fv<2>(a, n, D, fv, st);
   }
 }
 

@@ -71,6 +71,17 @@ def test_argument_checks_reject_before_launch(lib):
     x = fsa_mx_tensor(16, 16, 0, 0, 0, 0, 0, 0)
     assert lib.fsa_mx_quantize(vp(16), 1, 1, 128, 128, 0, 3, ctypes.byref(x), vp(0)) == fsa.FSA_ERR_UNSUPPORTED_FMT
     assert lib.fsa_mx_quantize(vp(0), 1, 1, 128, 128, 0, 0, ctypes.byref(x), vp(0)) == fsa.FSA_ERR_INVALID_ARG
+    # the one-launch Q/K/V form: null or misaligned inputs, EFQ as a storage format, a bad head dimension
+    ox, oy, oz = (fsa_mx_tensor(16, 16, 0, 0, 0, 0, 0, 0) for _ in range(3))
+
+    def qkv(q, k, vv, D, fq, fv, o=ox):
+        return lib.fsa_mx_quantize_qkv(q, k, vv, 1, 4, 2, 128, 256, D, fq, fv, ctypes.byref(o), ctypes.byref(oy),
+                                       ctypes.byref(oz), vp(0))
+    assert qkv(vp(16), vp(0), vp(16), 128, 0, 0) == fsa.FSA_ERR_INVALID_ARG
+    assert qkv(vp(16), vp(24), vp(16), 128, 0, 0) == fsa.FSA_ERR_INVALID_ARG
+    assert qkv(vp(16), vp(16), vp(16), 128, 0, 3) == fsa.FSA_ERR_UNSUPPORTED_FMT
+    assert qkv(vp(16), vp(16), vp(16), 96, 0, 0) == fsa.FSA_ERR_INVALID_ARG
+    assert qkv(vp(16), vp(16), vp(16), 128, 0, 0, o=fsa_mx_tensor(16, 0, 0, 0, 0, 0, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
 
 
 def test_kernel_poly_constants_match_oracle():

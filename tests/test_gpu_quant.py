@@ -103,3 +103,63 @@ def test_quant_full_workloads(name):
     _check_rows(q, fq)
     _check_rows(k, fq)
     _check_cols(v, fv)
+
+
+@pytest.mark.parametrize("fq,fv,B,H,Hkv,Sq,Sk,D", [
+    (0, 0, 1, 4, 2, 300, 300, 128),      # GQA, ragged tail
+    (1, 2, 1, 2, 2, 77, 200, 64),        # E2M3 / E2M1, rectangular, D 64
+    (2, 2, 2, 3, 1, 129, 1, 128),        # one key
+    (2, 0, 1, 1, 1, 512, 384, 64),
+])
+def test_quant_qkv_one_launch(fq, fv, B, H, Hkv, Sq, Sk, D):
+    """The one-launch Q/K/V form writes the codes and scales of three separate
+    calls, byte for byte (padding slots included), and those are the oracle's."""
+    fsa = _fsa()
+    q = edge_tensor((B, H, Sq, D), 30 + fq)
+    k = edge_tensor((B, Hkv, Sk, D), 31 + fq)
+    v = edge_tensor((B, Hkv, Sk, D), 32 + fv)
+    qd, kd, vd = _dev(q), _dev(k), _dev(v)
+    mq, mk, mv = fsa.fsa_mx_quantize_qkv(qd, kd, vd, fq, fv)
+    sq = fsa.fsa_mx_quantize(qd, fsa.FSA_MX_ROWS, fq)
+    sk = fsa.fsa_mx_quantize(kd, fsa.FSA_MX_ROWS, fq)
+    sv = fsa.fsa_mx_quantize(vd, fsa.FSA_MX_COLS_T, fv)
+    torch.cuda.synchronize()
+    for a, b in ((mq, sq), (mk, sk), (mv, sv)):
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+    c, s_ = unpack_rows(mq.codes.cpu().numpy(), mq.scales.cpu().numpy(), fq, B, H, Sq, D)
+    oc, os_ = oracle.mx_quantize_rows(q, fq)
+    np.testing.assert_array_equal(s_, os_)
+    np.testing.assert_array_equal(c, oc)
+    c, s_ = unpack_cols(mv.codes.cpu().numpy(), mv.scales.cpu().numpy(), fv, B, Hkv, Sk, D)
+    oc, os_ = oracle.mx_quantize_cols(v, fv)
+    np.testing.assert_array_equal(s_, os_)
+    np.testing.assert_array_equal(c, oc)
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_quant_padding_slots(layout):
+    """Scale slots with no data hold 2^0 (0x7F): rows past S and blocks past D
+    (rows layout), rows d >= D and key blocks past S (transposed layout)."""
+    fsa = _fsa()
+    B, H, S, D = 1, 2, 200, 64
+    x = edge_tensor((B, H, S, D), 40)
+    mt = fsa.fsa_mx_quantize(_dev(x), layout, 0)
+    torch.cuda.synchronize()
+    sc = mt.scales.cpu().numpy().reshape(B * H, -1, 512)
+    r = np.arange(128)
+    slot = lambda rr, b: (rr % 32) * 16 + (rr // 32) * 4 + b
+    if layout == 0:
+        for bh in range(B * H):
+            assert (sc[bh, 0][slot(r, 2)] == 0x7F).all() and (sc[bh, 0][slot(r, 3)] == 0x7F).all()
+            tail = r[r >= S - 128]
+            for b in range(4):
+                assert (sc[bh, 1][slot(tail, b)] == 0x7F).all()
+    else:
+        dd = r[r >= D]
+        for bh in range(B * H):
+            for t in range(2):
+                for b in range(4):
+                    assert (sc[bh, t][slot(dd, b)] == 0x7F).all()
+            # block 3 of tile 1 (keys 224..255) lies wholly past S = 200
+            for dv in range(D):
+                assert sc[bh, 1][slot(dv, 3)] == 0x7F

@@ -119,6 +119,18 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks of the default process group
+    (the values themselves when there is none): the slowest replica sets the time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def run_gpu(args, w: Workload, world):
     import torch
     import softmax_mx_block_gb300 as fsa
@@ -250,11 +262,7 @@ def run_gpu(args, w: Workload, world):
             if it >= args.warmup:
                 bf_ms.append(e0.elapsed_time(e1))
 
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([total_ms / args.steps, e2e_ms], dev)
     return dict(ms=ms, attn_ms=attn_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks, stats=st, launch_mode=launch_mode,
                 launches=args.steps * 2 * len(layers), bf16_ms=statistics.mean(bf_ms))
 

@@ -118,6 +118,89 @@ def test_floor_uniform_rows_and_error_order():
     assert errs[0] < errs[1] < errs[2]        # 3, 3 and 1 mantissa bits, narrower range for E2M3
 
 
+def test_floor_and_emulate_use_each_blocks_own_scale():
+    """Q and K rows whose two 32-element blocks differ in magnitude by 2^6 (every
+    value exact in all three formats): with unquantised P the floor equals exact
+    attention, which only holds if each block is dequantised with its own scale."""
+    B, H, S, D = 1, 1, 70, 64
+    rng = np.random.default_rng(8)
+    def mixed(seed):
+        x = np.random.default_rng(seed).integers(-3, 4, (B, H, S, D)).astype(np.float32)
+        x[..., 32:] /= 64.0
+        return bf(x)
+    q, k, v = mixed(1), mixed(2), rnd((B, H, S, D), 3, integer=True)
+    rows = allrows(B, H, S)
+    ex = oracle.attn_exact(q, k, v, True, 0.5, rows)
+    for fq in (0, 1, 2):
+        mx = oracle.MxInputs.from_bf16(q, k, v, fq, fq)
+        assert not np.array_equal(mx.qs[..., 0], mx.qs[..., 1])
+        fl = oracle.attn_floor(mx, S, True, 0.5, fq, rows, quantize_p=False)
+        assert np.allclose(fl, ex, atol=1e-12), fq
+
+
+def test_floor_p_quantisation_closed_forms():
+    """Closed forms of the floor's P quantisation (MX rule on 32-key blocks, E2M1 P).
+    (a) Keys 0..15 score 0 and keys 16..31 score -4 share one block whose scale
+        comes from p = 1 (E = 0 - 2): e^-4 * 2^2 = 0.073 rounds to code 0, so O is
+        the mean of v over keys 0..15.
+    (b) Two keys scoring 0 and -0.875: e^-0.875 * 2^2 = 1.667 rounds to 1.5, so
+        p~ = (1, 0.375) and O = (v0 + 0.375 v1) / 1.375."""
+    D = 64
+    # (a) one query, q = e_0; k_j = (0 or -4) e_0; scale 1
+    q = np.zeros((1, 1, 1, D), np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, 1, 32, D), np.float32)
+    k[0, 0, 16:, 0] = -4.0
+    v = np.random.default_rng(4).integers(-3, 4, (1, 1, 32, D)).astype(np.float32)
+    mx = oracle.MxInputs.from_bf16(bf(q), bf(k), bf(v), 0, 2)
+    out = oracle.attn_floor(mx, 32, False, 1.0, 2, [0])
+    assert np.allclose(out[0], v[0, 0, :16].mean(axis=0), atol=1e-12)
+    # (b) two keys
+    k = np.zeros((1, 1, 2, D), np.float32)
+    k[0, 0, 1, 0] = -0.875
+    v = np.zeros((1, 1, 2, D), np.float32)
+    v[0, 0, 0] = 1.0
+    v[0, 0, 1] = -2.0
+    mx = oracle.MxInputs.from_bf16(bf(q), bf(k), bf(v), 0, 2)
+    out = oracle.attn_floor(mx, 2, False, 1.0, 2, [0])
+    assert np.allclose(out[0], (1.0 - 0.75) / 1.375, atol=1e-12)
+
+
+def test_emulate_with_exact_exp_equals_floor_on_one_tile():
+    """On a single key tile the frozen maximum is the exact row maximum, so the
+    emulation with the exact exp2 model (every mask bit set) takes the same codes as
+    the exp-then-quantise floor and gives the same output; the cubic (no bit set)
+    does not."""
+    B, H, S, D = 1, 2, 128, 64
+    rng = np.random.default_rng(5)
+    q = bf(rng.standard_normal((B, H, S, D)) * 1.5)
+    k, v = bf(rng.standard_normal((B, H, S, D))), bf(rng.standard_normal((B, H, S, D)))
+    rows = allrows(B, H, S)
+    for fq in (0, 1):
+        mx = oracle.MxInputs.from_bf16(q, k, v, fq, fq)
+        fl = oracle.attn_floor(mx, S, False, 0.125, fq, rows)
+        hw = oracle.fsa_emulate(mx, S, False, 0.125, fq, rows, delta=8.0, mufu_mask=0xFFFFFFFF)["out"]
+        po = oracle.fsa_emulate(mx, S, False, 0.125, fq, rows, delta=8.0, mufu_mask=0)["out"]
+        assert np.array_equal(hw, fl), fq
+        assert not np.array_equal(po, fl), fq
+
+
+def test_emulate_efq_codes_span_the_e2m1_range():
+    """The EFQ rule maps onto all nonnegative E2M1 codes: over a few random rows every
+    code 0..7 occurs, the block holding the frozen maximum gets exactly code 6
+    (r = 2, 2r + beta = 6), and no code exceeds 7."""
+    B, H, S, D = 1, 1, 512, 64
+    q, k, v = rnd((B, H, S, D), 1, 1.5), rnd((B, H, S, D), 2), rnd((B, H, S, D), 3)
+    mx = oracle.MxInputs.from_bf16(q, k, v, 2, 2)
+    rows = np.arange(0, S, 7, dtype=np.int64)
+    res = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=8.0, dump=True)
+    pc = res["p_codes"]
+    assert set(np.unique(pc)) == set(range(8))
+    for n in range(len(rows)):
+        jmax = int(np.argmax(res["s"][n, :128]))     # the first tile's maximum sets M
+        assert pc[n, jmax] == 6
+
+
 # --------------------------------------------------------------------------- exp2 approximation
 def test_exp2_poly_exact_at_integers_and_error_bound():
     for n in range(-60, 10):
@@ -254,6 +337,31 @@ def test_bf16_emulate_pins():
     kk[0, 0, 200] = 8.0 * bf16_bits_to_f32(q)[0, 0, 250]
     r = oracle.bf16_emulate(q, bf(kk), v, False, 0.125, rows)
     assert r["rescales"][250] == 1
+    # without such a key, tile maxima move by far less than tau: no row rescales
+    assert oracle.bf16_emulate(q, k, v, False, 0.125, rows)["rescales"].sum() == 0
+
+
+def test_bf16_emulate_rounds_p_to_nearest_even():
+    """p is rounded to bf16 with ties to even.  Scores 0 and s1 = -1.4140625 +
+    0.0027770996 (exact in fp32) with c = fp32(scale log2 e) = 1: 2^s1 in fp32 is
+    0.3759765625, exactly halfway between the bf16 neighbours 0.375 (even) and
+    0.376953125, so p1 = 0.375 and, with v0 = 0 and v1 = 1, O = 0.375 / 1.375."""
+    D = 64
+    scale = float(np.float32(0.6931472))
+    assert np.float32(np.float64(np.float32(scale)) * 1.4426950408889634) == 1.0
+    a, b = np.float32(-1.4140625), np.float32(0.0027770996)
+    s1 = np.float32(np.float64(a) + np.float64(b))
+    assert np.float64(s1) == np.float64(a) + np.float64(b)
+    assert np.float32(np.exp2(np.float64(s1))) == np.float32(0.3759765625)
+    q = np.zeros((1, 1, 1, D), np.float32)
+    q[..., :2] = 1.0
+    k = np.zeros((1, 1, 2, D), np.float32)
+    k[0, 0, 1, :2] = (a, b)
+    v = np.zeros((1, 1, 2, D), np.float32)
+    v[0, 0, 1] = 1.0
+    assert np.array_equal(bf16_bits_to_f32(bf(k)), k)
+    out = oracle.bf16_emulate(bf(q), bf(k), bf(v), False, scale, [0])["out"]
+    assert np.allclose(out[0], 0.375 / 1.375, rtol=0, atol=1e-15)
 
 
 @pytest.mark.parametrize("fq,fp,mufu", [(0, 0, 0xFFFFFFFF), (0, 0, 0), (2, 3, 0), (1, 2, 0x77777777)])

@@ -124,6 +124,18 @@ def test_mx_scale_hand_cases(fmt, emax):
 
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_mx_scale_clamps_at_minus_127(fmt):
+    """E8M0 has no scale below 2^-127: a block whose max is 2^-126 (the smallest
+    normal bf16) would want E = -126 - emax and gets -127 (scale byte 0); the max
+    element then carries the factor 2^(127 - 126) = 2 in its code."""
+    x = np.zeros((1, 32), np.float32)
+    x[0, 5] = 2.0 ** -126
+    c, s = oracle.mx_quantize_rows(_bf16(x), fmt)
+    assert s[0, 0] == 0
+    assert oracle.decode(fmt, int(c[0, 5])) == 2.0
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_mx_exact_roundtrip_on_representable(fmt):
     """x = decode(code) * 2^E with the block max at the format's top binade
     quantises back to the same codes and the scale byte E + 127."""

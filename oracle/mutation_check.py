@@ -66,6 +66,15 @@ M = [
  ("emu block max wrong", "            for (int j = jb; j < je; ++j) if (s[j - j0] > smax) smax = s[j - j0];\n            float tmax", "            smax = s[jb - j0];\n            float tmax"),
  ("k scale index", "op->ks[krow * nb + d / 32]", "op->ks[krow * nb]"),
  ("v scale index", "op->vs[vrow * (Skp / 32) + j / 32]", "op->vs[vrow * (Skp / 32)]"),
+ ("mx pads with ones", "idx * elem_stride]) : 0.0;", "idx * elem_stride]) : 1.0;"),
+ ("groups by batch only", "k[n].key = (int64_t)b * g->Hkv + kvh;", "k[n].key = (int64_t)b;"),
+ ("exact v from k", "kv->vh[(int64_t)d * nk + j] = bf16_to_double(v[base + (int64_t)j * D + d]);",
+  "kv->vh[(int64_t)d * nk + j] = bf16_to_double(k[base + (int64_t)j * D + d]);"),
+ ("ambiguity too small", "#define AMB_S 4.76837158203125e-07   /* 2^-21 */", "#define AMB_S 1e-9"),
+ ("tiles not counted", "          ++tv;\n", ""),
+ ("fallbacks not counted", "              ++fb;\n", ""),
+ ("efq beta sign", "double y = 2.0 * (double)r + (double)opt->beta;", "double y = 2.0 * (double)r - (double)opt->beta;"),
+ ("bf16 rescale keeps l", "            l *= alpha;\n            M = x;", "            M = x;"),
 ]
 
 

@@ -337,6 +337,9 @@ def test_bf16_emulate_pins():
     kk[0, 0, 200] = 8.0 * bf16_bits_to_f32(q)[0, 0, 250]
     r = oracle.bf16_emulate(q, bf(kk), v, False, 0.125, rows)
     assert r["rescales"][250] == 1
+    # the rescale keeps numerator and denominator consistent: still exact attention
+    ex2 = oracle.attn_exact(q, bf(kk), v, False, 0.125, rows)
+    assert np.abs(r["out"][250] - ex2[250]).max() / np.sqrt((ex2[250] ** 2).mean()) < 1e-2
     # without such a key, tile maxima move by far less than tau: no row rescales
     assert oracle.bf16_emulate(q, k, v, False, 0.125, rows)["rescales"].sum() == 0
 

@@ -29,7 +29,8 @@
  *     are detected on the host before any launch; nothing is enqueued then.
  *   - Shapes: B batch, H query heads, Hkv key/value heads (H % Hkv == 0; query
  *     head h reads kv head h / (H/Hkv)), Sq queries, Sk keys, head dim D in
- *     {64, 128}; B*H <= 65535, Sq <= 65535*128, Sk <= 2^24 (else INVALID_ARG).
+ *     {64, 128}; the attention calls also need B*H <= 65535, Sq <= 65535*128
+ *     and Sk <= 2^24 (else INVALID_ARG).
  *     Causal masking is bottom-right aligned: key j is visible to
  *     query i iff j <= i + Sk - Sq.  A query with no visible key gets a zero
  *     output row.

@@ -92,3 +92,17 @@ def test_kernel_poly_constants_match_oracle():
     lits = [float.fromhex(x[:-1]) for x in re.findall(r"0x1\.[0-9a-f]+p-?\d+f", line)]
     c = oracle.exp2_poly_coeffs()
     assert sorted(lits) == sorted(float(x) for x in c[1:])
+
+
+def test_binding_refuses_host_tensors(lib):
+    """No CPU path: every compute entry of the binding rejects host tensors before
+    any call into the library, instead of computing on the CPU."""
+    import torch
+    import softmax_mx_block_gb300 as fsa
+    x = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16)
+    with pytest.raises(fsa.FsaError, match="CUDA tensor"):
+        fsa.fsa_mx_quantize(x, fsa.FSA_MX_ROWS, "E4M3")
+    with pytest.raises(fsa.FsaError, match="CUDA tensor"):
+        fsa.fsa_mx_quantize_qkv(x, x, x, "E4M3", "E4M3")
+    with pytest.raises(fsa.FsaError, match="CUDA tensor"):
+        fsa.fsa_attention_fwd_bf16(x, x, x)

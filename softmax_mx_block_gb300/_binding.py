@@ -129,6 +129,29 @@ def fsa_mx_sizes(B, H, S, D, layout, fmt):
     return cb.value, sb.value
 
 
+def _check_mx_buffers(m: MxTensor, name: str):
+    """codes and scales are contiguous uint8 tensors of at least fsa_mx_sizes bytes
+    for the tensor's own shape, layout and format (the kernels write and read that
+    many bytes; the C ABI receives bare pointers and cannot check)."""
+    for t, part in ((m.codes, "codes"), (m.scales, "scales")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or not t.is_contiguous():
+            raise FsaError(FSA_ERR_INVALID_ARG, f"{name}.{part} must be a contiguous uint8 tensor")
+    cb, sb = fsa_mx_sizes(m.B, m.H, m.S, m.D, m.layout, m.fmt)
+    if m.codes.numel() < cb or m.scales.numel() < sb:
+        raise FsaError(FSA_ERR_INVALID_ARG, f"{name}: codes/scales hold {m.codes.numel()}/{m.scales.numel()} bytes, "
+                                            f"need {cb}/{sb}")
+
+
+def _need_mx(m: MxTensor, name: str, device):
+    """An MX tensor on the given CUDA device with buffers large enough for it."""
+    for t, part in ((m.codes, "codes"), (m.scales, "scales")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"{name}.{part} must be a CUDA tensor")
+        if t.device != device:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"{name}.{part} is on {t.device}, the call on {device}")
+    _check_mx_buffers(m, name)
+
+
 def empty_mx(B, H, S, D, layout, fmt, device) -> MxTensor:
     cb, sb = fsa_mx_sizes(B, H, S, D, layout, fmt)
     return MxTensor(torch.empty(cb, dtype=torch.uint8, device=device), torch.empty(sb, dtype=torch.uint8, device=device),
@@ -142,6 +165,9 @@ def fsa_mx_quantize(x: torch.Tensor, layout, fmt, out: MxTensor | None = None, s
     fmt = _fmt(fmt)
     if out is None:
         out = empty_mx(B, H, S, D, layout, fmt, x.device)
+    else:
+        out.fmt, out.layout, out.B, out.H, out.S, out.D = fmt, int(layout), B, H, S, D
+        _need_mx(out, "out", x.device)
     st = out.struct()
     _check(load().fsa_mx_quantize(ctypes.c_void_p(x.data_ptr()), B, H, S, D, int(layout), fmt, ctypes.byref(st),
                                   _stream(stream)), "fsa_mx_quantize")
@@ -162,6 +188,11 @@ def fsa_mx_quantize_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, fmt_q
         out = (empty_mx(B, H, Sq, D, FSA_MX_ROWS, fmt_qk, q.device),
                empty_mx(B, Hkv, Sk, D, FSA_MX_ROWS, fmt_qk, q.device),
                empty_mx(B, Hkv, Sk, D, FSA_MX_COLS_T, fmt_v, q.device))
+    else:
+        for o, (h, S, layout, f), n in zip(out, ((H, Sq, FSA_MX_ROWS, fmt_qk), (Hkv, Sk, FSA_MX_ROWS, fmt_qk),
+                                                 (Hkv, Sk, FSA_MX_COLS_T, fmt_v)), ("q_out", "k_out", "v_out")):
+            o.fmt, o.layout, o.B, o.H, o.S, o.D = f, layout, B, h, S, D
+            _need_mx(o, n, q.device)
     sq, sk, sv = (o.struct() for o in out)
     _check(load().fsa_mx_quantize_qkv(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
                                       ctypes.c_void_p(v.data_ptr()), B, H, Hkv, Sq, Sk, D, fmt_qk, fmt_v,
@@ -202,6 +233,14 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
     if out is None:
         out = torch.empty((B, H, Sq, D), dtype=torch.float32, device=q.codes.device)
     _need_cuda(out, "out", torch.float32)
+    if out.numel() < B * H * Sq * D:
+        raise FsaError(FSA_ERR_INVALID_ARG, "out is smaller than B*H*Sq*D")
+    for m, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_mx(m, n, out.device)
+    if stats is not None:
+        _need_cuda(stats, "stats")
+        if stats.device != out.device or stats.numel() * stats.element_size() < STATS_BYTES:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"stats must hold {STATS_BYTES} bytes on {out.device}")
     o = default_opts()
     if delta is not None:
         o.delta = float(delta)
@@ -215,6 +254,8 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
         o.schedule = int(schedule)
     if row_fallbacks is not None:
         _need_cuda(row_fallbacks, "row_fallbacks", torch.int32)
+        if row_fallbacks.device != out.device or row_fallbacks.numel() < B * H * Sq:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"row_fallbacks must hold B*H*Sq int32 on {out.device}")
         o.row_fallbacks = row_fallbacks.data_ptr()
     qs, ks, vs = q.struct(), k.struct(), v.struct()
     _check(load().fsa_attention_fwd_ex(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs),

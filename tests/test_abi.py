@@ -106,3 +106,24 @@ def test_binding_refuses_host_tensors(lib):
         fsa.fsa_mx_quantize_qkv(x, x, x, "E4M3", "E4M3")
     with pytest.raises(fsa.FsaError, match="CUDA tensor"):
         fsa.fsa_attention_fwd_bf16(x, x, x)
+
+
+def test_binding_checks_mx_buffers(lib):
+    """The binding checks what the C ABI cannot see behind its bare pointers: MX
+    buffers of the right dtype and at least fsa_mx_sizes bytes, on a CUDA device."""
+    import torch
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import MxTensor, _check_mx_buffers, _need_mx
+    B, H, S, D = 1, 2, 300, 64
+    for layout, fmt in [(fsa.FSA_MX_ROWS, 0), (fsa.FSA_MX_ROWS, 2), (fsa.FSA_MX_COLS_T, 1), (fsa.FSA_MX_COLS_T, 2)]:
+        cb, sb = fsa.fsa_mx_sizes(B, H, S, D, layout, fmt)
+        ok = MxTensor(torch.empty(cb, dtype=torch.uint8), torch.empty(sb, dtype=torch.uint8), fmt, layout, B, H, S, D)
+        _check_mx_buffers(ok, "t")
+        for bad in (MxTensor(torch.empty(cb - 16, dtype=torch.uint8), ok.scales, fmt, layout, B, H, S, D),
+                    MxTensor(ok.codes, torch.empty(sb - 1, dtype=torch.uint8), fmt, layout, B, H, S, D),
+                    MxTensor(ok.codes.view(torch.int8), ok.scales, fmt, layout, B, H, S, D),
+                    MxTensor(ok.codes, ok.scales, fmt, layout, B, H, S + 128, D)):
+            with pytest.raises(fsa.FsaError):
+                _check_mx_buffers(bad, "t")
+        with pytest.raises(fsa.FsaError, match="CUDA tensor"):
+            _need_mx(ok, "t", torch.device("cpu"))

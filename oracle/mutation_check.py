@@ -75,6 +75,12 @@ M = [
  ("fallbacks not counted", "              ++fb;\n", ""),
  ("efq beta sign", "double y = 2.0 * (double)r + (double)opt->beta;", "double y = 2.0 * (double)r - (double)opt->beta;"),
  ("bf16 rescale keeps l", "            l *= alpha;\n            M = x;", "            M = x;"),
+ ("exact no max shift", "        if (s[j] > m) m = s[j];\n      }\n      double l = 0.0;",
+  "        m = 0.0;\n      }\n      double l = 0.0;"),
+ ("amb ignores fallback test", "<= dx + dM + 1.2e-7 * fabs(thr)) undetermined = 1;", "< 0.0) undetermined = 1;"),
+ ("amb alpha exact", "const double ra = 0.6931471805599453 * (dM + dx) + AMB_X;", "const double ra = 0.0;"),
+ ("amb block exponent", "if (Elo != Ehi && Ehi - emax > -127 && Elo - emax < 127) blk_undet = 1;", "blk_undet = 0;"),
+ ("amb block step", "dp = 0.25 * pt[j - j0] + orc_decode(efmt, 1) * sc * 2.0;", "dp = 0.0;"),
 ]
 
 

@@ -367,6 +367,50 @@ def test_bf16_emulate_rounds_p_to_nearest_even():
     assert np.allclose(out[0], 0.375 / 1.375, rtol=0, atol=1e-15)
 
 
+def _one_query_case(kvals, D=64):
+    """One query e_0 against keys k_j = kvals[j] e_0 (every value exact in bf16 and
+    E4M3), scale fp32(ln 2) so that c = fp32(scale log2 e) = 1 and the log2-domain
+    score of key j is kvals[j] exactly; V random integers."""
+    S = len(kvals)
+    q = np.zeros((1, 1, 1, D), np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, 1, S, D), np.float32)
+    k[0, 0, :, 0] = kvals
+    v = np.random.default_rng(9).integers(-3, 4, (1, 1, S, D)).astype(np.float32)
+    assert np.array_equal(bf16_bits_to_f32(bf(k)), k)
+    scale = float(np.float32(0.6931472))
+    assert np.float32(np.float64(np.float32(scale)) * 1.4426950408889634) == 1.0
+    return oracle.MxInputs.from_bf16(bf(q), bf(k), bf(v), 0, 0), S, scale
+
+
+def test_emulate_ambiguity_flags_boundary_cases():
+    """The bound of undetermined decisions sees the two fp32 boundaries that a score
+    perturbation of 2^-21 can cross.  Keys: tile 0 holds the maximum 0 (M = 0);
+    (a) a block of tile 1 whose maximum is exactly -3, so its block exponent sits on
+    floor's boundary: the bound is positive and covers the move when the scores
+    grow by 2^-21 and the exponent drops by one; (b) a tile-1 key exactly at M +
+    delta = 8: the fallback decision is undetermined, so the bound is infinite, and
+    the perturbed run does fall back."""
+    rng = np.random.default_rng(3)
+    grid = np.array([-(1 + i / 8) * 2.0 ** e for i in range(8) for e in range(-1, 3)], np.float32)
+    kv = rng.choice(grid[grid < -3.0], 256)
+    kv[:128] = rng.choice(grid, 128)
+    kv[0] = 0.0
+    kv[128] = -3.0
+    mx, S, scale = _one_query_case(kv)
+    base = oracle.fsa_emulate(mx, S, False, scale, 0, [0], delta=8.0, mufu_mask=0xFFFFFFFF, ambiguity=True)
+    pert = oracle.fsa_emulate(mx, S, False, scale, 0, [0], delta=8.0, mufu_mask=0xFFFFFFFF, s_perturb=2.0 ** -21)
+    diff = np.abs(pert["out"] - base["out"])
+    assert np.isfinite(base["amb"]).all() and base["amb"].max() > 0
+    assert diff.max() > 0 and np.all(diff <= base["amb"] * (1 + 1e-9) + 1e-15)
+    kv[130] = 8.0
+    mx, S, scale = _one_query_case(kv)
+    base = oracle.fsa_emulate(mx, S, False, scale, 0, [0], delta=8.0, mufu_mask=0xFFFFFFFF, ambiguity=True)
+    pert = oracle.fsa_emulate(mx, S, False, scale, 0, [0], delta=8.0, mufu_mask=0xFFFFFFFF, s_perturb=2.0 ** -21)
+    assert base["fallbacks"][0] == 0 and pert["fallbacks"][0] == 1
+    assert np.isinf(base["amb"]).all()
+
+
 @pytest.mark.parametrize("fq,fp,mufu", [(0, 0, 0xFFFFFFFF), (0, 0, 0), (2, 3, 0), (1, 2, 0x77777777)])
 def test_emulate_ambiguity_bound_covers_score_perturbations(fq, fp, mufu):
     """amb bounds how far the output can move when the fp32 scores move within the

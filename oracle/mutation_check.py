@@ -81,6 +81,11 @@ M = [
  ("amb alpha exact", "const double ra = 0.6931471805599453 * (dM + dx) + AMB_X;", "const double ra = 0.0;"),
  ("amb block exponent", "if (Elo != Ehi && Ehi - emax > -127 && Elo - emax < 127) blk_undet = 1;", "blk_undet = 0;"),
  ("amb block step", "dp = 0.25 * pt[j - j0] + orc_decode(efmt, 1) * sc * 2.0;", "dp = 0.0;"),
+ ("e4m3 no nan", "  if (fmt == 0 && e == 15 && m == 7) return NAN;\n", ""),
+ ("nan loses sign", "if (isnan(x)) return fmt == 0 ? (sbit | 0x7F) : sbit;", "if (isnan(x)) return fmt == 0 ? 0x7F : sbit;"),
+ ("subnormal quantum", "int emin = 1 - f.bias;                       /* exponent of the smallest normal */",
+  "int emin = -f.bias;"),
+ ("nonfinite codes", "c[i] = (uint8_t)(fmt == 0 ? 0x7F : 0);", "c[i] = (uint8_t)0x7F;"),
 ]
 
 

@@ -187,9 +187,21 @@ def test_mx_cols_blocks_along_sequence():
     assert np.array_equal(c, c2) and np.array_equal(s, s2)
 
 
-def test_mx_nonfinite_block():
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_mx_nonfinite_block(fmt):
+    """A block with an Inf takes the E8M0 NaN scale 0xFF (OCP MX: the whole block
+    then decodes to NaN).  Its element codes: the E4M3 NaN code 0x7F, or 0 in the
+    formats that have no NaN encoding; the finite neighbour block is untouched."""
     x = np.ones((1, 64), np.float32)
     x[0, 40] = np.inf
-    c, s = oracle.mx_quantize_rows(_bf16(x), 0)
-    assert s[0, 1] == 0xFF and s[0, 0] == 127 - 8
-    assert np.all(c[0, 32:] == 0x7F)
+    c, s = oracle.mx_quantize_rows(_bf16(x), fmt)
+    assert s[0, 1] == 0xFF and s[0, 0] == 127 - oracle.EMAX[fmt]
+    assert np.all(c[0, 32:] == (0x7F if fmt == 0 else 0))
+    assert math.isnan(oracle.decode(3, int(s[0, 1])))
+
+
+def test_encode_nan_keeps_sign_e4m3():
+    """E4M3 encodes NaN as S.1111.111 (OCP); the encoder keeps the sign of the NaN."""
+    assert oracle.encode(0, float("nan")) == 0x7F
+    assert oracle.encode(0, -float("nan")) == 0xFF
+    assert math.isnan(oracle.decode(0, 0x7F)) and math.isnan(oracle.decode(0, 0xFF))

@@ -60,13 +60,14 @@ class MxOperands(ctypes.Structure):
 
 
 class FsaOpts(ctypes.Structure):
-    _fields_ = [("delta", ctypes.c_float), ("mufu_mask", ctypes.c_uint32), ("beta", ctypes.c_int),
-                ("s_perturb", ctypes.c_double)]
+    _fields_ = [("delta", ctypes.c_float), ("mufu_mask", ctypes.c_uint32), ("beta", ctypes.c_float),
+                ("efq_a", ctypes.c_float), ("phi", ctypes.c_float), ("s_perturb", ctypes.c_double)]
 
 
 class FsaDump(ctypes.Structure):
     _fields_ = [("s", ctypes.c_void_p), ("p_codes", ctypes.c_void_p), ("p_scales", ctypes.c_void_p),
-                ("m_frozen", ctypes.c_void_p), ("amb", ctypes.c_void_p)]
+                ("m_frozen", ctypes.c_void_p), ("amb", ctypes.c_void_p), ("s_in", ctypes.c_void_p),
+                ("p_alt", ctypes.c_void_p)]
 
 
 def lib():
@@ -219,9 +220,18 @@ def attn_floor(mx: MxInputs, Sk, causal, scale, fmt_p, rows, quantize_p=True, nt
     return out
 
 
-def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_mask=0, beta=2,
-                dump=False, ambiguity=False, s_perturb=0.0, nthreads=None):
+EFQ_A, EFQ_B, EFQ_PHI = 1.6875, 3.5, 0.5625      # the EFQ rule's constants (see efq_scan.py)
+
+
+def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_mask=0, beta=EFQ_B,
+                efq_a=EFQ_A, phi=EFQ_PHI, dump=False, ambiguity=False, s_perturb=0.0, s_in=None, nthreads=None):
     """Step-by-step emulation of the fused MX forward.  fmt_p: 0/1/2 exp path, 3 EFQ.
+
+    EFQ codes are clamp(rne(fmaf(s, fp32(efq_a c), fp32(beta - fp32(efq_a (M + E))))), 0, 7)
+    with the block exponent E = floor(tmax + phi) - 2 (phi applies to EFQ only; the exp
+    path keeps the OCP rule).  s_in (float32 [rows, Skp], optional): raw scores to use
+    instead of the emulation's own (a kernel's scores); with dump=True the result then
+    also holds p_alt, the code at the other end of the hardware exp2's uncertainty.
 
     Returns dict(out, fallbacks, tiles); with dump=True also s/p_codes/p_scales/m_frozen;
     with ambiguity=True also amb [rows, D]: the bound on how far a kernel output may lie
@@ -238,19 +248,25 @@ def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_ma
     tv = np.zeros(n, np.int32)
     res = dict(out=out, fallbacks=fb, tiles=tv)
     d = None
-    if dump or ambiguity:
-        d = FsaDump(None, None, None, None, None)
+    if dump or ambiguity or s_in is not None:
+        d = FsaDump(None, None, None, None, None, None, None)
+    if s_in is not None:
+        s_in = np.ascontiguousarray(s_in, np.float32)
+        assert s_in.shape == (n, Skp)
+        d.s_in = s_in.ctypes.data
     if dump:
         res.update(s=np.zeros((n, Skp), np.float32), p_codes=np.zeros((n, Skp), np.uint8),
                    p_scales=np.zeros((n, Skp // 32), np.uint8), m_frozen=np.zeros((n, ntiles), np.float32))
         d.s, d.p_codes, d.p_scales, d.m_frozen = (res["s"].ctypes.data, res["p_codes"].ctypes.data,
                                                   res["p_scales"].ctypes.data, res["m_frozen"].ctypes.data)
+        res["p_alt"] = np.zeros((n, Skp), np.uint8)
+        d.p_alt = res["p_alt"].ctypes.data
     if ambiguity:
         res["amb"] = np.zeros((n, D), np.float64)
         d.amb = res["amb"].ctypes.data
     g = _geom(B, H, Hkv, Sq, Sk, D, causal)
     ops = mx.struct()
-    opts = FsaOpts(float(delta), int(mufu_mask) & 0xFFFFFFFF, int(beta), float(s_perturb))
+    opts = FsaOpts(float(delta), int(mufu_mask) & 0xFFFFFFFF, float(beta), float(efq_a), float(phi), float(s_perturb))
     lib().orc_fsa_emulate(ctypes.byref(ops), ctypes.byref(g), ctypes.c_float(scale), ctypes.c_int(fmt_p),
                           ctypes.byref(opts), _p(rows), ctypes.c_int64(n), _p(out), _p(fb), _p(tv),
                           ctypes.byref(d) if d is not None else None, ctypes.c_int(nthreads or nthreads_default()))

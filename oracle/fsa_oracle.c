@@ -487,7 +487,12 @@ float orc_exp2_poly(float r) {
 /*     E = clamp(floor(tmax) - emax, -127, 127); bE = fp32(M + E);               */
 /*     r_j = fmaf(s_j, c, -bE)  (residual: shifted log2 score minus E)           */
 /*     exp path:  code = encode_fmt(exp2approx(r_j))                             */
-/*     EFQ path:  code = clamp(round_half_even(2 r_j + beta), 0, 7)  (E2M1)      */
+/*     EFQ path:  the shift and the affine rule y = a r_j + b are one fused      */
+/*                multiply-add on the raw score (the fold of [FSA-digest]        */
+/*                summary): y = fmaf(s_j, A, Bk), A = fp32(a c), Bk =            */
+/*                fp32(b - fp32(a bE)); code = clamp(round_half_even(y), 0, 7)    */
+/*                (E2M1); the block exponent takes the reference point phi:      */
+/*                E = clamp(floor(fp32(tmax + phi)) - emax, -127, 127).           */
 /*     scale byte = E + 127; a block with no visible key: codes 0, scale 0x00    */
 /*  5. O_acc += sum p~_j v_hat_j, l += sum p~_j with p~_j = dec(code) 2^E (fp64) */
 /*  6. O = O_acc / l (0 if l == 0)                                               */
@@ -499,7 +504,9 @@ float orc_exp2_poly(float r) {
 typedef struct {
   float delta;        /* fallback margin, log2 units: fall back when x > M + delta */
   uint32_t mufu_mask; /* per position in a 32-block: 1 = hardware exp2 model */
-  int beta;           /* EFQ affine offset (default 2) */
+  float beta;         /* EFQ affine offset b (default 2) */
+  float efq_a;        /* EFQ affine slope a (default 2) */
+  float phi;          /* reference point of the P block scale: E = floor(tmax + phi) - emax (default 0) */
   double s_perturb;   /* test knob: raw scores are fp32(dot * (1 + s_perturb)); 0 normally */
 } orc_fsa_opts;
 
@@ -509,6 +516,10 @@ typedef struct {      /* optional per-row dumps, NULL to skip */
   uint8_t* p_scales;  /* [nrows][Skp/32] P scale bytes */
   float* m_frozen;    /* [nrows][ntiles] M after the tile's max step (NaN if skipped) */
   double* amb;        /* [nrows][D] bound on |O_kernel - O| from undetermined decisions (below) */
+  const float* s_in;  /* optional input [nrows][Skp]: raw scores to use instead of step 1's
+                         (a kernel's own scores, so that steps 2-6 can be checked given them) */
+  uint8_t* p_alt;     /* [nrows][Skp] the code at the other end of the exp2 uncertainty
+                         (AMB_X) for hardware-exp2 positions; equal to p_codes elsewhere */
 } orc_fsa_dump;
 
 /* Decisions the kernel takes in fp32 that this emulation cannot reproduce bit for
@@ -546,6 +557,8 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
   const int efq = fmt_p == 3;
   const int efmt = efq ? 2 : fmt_p;
   const int emax = orc_emax(efmt);
+  const float a_c = opt->efq_a * c;               /* EFQ: fp32(a c) */
+  const float phi = efq ? opt->phi : 0.0f;        /* the exp path keeps the OCP scale rule */
   float pc[4];
   orc_exp2_poly_coeffs(pc);
   int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nrows + 1));
@@ -568,6 +581,7 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
       if (dump && dump->m_frozen) for (int t = 0; t < ntiles; ++t) dump->m_frozen[n * ntiles + t] = NAN;
       if (dump && dump->s) for (int64_t j = 0; j < Skp; ++j) dump->s[n * Skp + j] = -INFINITY;
       if (dump && dump->p_codes) memset(dump->p_codes + n * Skp, 0, (size_t)Skp);
+      if (dump && dump->p_alt) memset(dump->p_alt + n * Skp, 0, (size_t)Skp);
       if (dump && dump->p_scales) memset(dump->p_scales + n * (Skp / 32), 0, (size_t)(Skp / 32));
       if (nk > 0) {
         double qh[256];
@@ -597,13 +611,17 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
               acc += blk;
               aabs += fabs(blk);
             }
-            s[j - j0] = (float)(acc * (1.0 + opt->s_perturb));
-            ds[j - j0] = AMB_S * aabs + (opt->s_perturb != 0.0 ? fabs((double)s[j - j0] * opt->s_perturb) : 0.0);
+            s[j - j0] = (dump && dump->s_in) ? dump->s_in[n * Skp + j] : (float)(acc * (1.0 + opt->s_perturb));
+            /* given scores (a kernel's own) carry no score uncertainty */
+            ds[j - j0] = (dump && dump->s_in) ? 0.0
+                         : AMB_S * aabs + (opt->s_perturb != 0.0 ? fabs((double)s[j - j0] * opt->s_perturb) : 0.0);
             if (s[j - j0] > mx) { mx = s[j - j0]; jmx = j; }
           }
           float x = mx * c;
-          /* uncertainty of x (fp32 product of an uncertain score) */
-          const double dx = (double)c * ds[jmx - j0] + 1.2e-7 * fabs((double)x);
+          /* uncertainty of x (fp32 product of an uncertain score); none when the scores
+             are given: every later fp32 step is then the kernel's own, bit for bit */
+          const double rt = (dump && dump->s_in) ? 0.0 : 1.2e-7;
+          const double dx = (double)c * ds[jmx - j0] + rt * fabs((double)x);
           if (!M_set) {
             M = x;
             M_set = 1;
@@ -611,7 +629,7 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
             jM = jmx;
           } else {
             const double thr = (double)(M + opt->delta);
-            if (A && fabs((double)x - thr) <= dx + dM + 1.2e-7 * fabs(thr)) undetermined = 1;
+            if (A && fabs((double)x - thr) <= dx + dM + rt * fabs(thr) && rt > 0.0) undetermined = 1;
             if (x > M + opt->delta) {
               float Mn = x;
               double alpha = exp2((double)(M - Mn));
@@ -636,10 +654,11 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
             float smax = -INFINITY;
             for (int j = jb; j < je; ++j) if (s[j - j0] > smax) smax = s[j - j0];
             float tmax = smax * c - M;       /* fp32(fp32(smax*c) - M): 0 in the block holding M */
-            int E = (int)floorf(tmax) - emax;
+            int E = (int)floorf(tmax + phi) - emax;
             if (E < -127) E = -127;
             if (E > 127) E = 127;
             float bE = M + (float)E;
+            float Bk = opt->beta - opt->efq_a * bE;   /* EFQ: fp32(b - fp32(a bE)) */
             double sc = ldexp(1.0, E);
             int blk_undet = 0;
             if (A && smax != -INFINITY) {
@@ -648,8 +667,9 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
               /* the block holding the score that set M has tmax = 0 exactly on both sides */
               if (jM >= jb && jM < je && s[jM - j0] == smax) jsm = -1;
               if (jsm >= 0) {
-                const double dt = (double)c * ds[jsm - j0] + dM + 1.2e-7 * (fabs((double)(smax * c)) + fabs((double)M));
-                const int Elo = (int)floor((double)tmax - dt), Ehi = (int)floor((double)tmax + dt);
+                const double dt = (double)c * ds[jsm - j0] + dM + rt * (fabs((double)(smax * c)) + fabs((double)M));
+                const double tp = (double)(tmax + phi);
+                const int Elo = (int)floor(tp - dt), Ehi = (int)floor(tp + dt);
                 if (Elo != Ehi && Ehi - emax > -127 && Elo - emax < 127) blk_undet = 1;
               }
             }
@@ -657,15 +677,24 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
               float r = fmaf(s[j - j0], c, -bE);
               uint32_t code;
               int hw = (opt->mufu_mask >> (j % 32)) & 1;
+              uint32_t alt;
               if (efq) {
-                double y = 2.0 * (double)r + (double)opt->beta;   /* exact */
-                double kk = nearbyint(y);                         /* ties to even */
+                float y = fmaf(s[j - j0], a_c, Bk);                 /* one rounding to fp32 */
+                double kk = nearbyint((double)y);                 /* ties to even */
                 if (!(kk > 0.0)) kk = 0.0;
                 if (kk > 7.0) kk = 7.0;
                 code = (uint32_t)kk;
+                alt = code;
               } else {
                 code = orc_encode(efmt, (double)exp2_model(r, hw, pc));
+                alt = code;
+                if (hw && dump && dump->p_alt) {
+                  const uint32_t lo = orc_encode(efmt, exp2((double)r) * (1.0 - AMB_X));
+                  const uint32_t hi = orc_encode(efmt, exp2((double)r) * (1.0 + AMB_X));
+                  alt = code == lo ? hi : lo;
+                }
               }
+              if (dump && dump->p_alt) dump->p_alt[n * Skp + j] = (uint8_t)alt;
               pt[j - j0] = orc_decode(efmt, code) * sc;
               if (A && s[j - j0] != -INFINITY) {
                 double dp = 0.0;
@@ -673,11 +702,13 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
                   /* requantised one exponent step finer or coarser */
                   dp = 0.25 * pt[j - j0] + orc_decode(efmt, 1) * sc * 2.0;
                 } else {
-                  const double dr = (double)c * ds[j - j0] + dM + 1.2e-7 * (fabs((double)s[j - j0] * c) + fabs((double)bE));
+                  const double dr = (double)c * ds[j - j0] + dM + rt * (fabs((double)s[j - j0] * c) + fabs((double)bE));
                   const double rlo = (double)r - dr, rhi = (double)r + dr;
                   uint32_t clo, chi;
                   if (efq) {
-                    double klo = nearbyint(2.0 * rlo + opt->beta), khi = nearbyint(2.0 * rhi + opt->beta);
+                    const double dy = (double)opt->efq_a * dr;
+                    const double y = (double)fmaf(s[j - j0], a_c, Bk);
+                    double klo = nearbyint(y - dy), khi = nearbyint(y + dy);
                     klo = klo < 0.0 ? 0.0 : (klo > 7.0 ? 7.0 : klo);
                     khi = khi < 0.0 ? 0.0 : (khi > 7.0 ? 7.0 : khi);
                     clo = (uint32_t)klo; chi = (uint32_t)khi;
@@ -685,8 +716,9 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
                     clo = orc_encode(efmt, exp2(rlo) * (1.0 - AMB_X));
                     chi = orc_encode(efmt, exp2(rhi) * (1.0 + AMB_X));
                   } else {
-                    clo = orc_encode(efmt, (double)exp2_model((float)rlo, 0, pc) * (1.0 - 1e-7));
-                    chi = orc_encode(efmt, (double)exp2_model((float)rhi, 0, pc) * (1.0 + 1e-7));
+                    const double rp = rt > 0.0 ? 1e-7 : 0.0;   /* the cubic is bit-exact given the scores */
+                    clo = orc_encode(efmt, (double)exp2_model((float)rlo, 0, pc) * (1.0 - rp));
+                    chi = orc_encode(efmt, (double)exp2_model((float)rhi, 0, pc) * (1.0 + rp));
                   }
                   if (clo != chi) dp = fabs(orc_decode(efmt, chi) - orc_decode(efmt, clo)) * sc;
                 }

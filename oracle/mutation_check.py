@@ -48,11 +48,11 @@ M = [
  ("emu no margin", "            if (x > M + opt->delta) {", "            if (x > M) {"),
  ("emu fallback keeps l", "              l *= alpha;\n              if (A) {", "              if (A) {"),
  ("emu alpha sign", "double alpha = exp2((double)(M - Mn));", "double alpha = exp2((double)(Mn - M));"),
- ("emu E +1", "            int E = (int)floorf(tmax) - emax;", "            int E = (int)floorf(tmax) - emax + 1;"),
+ ("emu E +1", "            int E = (int)floorf(tmax + phi) - emax;", "            int E = (int)floorf(tmax + phi) - emax + 1;"),
  ("emu r without E", "              float r = fmaf(s[j - j0], c, -bE);", "              float r = fmaf(s[j - j0], c, -M);"),
- ("efq no factor 2", "double y = 2.0 * (double)r + (double)opt->beta;   /* exact */", "double y = (double)r + (double)opt->beta;"),
+ ("efq slope from c only", "  const float a_c = opt->efq_a * c;               /* EFQ: fp32(a c) */", "  const float a_c = c;"),
  ("efq clamp 6", "                if (kk > 7.0) kk = 7.0;\n                code", "                if (kk > 6.0) kk = 6.0;\n                code"),
- ("efq floor", "double kk = nearbyint(y);                         /* ties to even */", "double kk = floor(y);"),
+ ("efq floor", "double kk = nearbyint((double)y);                 /* ties to even */", "double kk = floor((double)y);"),
  ("emu pt scale", "              pt[j - j0] = orc_decode(efmt, code) * sc;", "              pt[j - j0] = orc_decode(efmt, code) * sc * 2.0;"),
  ("emu mask inverted", "int hw = (opt->mufu_mask >> (j % 32)) & 1;", "int hw = !((opt->mufu_mask >> (j % 32)) & 1);"),
  ("emu tiles of 64", "  const int D = g->D, BN = 128;\n  const int64_t Skp", "  const int D = g->D, BN = 64;\n  const int64_t Skp"),
@@ -73,11 +73,17 @@ M = [
  ("ambiguity too small", "#define AMB_S 4.76837158203125e-07   /* 2^-21 */", "#define AMB_S 1e-9"),
  ("tiles not counted", "          ++tv;\n", ""),
  ("fallbacks not counted", "              ++fb;\n", ""),
- ("efq beta sign", "double y = 2.0 * (double)r + (double)opt->beta;", "double y = 2.0 * (double)r - (double)opt->beta;"),
+ ("efq beta sign", "float Bk = opt->beta - opt->efq_a * bE;", "float Bk = -opt->beta - opt->efq_a * bE;"),
+ ("efq offset without E", "float Bk = opt->beta - opt->efq_a * bE;", "float Bk = opt->beta - opt->efq_a * M;"),
+ ("efq phi ignored", "  const float phi = efq ? opt->phi : 0.0f;", "  const float phi = 0.0f;"),
+ ("phi on the exp path", "  const float phi = efq ? opt->phi : 0.0f;", "  const float phi = opt->phi;"),
+ ("efq codes not clamped below", "                if (!(kk > 0.0)) kk = 0.0;", ""),
  ("bf16 rescale keeps l", "            l *= alpha;\n            M = x;", "            M = x;"),
  ("exact no max shift", "        if (s[j] > m) m = s[j];\n      }\n      double l = 0.0;",
   "        m = 0.0;\n      }\n      double l = 0.0;"),
- ("amb ignores fallback test", "<= dx + dM + 1.2e-7 * fabs(thr)) undetermined = 1;", "< 0.0) undetermined = 1;"),
+ ("amb ignores fallback test", "<= dx + dM + rt * fabs(thr) && rt > 0.0) undetermined = 1;", "< 0.0) undetermined = 1;"),
+ ("given scores ignored", "            s[j - j0] = (dump && dump->s_in) ? dump->s_in[n * Skp + j] : (float)(acc * (1.0 + opt->s_perturb));",
+  "            s[j - j0] = (float)(acc * (1.0 + opt->s_perturb));"),
  ("amb alpha exact", "const double ra = 0.6931471805599453 * (dM + dx) + AMB_X;", "const double ra = 0.0;"),
  ("amb block exponent", "if (Elo != Ehi && Ehi - emax > -127 && Elo - emax < 127) blk_undet = 1;", "blk_undet = 0;"),
  ("amb block step", "dp = 0.25 * pt[j - j0] + orc_decode(efmt, 1) * sc * 2.0;", "dp = 0.0;"),

@@ -185,20 +185,24 @@ def test_emulate_with_exact_exp_equals_floor_on_one_tile():
         assert not np.array_equal(po, fl), fq
 
 
-def test_emulate_efq_codes_span_the_e2m1_range():
-    """The EFQ rule maps onto all nonnegative E2M1 codes: over a few random rows every
-    code 0..7 occurs, the block holding the frozen maximum gets exactly code 6
-    (r = 2, 2r + beta = 6), and no code exceeds 7."""
+@pytest.mark.parametrize("a,b,phi,code_of_max", [(oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI, 7), (2.0, 2.0, 0.0, 6),
+                                                 (2.0, 1.0, 0.0, 5), (1.5, 3.0, 0.75, 6)])
+def test_emulate_efq_codes_span_the_e2m1_range(a, b, phi, code_of_max):
+    """The EFQ rule maps onto the nonnegative E2M1 codes: over a few random rows every
+    code from 0 up to the code of the row maximum occurs and none exceeds 7.  The
+    score that sets the frozen maximum has t = 0 exactly, so its block exponent is
+    E = floor(phi) - 2 = -2, its residual 2 and its code rne(2a + b) clamped to 7:
+    rne(6.8125) = 7, rne(6) = 6, rne(5) = 5, rne(6) = 6 for the four rules."""
     B, H, S, D = 1, 1, 512, 64
     q, k, v = rnd((B, H, S, D), 1, 1.5), rnd((B, H, S, D), 2), rnd((B, H, S, D), 3)
     mx = oracle.MxInputs.from_bf16(q, k, v, 2, 2)
     rows = np.arange(0, S, 7, dtype=np.int64)
-    res = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=8.0, dump=True)
+    res = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=8.0, dump=True, efq_a=a, beta=b, phi=phi)
     pc = res["p_codes"]
-    assert set(np.unique(pc)) == set(range(8))
+    assert set(range(code_of_max + 1)) <= set(np.unique(pc)) <= set(range(8))
     for n in range(len(rows)):
         jmax = int(np.argmax(res["s"][n, :128]))     # the first tile's maximum sets M
-        assert pc[n, jmax] == 6
+        assert pc[n, jmax] == code_of_max
 
 
 # --------------------------------------------------------------------------- exp2 approximation
@@ -299,12 +303,12 @@ def test_emulate_pgen_block_structure():
             assert 0x78 <= c <= 0x7E
 
 
-@pytest.mark.parametrize("fq,fp,bound", [(0, 0, 1.1), (1, 1, 1.1), (2, 2, 1.1), (2, 3, 2.0)])
+@pytest.mark.parametrize("fq,fp,bound", [(0, 0, 1.1), (1, 1, 1.1), (2, 2, 1.1), (2, 3, 1.1)])
 def test_emulate_error_close_to_floor_on_tiny(fq, fp, bound):
     """The pages' claim (Fused-Softmax brief, abstract): the approximation's extra
     error stays near the floor set by quantising the GEMM operands.  The exp paths
-    meet 1.1x; the EFQ direct-code reading costs more (measured ~1.5x) because its
-    log-domain rounding zeroes values below ~0.59 2^E that E2M1 rounding keeps."""
+    meet 1.1x; so does the EFQ rule with the constants of oracle/efq_scan.py on this
+    case (1.0996x; the first reading a = b = 2, phi = 0 gave 1.51x)."""
     from workloads import WORKLOADS, generate, sample_rows
     w = WORKLOADS["tiny"]
     q, k, v = generate(w)
@@ -435,3 +439,71 @@ def test_emulate_ambiguity_bound_covers_score_perturbations(fq, fp, mufu):
         moved += int(np.sum(diff.max(axis=1) > 1e-12))
         assert np.all(diff <= amb * (1 + 1e-9) + 1e-12), f"eps {eps}: {np.max(diff - amb):.3e}"
     assert moved > 0
+
+
+# --------------------------------------------------------------------------- EFQ block scale and given scores
+@pytest.mark.parametrize("a,b,phi", [(oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI), (1.5, 3.0, 0.75), (2.0, 2.0, 0.0)])
+def test_emulate_efq_block_max_residual_window(a, b, phi):
+    """E = floor(tmax + phi) - 2 puts every block's largest residual t - E in
+    [2 - phi, 3 - phi), so the block maximum's code lies between the rule's codes at the
+    two ends: rne(a (2 - phi) + b) .. rne(a (3 - phi) + b), clamped to 7; with phi > 0 the
+    upper end is never reached by the OCP window [2, 3)."""
+    B, H, S, D = 1, 1, 512, 64
+    q, k, v = rnd((B, H, S, D), 11, 1.5), rnd((B, H, S, D), 12), rnd((B, H, S, D), 13)
+    mx = oracle.MxInputs.from_bf16(q, k, v, 2, 2)
+    rows = np.arange(0, S, 5, dtype=np.int64)
+    res = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=8.0, dump=True, efq_a=a, beta=b, phi=phi)
+    lo = min(7, int(np.round(a * (2 - phi) + b)))
+    hi = min(7, int(np.round(a * (3 - phi) + b)))
+    seen = set()
+    for n in range(len(rows)):
+        for blk in range(S // 32):
+            s = res["s"][n, 32 * blk:32 * blk + 32]
+            c = int(res["p_codes"][n, 32 * blk + int(np.argmax(s))])
+            assert lo <= c <= hi, (n, blk, c, lo, hi)
+            seen.add(c)
+    assert len(seen) >= 2
+
+
+def test_emulate_phi_only_moves_efq_scales():
+    """The reference point phi belongs to the EFQ rule: the exp-then-round paths keep
+    the OCP block scale and give identical results for any phi; EFQ results change."""
+    B, H, S, D = 1, 2, 300, 64
+    q, k, v = rnd((B, H, S, D), 21), rnd((B, H, S, D), 22), rnd((B, H, S, D), 23)
+    rows = allrows(B, H, S)
+    for fq, fp in ((0, 0), (1, 1), (2, 2)):
+        mx = oracle.MxInputs.from_bf16(q, k, v, fq, fp)
+        r0 = oracle.fsa_emulate(mx, S, False, 0.125, fp, rows, phi=0.0, dump=True)
+        r1 = oracle.fsa_emulate(mx, S, False, 0.125, fp, rows, phi=0.75, dump=True)
+        assert np.array_equal(r0["p_codes"], r1["p_codes"]) and np.array_equal(r0["out"], r1["out"])
+    mx = oracle.MxInputs.from_bf16(q, k, v, 2, 2)
+    r0 = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, phi=0.0, dump=True)
+    r1 = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, phi=0.75, dump=True)
+    assert not np.array_equal(r0["p_scales"], r1["p_scales"])
+
+
+def test_emulate_given_scores_drive_the_algorithm():
+    """s_in replaces the emulation's own scores: given its own scores back, everything is
+    unchanged (and no score uncertainty is left: for EFQ the ambiguity bound is zero on
+    rows without a fallback, and the exp2 of a fallback's factor elsewhere);
+    given a raised score in a late tile, that row falls back and its M follows it."""
+    B, H, S, D = 1, 1, 384, 64
+    q, k, v = rnd((B, H, S, D), 31), rnd((B, H, S, D), 32), rnd((B, H, S, D), 33)
+    rows = allrows(B, H, S)
+    mx = oracle.MxInputs.from_bf16(q, k, v, 2, 2)
+    base = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=0.0, dump=True)
+    same = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=0.0, dump=True, s_in=base["s"], ambiguity=True)
+    for key in ("out", "p_codes", "p_scales", "fallbacks"):
+        assert np.array_equal(base[key], same[key]), key
+    # what is left is the hardware exp2 of a fallback's factor (2^-21 relative)
+    nofb = same["fallbacks"] == 0
+    assert nofb.any() and not same["amb"][nofb].any()
+    assert np.all(same["amb"] <= 2.0 ** -20 * np.abs(same["out"]).max())
+    s2 = base["s"].copy()
+    row, key = 7, 300
+    s2[row, key] = base["s"][row].max() + 40.0
+    moved = oracle.fsa_emulate(mx, S, False, 0.125, 3, rows, delta=0.0, dump=True, s_in=s2)
+    c = np.float32(np.float32(0.125) * np.float32(1.4426950408889634))
+    assert moved["fallbacks"][row] == base["fallbacks"][row] + (0 if base["m_frozen"][row, 2] >= np.float32(s2[row, key] * c) else 1)
+    assert moved["m_frozen"][row, 2] == np.float32(s2[row, key] * c)
+    assert moved["p_codes"][row, key] == min(7, int(np.round(oracle.EFQ_A * 2 + oracle.EFQ_B)))

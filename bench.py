@@ -32,13 +32,21 @@ sys.path.insert(0, ROOT)
 
 from workloads import WORKLOADS, Workload, generate  # noqa: E402
 
-DEFAULT_WORKLOAD = "prefill"
+# the largest single-GPU workload: long-context causal attention at 128K keys, MXFP4
+# QK^T with EFQ probability codes
+DEFAULT_WORKLOAD = "long_efq_128k"
+# further workloads reported in the same line (kernel throughput, fraction of the
+# measured peak, speedup over the BF16 kernel, fallback rate)
+EXTRA_WORKLOADS = ["long_fp8_16k", "long_fp8_128k", "long_efq_16k", "video_dit", "adversarial"]
 FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
-# nominal dense ratio of each block-scaled kind to BF16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s)
-KIND_RATIO = {"E4M3": 2.0, "E2M3": 2.0, "E2M1": 6.0, "E2M1_EFQ": 6.0}
-# DRAM bytes (read + write) per attention launch from an ncu capture of the current
-# kernel build, by workload (profiles/fsa_attn_e4m3_*.md); absent: not captured
-TRAFFIC = {"prefill": 26_028_288 + 14_892_032, "long_fp8_16k": 105_790_976 + 212_229_120}
+# tensor-core kind of each operand format: 0 kind::f16, 1 kind::mxf8f6f4, 2 kind::mxf4
+KIND = {"E4M3": 1, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 2}
+# nominal dense ratio of each kind to BF16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s): used
+# only when the probe could not run
+KIND_RATIO = {0: 1.0, 1: 2.0, 2: 6.0}
+# DRAM bytes (read + write) of one attention launch of the current kernel build, from
+# an ncu capture, by workload; absent: not captured for this build
+TRAFFIC = {}
 
 
 def metric_name():
@@ -54,11 +62,56 @@ def peaks():
     return 1900.0, 1700.0, "fallback"
 
 
-def peak_for(w: Workload):
-    """Dense block-scaled peak for the workload's formats (harmonic mix of the QK and PV kinds)."""
+def peak_for(w: Workload, measured=None):
+    """Dense peak for the workload's formats: the harmonic mix of its QK^T and PV kinds
+    (each GEMM is half the FLOPs).  measured: {kind: TFLOP/s} from the probe; else the
+    MEASURED_PEAKS bf16 figure times the nominal ratio."""
     bf16, _, src = peaks()
-    pq, pp = bf16 * KIND_RATIO[w.fmt_qk], bf16 * KIND_RATIO[w.fmt_pv]
+    kq, kp = KIND[w.fmt_qk], KIND[w.fmt_pv]
+    if measured and kq in measured and kp in measured:
+        pq, pp, src = measured[kq], measured[kp], "measured on this GPU by the tcgen05 probe (fsa_mma_peak)"
+    else:
+        pq, pp = bf16 * KIND_RATIO[kq], bf16 * KIND_RATIO[kp]
+        src = f"{src} bf16 burst x nominal block-scaled/bf16 ratio"
     return 1.0 / (0.5 / pq + 0.5 / pp), src
+
+
+def measure_mma_peaks(dev, seconds=0.03, sustained_s=0.0):
+    """Dense tensor-core TFLOP/s per kind (0 bf16, 1 MXFP8, 2 MXFP4) from the library's
+    probe: one CTA per SM, operands resident on chip, timed with CUDA events.  Burst: one
+    launch of about `seconds`; sustained: back-to-back launches for `sustained_s`."""
+    import torch
+    import softmax_mx_block_gb300 as fsa
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = {}
+    for kind in (0, 1, 2):
+        fsa.fsa_mma_peak(kind, n_sm, 2000, status)           # warm-up and a first rate
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        f = fsa.fsa_mma_peak(kind, n_sm, 20000, status)
+        e1.record()
+        torch.cuda.synchronize()
+        rate = f / (e0.elapsed_time(e1) * 1e-3)
+        iters = max(1000, int(seconds * rate / (f / 20000)))
+        best = 0.0
+        for _ in range(3):
+            e0.record()
+            f = fsa.fsa_mma_peak(kind, n_sm, iters, status)
+            e1.record()
+            torch.cuda.synchronize()
+            best = max(best, f / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        out[kind] = {"burst": best}
+        if sustained_s > 0:
+            n = max(1, int(sustained_s / seconds))
+            e0.record()
+            tot = sum(fsa.fsa_mma_peak(kind, n_sm, iters, status) for _ in range(n))
+            e1.record()
+            torch.cuda.synchronize()
+            out[kind]["sustained"] = tot / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    if int(status.item()) != 0:
+        raise RuntimeError("tensor-core probe timed out")
+    return out
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -137,8 +190,6 @@ def run_gpu(args, w: Workload, world):
     from softmax_mx_block_gb300._binding import empty_mx
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    fsa.load()
     layers = [w.layer(l) for l in range(w.layers)] if w.layers > 1 else [w]
     host, inputs, bufs = [], [], []
     for wl in layers:
@@ -267,6 +318,70 @@ def run_gpu(args, w: Workload, world):
                 launches=args.steps * 2 * len(layers), bf16_ms=statistics.mean(bf_ms))
 
 
+def time_workload(name, dev, steps, exp_mode, measured_peaks):
+    """Attention-kernel throughput of one further workload (inputs resident, L2 flushed
+    between launches), the BF16 kernel on the same inputs, and the fallback rate at the
+    library's default margin (and at margin 0 for the adversarial workload)."""
+    import torch
+    import softmax_mx_block_gb300 as fsa
+    w = WORKLOADS[name]
+    layers = [w.layer(l) for l in range(w.layers)] if w.layers > 1 else [w]
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    attn_ms, bf_ms = [], []
+    st8, st0 = fsa.new_stats(dev), fsa.new_stats(dev)
+    for wl in layers:
+        q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in generate(wl))
+        fq, fp = FMT[wl.fmt_qk], FMT[wl.fmt_pv]
+        mq, mk, mv = fsa.fsa_mx_quantize_qkv(q, k, v, fq, 2 if fp == 3 else fp)
+        out = torch.empty((wl.B, wl.H, wl.Sq, wl.D), dtype=torch.float32, device=dev)
+        call = dict(causal=wl.causal, scale=wl.scale, fmt_qk=fq, fmt_pv=fp, exp_mode=exp_mode)
+        n = steps if len(layers) == 1 else 2
+        for it in range(3 + n):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fsa.fsa_attention_fwd(mq, mk, mv, out, stats=st8 if it == 3 else None, **call)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= 3:
+                attn_ms.append(e0.elapsed_time(e1))
+        if wl.kind == "planted":
+            fsa.fsa_attention_fwd(mq, mk, mv, out, stats=st0, delta=0.0, **call)
+        del mq, mk, mv
+        vt = fsa.fsa_bf16_transpose_v(v)
+        for it in range(2 + max(1, n // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fsa.fsa_attention_fwd_bf16(q, k, vt, out, causal=wl.causal, scale=wl.scale)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= 2:
+                bf_ms.append(e0.elapsed_time(e1))
+        del q, k, v, vt, out
+    torch.cuda.synchronize()
+    r8, r0 = fsa.read_stats(st8), fsa.read_stats(st0)
+    # per layer: the mean launch time; per workload: FLOPs of all layers over their summed means
+    per_layer = len(attn_ms) // len(layers)
+    a_ms = sum(statistics.mean(attn_ms[i * per_layer:(i + 1) * per_layer]) for i in range(len(layers)))
+    per_layer_bf = len(bf_ms) // len(layers)
+    b_ms = sum(statistics.mean(bf_ms[i * per_layer_bf:(i + 1) * per_layer_bf]) for i in range(len(layers)))
+    tf = w.flops / (a_ms * 1e-3) / 1e12
+    peak, _ = peak_for(w if w.layers == 1 else layers[0], measured_peaks)
+    if w.layers > 1:   # alternating kinds: the harmonic mix over the layers
+        peak = len(layers) / sum(1.0 / peak_for(wl, measured_peaks)[0] for wl in layers)
+    res = {"tflops": tf, "frac_of_peak": tf / peak, "peak_tflops": peak,
+           "bf16_tflops": w.flops / (b_ms * 1e-3) / 1e12, "speedup_vs_bf16": b_ms / a_ms,
+           "fallback_rate": r8["fallback_events"] / r8["row_tiles"] if r8["row_tiles"] else None,
+           "delta": 8.0}
+    if w.kind == "planted":
+        res["fallback_rate_delta0"] = r0["fallback_events"] / r0["row_tiles"] if r0["row_tiles"] else None
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 # which key positions of a 32-key block the oracle takes through ex2 (bit set) for
 # each exp mode: 0 the cubic everywhere, 1 ex2 everywhere, 2 the cubic at 4k+3
@@ -315,6 +430,8 @@ def main():
     ap.add_argument("--impl", default="fsa", choices=["fsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the quantisation eagerly (no CUDA graph)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the further workloads of the line")
+    ap.add_argument("--no-peak-probe", action="store_true", help="skip the tensor-core probe (nominal ratios)")
     ap.add_argument("--exp-mode", type=int, default=1, choices=[0, 1, 2],
                     help="0 cubic, 1 ex2.approx (default, the library's), 2 split 3:1")
     args = ap.parse_args()
@@ -343,6 +460,17 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
+    import torch
+    import softmax_mx_block_gb300 as fsa
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    fsa.load()
+    measured = None
+    peak_info = None
+    if not args.no_peak_probe:
+        mp = measure_mma_peaks(dev, sustained_s=0.5)
+        measured = {k: v["burst"] for k, v in mp.items()}
+        peak_info = {{0: "bf16", 1: "mxf8f6f4_e4m3", 2: "mxf4_e2m1"}[k]: v for k, v in mp.items()}
     r = run_gpu(args, w, world)
     if world > 1:
         import torch
@@ -352,7 +480,9 @@ def main():
     config["launch"] = r["launch_mode"]
     value = flops_per_step * world / (r["ms"] * 1e-3) / 1e12
     attn_tflops = flops_per_step / w.layers / (r["attn_ms"] * 1e-3) / 1e12
-    peak, src = peak_for(w)
+    peak, src = peak_for(w, measured)
+    if w.layers > 1:
+        peak = w.layers / sum(1.0 / peak_for(w.layer(l), measured)[0] for l in range(w.layers))
     rt = r["stats"]["row_tiles"]
     line = {
         "metric": metric_name(), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -367,12 +497,19 @@ def main():
         "fallback_rate": (r["stats"]["fallback_events"] / rt) if rt else None,
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak, "traffic": TRAFFIC.get(w.name),
-                     "peak_source": f"{src} bf16 burst x nominal block-scaled/bf16 ratio"},
+                     "peak_source": src + " (burst; dense M=128 N=128 MMAs, harmonic mix of the QK^T and PV kinds)"},
+        "tensor_peaks_tflops": peak_info,
         "e2e": {"value": flops_per_step * world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if not args.no_extra and world == 1:
+        line["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            if name != w.name:
+                line["workloads"][name] = time_workload(name, torch.device("cuda", 0), min(args.steps, 5),
+                                                        args.exp_mode, measured)
     if not args.no_cpu_baseline and world == 1:
         v, desc, threads = run_oracle_sample(w, budget_s=15.0, exp_mode=args.exp_mode)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}

@@ -127,21 +127,73 @@ typedef enum {
   FSA_EXP_SPLIT = 2   /* key positions 4k+3 (of each 32-key block) the cubic, the others ex2.approx */
 } fsa_exp_mode;
 
+typedef enum {
+  FSA_OUT_F32 = 0,    /* O as fp32 */
+  FSA_OUT_BF16 = 1    /* O as bf16: the fp32 result rounded to nearest even */
+} fsa_out_dtype;
+
+/* Debug dumps of every key tile the kernel processes (a test instrument: the
+ * P~ codes are the method's product, and the EFQ-Softmax page, abstract, defines
+ * them as nonnegative E2M1 codes under exponent-only block scales).  All
+ * pointers are device memory of the caller.  Query row r (r = (b*H + h)*Sq + i)
+ * is dumped to slot row_slot[r] (row_slot NULL: slot r; a negative slot: not
+ * dumped); N is the number of slots, NKT = ceil(Sk/128) key tiles.  Entries of
+ * tiles a query tile does not process are left untouched (callers initialise
+ * them).  The debug instance computes the same outputs as the production kernel,
+ * bit for bit.
+ *   s        : float    [N][NKT*128]  raw fp32 scores of the MMA (masked keys -inf)
+ *   m        : float    [N][NKT]      frozen maximum M used for the tile's P~
+ *   p        : uint32_t [N][NKT][32]  P~ code words as written to tensor memory:
+ *                                     one byte per code (E4M3; E2M3 in the low 6
+ *                                     bits) in words 0..31, or two E2M1 codes per
+ *                                     byte (even key in the low nibble) in words 0..15
+ *   p_scales : uint32_t [N][NKT]      byte b = E8M0 scale of the tile's 32-key block b
+ *   row_slot : int32_t  [B*H*Sq]      optional slot of each query row */
 typedef struct {
-  float    delta;        /* fallback margin in log2 units (default 8): a later tile falls back
-                            only when its maximum exceeds the frozen one by more than delta;
-                            per-block scales make a stale maximum cost no precision */
+  float*    s;
+  float*    m;
+  uint32_t* p;
+  uint32_t* p_scales;
+  const int32_t* row_slot;
+} fsa_debug_dump;
+
+/* The EFQ direct-code rule (EFQ-Softmax page, abstract: an exponent-only block
+ * scale from the local maximum, shifted scores in a normalised residual domain,
+ * codes by a single affine rule; the page prints no constants).  Per 32-key block
+ * with maximum shifted score tmax (log2 units):
+ *     E    = clamp(floor(tmax + efq_phi) - 2, -127, 127)
+ *     code = clamp(rne(efq_a * (t - E) + efq_b), 0, 7)
+ * computed as one fused multiply-add per raw score s (t - E = s*c - (M + E)).
+ * The defaults come from a scan of the rule family against fp64 exact attention
+ * on the long-context workload (the error-floor criterion of the Fused-Softmax
+ * brief, abstract). */
+#define FSA_EFQ_A_DEFAULT   1.6875f
+#define FSA_EFQ_B_DEFAULT   3.5f
+#define FSA_EFQ_PHI_DEFAULT 0.5625f
+
+typedef struct {
+  float    delta;        /* fallback margin in log2 units, >= 0 (default 8): a later tile falls
+                            back only when its maximum exceeds the frozen one by more than
+                            delta; per-block scales make a stale maximum cost no precision.
+                            0 is the literal test "any score exceeds the frozen maximum" */
   int32_t  exp_mode;     /* fsa_exp_mode (default FSA_EXP_MUFU: on sm_103a the hardware exp2
                             issues at twice the rate of earlier parts, and the cubic's
                             extra FMA-pipe instructions cost more than they save) */
-  int32_t  efq_beta;     /* integer offset of the EFQ rule code = rne(2 r + beta) (default 2) */
+  float    efq_a;        /* EFQ slope a (default FSA_EFQ_A_DEFAULT), finite, 0 < a <= 16 */
+  float    efq_b;        /* EFQ offset b (default FSA_EFQ_B_DEFAULT), finite, |b| <= 64 */
+  float    efq_phi;      /* EFQ block-scale reference point (default FSA_EFQ_PHI_DEFAULT), 0 <= phi < 1 */
   uint32_t timeout_ms;   /* limit of each on-chip wait (0: 4000 ms) */
   int32_t* row_fallbacks;/* optional device int32 [B][H][Sq]: fallback count per row */
   int32_t  inject_stall; /* test hook: 1 makes the MMA warp wait on a barrier nobody
                             arrives on, so the bounded wait expires (status TIMEOUT) */
   int32_t  schedule;     /* fsa_schedule (default FSA_SCHED_AUTO); the result does not
                             depend on it: both schedules compute bit-identical outputs */
-  int32_t  reserved[2];
+  int32_t  out_dtype;    /* fsa_out_dtype of `out` (default FSA_OUT_F32) */
+  int32_t  reserved;
+  const fsa_debug_dump* debug;  /* optional (NULL: none): run the debug instance, which
+                            also writes the per-tile dumps; per-query-tile schedule,
+                            formats with fmt_qk == fmt_pv or E2M1 with E2M1_EFQ, exp
+                            modes POLY and MUFU (else FSA_ERR_UNSUPPORTED_FMT) */
 } fsa_opts;
 
 typedef enum {
@@ -157,7 +209,8 @@ typedef enum {
 typedef struct {                      /* device memory, zeroed by the caller */
   unsigned long long fallback_events; /* (row, tile) pairs whose score beat the frozen max */
   unsigned long long row_tiles;       /* (row, tile) pairs with at least one visible key */
-  int32_t status;                     /* FSA_OK or FSA_ERR_TIMEOUT */
+  int32_t status;                     /* FSA_OK or FSA_ERR_TIMEOUT; after TIMEOUT the output
+                                         is undefined */
   int32_t reserved;
 } fsa_stats;
 
@@ -179,9 +232,18 @@ int fsa_attention_fwd(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_
                       int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                       int fmt_qk, int fmt_pv, void* stream);
 
-/* As fsa_attention_fwd with options (NULL: defaults) and device statistics
- * (NULL: none; without stats a wait that times out is not reported). */
-int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, float* out,
+/* As fsa_attention_fwd with options and statistics: the frozen-maximum margin
+ * (the fallback of "Moving softmax to matrix operations...", "Read it as"), the
+ * exp2 path of the exp-then-round formats (its "fast method"), the EFQ rule's
+ * constants (EFQ-Softmax page, abstract), the output dtype (`out` is fp32 or
+ * bf16 [B][H][Sq][D] per opts->out_dtype, 16-byte aligned), the schedule, the
+ * wait limit and the debug dumps.  opts NULL: defaults.  stats: device
+ * fsa_stats (NULL: none; without stats a wait that times out is not reported).
+ * Errors as fsa_attention_fwd, plus FSA_ERR_INVALID_ARG for options out of
+ * range (negative or non-finite delta, exp_mode, EFQ constants, schedule,
+ * out_dtype) and FSA_ERR_UNSUPPORTED_FMT for a debug run of a format pair or
+ * exp mode without a debug instance. */
+int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, void* out,
                          int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                          int fmt_qk, int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream);
 
@@ -198,6 +260,56 @@ int fsa_bf16_transpose_v(const void* v, void* vt, int B, int Hkv, int S, int D, 
 int fsa_attention_fwd_bf16(const void* q, const void* k, const void* vt, float* out,
                            int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                            fsa_stats* stats, void* stream);
+
+/* ------------------------------------------------- hybrid-format layer schedule */
+/* One attention layer of a model that picks its MX formats per layer (the
+ * Fused-Softmax brief, abstract: a hybrid MXFP6/MXFP4 schedule on a video
+ * model).  Fields as the arguments of fsa_attention_fwd_ex; `out` is fp32 or
+ * bf16 per the call's opts->out_dtype; `delta` is this layer's frozen-maximum
+ * margin (>= 0); `stats` optional device fsa_stats of this layer. */
+typedef struct {
+  const fsa_mx_tensor* q;
+  const fsa_mx_tensor* k;
+  const fsa_mx_tensor* v;
+  void*   out;
+  int32_t B, H, Hkv, Sq, Sk, D, causal;
+  float   scale;
+  int32_t fmt_qk, fmt_pv;
+  float   delta;
+  fsa_stats* stats;
+} fsa_layer;
+
+/* Run n_layers layers back to back on `stream`, each with its own formats and
+ * margin and the remaining options of `opts` (NULL: defaults; a debug dump is
+ * refused, the per-row fallback buffer is not used).  Every layer's arguments
+ * are checked before the first launch: on an argument error nothing is
+ * enqueued.  Errors as fsa_attention_fwd_ex. */
+int fsa_attention_fwd_layers(const fsa_layer* layers, int n_layers, const fsa_opts* opts, void* stream);
+
+/* Host-side margin update driven by the fallback counts of a previous run (the
+ * speculative maximum of "Moving softmax to matrix operations...", "Read it
+ * as", falls back when the guess is wrong; a larger margin trades fallbacks for
+ * accumulator headroom).  stats: HOST copies of each layer's fsa_stats; delta:
+ * host array of the layers' margins, updated in place: a layer whose fallback
+ * rate (events / row-tiles) is above target_rate gets delta + step, at most
+ * max_delta; layers without evidence (status not FSA_OK, no row-tiles) keep
+ * theirs.  FSA_ERR_INVALID_ARG for null arrays, step <= 0, a negative target or
+ * maximum, or a delta outside [0, max_delta]. */
+int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, float step, float max_delta,
+                   float* delta);
+
+/* ------------------------------------------------------ tensor-core peak probe */
+/* Measurement instrument (the roofline denominator of the attention kernels; the
+ * Fused-Softmax brief, abstract, quotes its kernels' throughput on the block-
+ * scaled matrix cores).  Launches n_ctas CTAs (one per SM is the intent) that
+ * each issue `iters` iterations of dense M=128, N=128, K=128 products from
+ * shared-memory operand tiles into tensor memory, as 8 kind::f16 bf16 MMAs
+ * (kind 0), 4 kind::mxf8f6f4 E4M3 block-scaled MMAs (kind 1) or 2 kind::mxf4
+ * E2M1 block-scaled MMAs (kind 2).  *flops (host, optional) receives the
+ * launch's 2*M*N*K*iters*n_ctas; time the launch with events on `stream`.
+ * status: optional device int32, set to FSA_ERR_TIMEOUT if the final wait
+ * (2 s) expires.  Errors: FSA_ERR_INVALID_ARG, FSA_ERR_LAUNCH. */
+int fsa_mma_peak(int kind, int n_ctas, long long iters, int32_t* status, double* flops, void* stream);
 
 const char* fsa_status_string(int status);
 int fsa_version(void);

@@ -36,12 +36,34 @@ class fsa_mx_tensor(ctypes.Structure):
                 ("D", ctypes.c_int32)]
 
 
+class fsa_debug_dump(ctypes.Structure):
+    _fields_ = [("s", ctypes.c_void_p), ("m", ctypes.c_void_p), ("p", ctypes.c_void_p), ("p_scales", ctypes.c_void_p),
+                ("row_slot", ctypes.c_void_p)]
+
+
 class fsa_opts(ctypes.Structure):
-    _fields_ = [("delta", ctypes.c_float), ("exp_mode", ctypes.c_int32), ("efq_beta", ctypes.c_int32),
-                ("timeout_ms", ctypes.c_uint32), ("row_fallbacks", ctypes.c_void_p), ("inject_stall", ctypes.c_int32),
-                ("schedule", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
+    _fields_ = [("delta", ctypes.c_float), ("exp_mode", ctypes.c_int32), ("efq_a", ctypes.c_float),
+                ("efq_b", ctypes.c_float), ("efq_phi", ctypes.c_float), ("timeout_ms", ctypes.c_uint32),
+                ("row_fallbacks", ctypes.c_void_p), ("inject_stall", ctypes.c_int32), ("schedule", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("debug", ctypes.POINTER(fsa_debug_dump))]
 
 
+class fsa_stats(ctypes.Structure):
+    _fields_ = [("fallback_events", ctypes.c_uint64), ("row_tiles", ctypes.c_uint64), ("status", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class fsa_layer(ctypes.Structure):
+    _fields_ = [("q", ctypes.POINTER(fsa_mx_tensor)), ("k", ctypes.POINTER(fsa_mx_tensor)),
+                ("v", ctypes.POINTER(fsa_mx_tensor)), ("out", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("Sq", ctypes.c_int32),
+                ("Sk", ctypes.c_int32), ("D", ctypes.c_int32), ("causal", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("fmt_qk", ctypes.c_int32), ("fmt_pv", ctypes.c_int32), ("delta", ctypes.c_float),
+                ("stats", ctypes.c_void_p)]
+
+
+FSA_OUT_F32, FSA_OUT_BF16 = 0, 1
 STATS_BYTES = 24      # fsa_stats: u64 fallback_events, u64 row_tiles, i32 status, i32 reserved
 
 _lib = None
@@ -69,6 +91,9 @@ def load(build_if_missing: bool = True):
             L.fsa_attention_fwd.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + [vp, i, i, i, i, i, i, i, f, i, i, vp]
             L.fsa_attention_fwd_ex.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + \
                 [vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, vp]
+            L.fsa_attention_fwd_layers.argtypes = [ctypes.POINTER(fsa_layer), i, ctypes.POINTER(fsa_opts), vp]
+            L.fsa_tune_delta.argtypes = [ctypes.POINTER(fsa_stats), i, f, f, f, ctypes.POINTER(ctypes.c_float)]
+            L.fsa_mma_peak.argtypes = [i, i, ctypes.c_longlong, vp, ctypes.POINTER(ctypes.c_double), vp]
             L.fsa_bf16_transpose_v.argtypes = [vp, vp, i, i, i, i, vp]
             L.fsa_attention_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp]
             L.fsa_default_opts.argtypes = [ctypes.POINTER(fsa_opts)]
@@ -76,7 +101,8 @@ def load(build_if_missing: bool = True):
             L.fsa_status_string.argtypes = [i]
             L.fsa_status_string.restype = ctypes.c_char_p
             for n in ("fsa_mx_sizes", "fsa_mx_quantize", "fsa_mx_quantize_qkv", "fsa_attention_fwd",
-                      "fsa_attention_fwd_ex", "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version"):
+                      "fsa_attention_fwd_ex", "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version",
+                      "fsa_attention_fwd_layers", "fsa_tune_delta", "fsa_mma_peak"):
                 getattr(L, n).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -219,20 +245,78 @@ def read_stats(stats: torch.Tensor) -> dict:
     return dict(fallback_events=int(v[0].item()), row_tiles=int(v[1].item()), status=st)
 
 
+def _out_dtype(out_dtype):
+    if out_dtype in (None, "f32", torch.float32, FSA_OUT_F32):
+        return FSA_OUT_F32, torch.float32
+    if out_dtype in ("bf16", torch.bfloat16, FSA_OUT_BF16):
+        return FSA_OUT_BF16, torch.bfloat16
+    raise FsaError(FSA_ERR_INVALID_ARG, f"out_dtype {out_dtype!r}")
+
+
+def _opts(delta=None, exp_mode=None, efq_a=None, efq_b=None, efq_phi=None, timeout_ms=0, inject_stall=False,
+          schedule=None, out_dtype=FSA_OUT_F32) -> fsa_opts:
+    o = default_opts()
+    if delta is not None:
+        o.delta = float(delta)
+    if exp_mode is not None:
+        o.exp_mode = int(exp_mode)
+    if efq_a is not None:
+        o.efq_a = float(efq_a)
+    if efq_b is not None:
+        o.efq_b = float(efq_b)
+    if efq_phi is not None:
+        o.efq_phi = float(efq_phi)
+    if timeout_ms:
+        o.timeout_ms = int(timeout_ms)
+    o.inject_stall = int(bool(inject_stall))
+    if schedule is not None:
+        o.schedule = int(schedule)
+    o.out_dtype = int(out_dtype)
+    return o
+
+
+class DebugDump:
+    """Device buffers for the debug instance's per-tile dumps (fsa_debug_dump): every
+    query row, or only `rows` (global row ids, dumped in that order).  Entries the
+    kernel does not write keep their initial values: scores -inf, M NaN, words 0."""
+
+    def __init__(self, B, H, Sq, Sk, device=None, rows=None):
+        R, nkt = B * H * Sq, (Sk + 127) // 128
+        dev = device or "cuda"
+        self.row_slot = None
+        if rows is not None:
+            rows = torch.as_tensor(rows, dtype=torch.int64)
+            slot = torch.full((R,), -1, dtype=torch.int32)
+            slot[rows] = torch.arange(len(rows), dtype=torch.int32)
+            self.row_slot = slot.to(dev)
+            R = len(rows)
+        self.n_rows, self.nkt = R, nkt
+        self.s = torch.full((R, nkt * 128), float("-inf"), dtype=torch.float32, device=dev)
+        self.m = torch.full((R, nkt), float("nan"), dtype=torch.float32, device=dev)
+        self.p = torch.zeros((R, nkt, 32), dtype=torch.int32, device=dev)
+        self.p_scales = torch.zeros((R, nkt), dtype=torch.int32, device=dev)
+
+    def struct(self) -> fsa_debug_dump:
+        return fsa_debug_dump(self.s.data_ptr(), self.m.data_ptr(), self.p.data_ptr(), self.p_scales.data_ptr(),
+                              self.row_slot.data_ptr() if self.row_slot is not None else 0)
+
+
 def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
                       causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=None, exp_mode=None,
-                      efq_beta=2, timeout_ms=0, row_fallbacks: torch.Tensor | None = None, stats=None,
-                      inject_stall=False, schedule=None, stream=None) -> torch.Tensor:
-    """O [B,H,Sq,D] fp32 by the fused MX forward (fsa_attention_fwd_ex)."""
+                      efq_a=None, efq_b=None, efq_phi=None, timeout_ms=0,
+                      row_fallbacks: torch.Tensor | None = None, stats=None, inject_stall=False, schedule=None,
+                      out_dtype=None, debug: DebugDump | None = None, stream=None) -> torch.Tensor:
+    """O [B,H,Sq,D] (fp32, or bf16 with out_dtype="bf16") by the fused MX forward (fsa_attention_fwd_ex)."""
     B, H, Sq, D = q.B, q.H, q.S, q.D
     Hkv = k.H if Hkv is None else Hkv
     Sk = k.S
     scale = D ** -0.5 if scale is None else scale
     fmt_qk = q.fmt if fmt_qk is None else _fmt(fmt_qk)
     fmt_pv = v.fmt if fmt_pv is None else _fmt(fmt_pv)
+    od, tdt = _out_dtype(out_dtype if out is None or out_dtype is not None else out.dtype)
     if out is None:
-        out = torch.empty((B, H, Sq, D), dtype=torch.float32, device=q.codes.device)
-    _need_cuda(out, "out", torch.float32)
+        out = torch.empty((B, H, Sq, D), dtype=tdt, device=q.codes.device)
+    _need_cuda(out, "out", tdt)
     if out.numel() < B * H * Sq * D:
         raise FsaError(FSA_ERR_INVALID_ARG, "out is smaller than B*H*Sq*D")
     for m, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -241,22 +325,26 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
         _need_cuda(stats, "stats")
         if stats.device != out.device or stats.numel() * stats.element_size() < STATS_BYTES:
             raise FsaError(FSA_ERR_INVALID_ARG, f"stats must hold {STATS_BYTES} bytes on {out.device}")
-    o = default_opts()
-    if delta is not None:
-        o.delta = float(delta)
-    if exp_mode is not None:
-        o.exp_mode = int(exp_mode)
-    o.efq_beta = int(efq_beta)
-    if timeout_ms:
-        o.timeout_ms = int(timeout_ms)
-    o.inject_stall = int(bool(inject_stall))
-    if schedule is not None:
-        o.schedule = int(schedule)
+    o = _opts(delta, exp_mode, efq_a, efq_b, efq_phi, timeout_ms, inject_stall, schedule, od)
     if row_fallbacks is not None:
         _need_cuda(row_fallbacks, "row_fallbacks", torch.int32)
         if row_fallbacks.device != out.device or row_fallbacks.numel() < B * H * Sq:
             raise FsaError(FSA_ERR_INVALID_ARG, f"row_fallbacks must hold B*H*Sq int32 on {out.device}")
         o.row_fallbacks = row_fallbacks.data_ptr()
+    if debug is not None:
+        nkt = (Sk + 127) // 128
+        nslot = debug.n_rows if debug.row_slot is not None else B * H * Sq
+        if debug.nkt != nkt:
+            raise FsaError(FSA_ERR_INVALID_ARG, "debug dump made for another key length")
+        for t, n, cols in ((debug.s, "s", nkt * 128), (debug.m, "m", nkt), (debug.p, "p", nkt * 32),
+                           (debug.p_scales, "p_scales", nkt)):
+            _need_cuda(t, f"debug.{n}")
+            if t.device != out.device or t.numel() < nslot * cols:
+                raise FsaError(FSA_ERR_INVALID_ARG, f"debug.{n} is too small")
+        if debug.row_slot is not None and (debug.row_slot.numel() != B * H * Sq or debug.row_slot.device != out.device):
+            raise FsaError(FSA_ERR_INVALID_ARG, "debug.row_slot must hold B*H*Sq slots on the output's device")
+        dd = debug.struct()
+        o.debug = ctypes.pointer(dd)
     qs, ks, vs = q.struct(), k.struct(), v.struct()
     _check(load().fsa_attention_fwd_ex(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs),
                                        ctypes.c_void_p(out.data_ptr()), B, H, Hkv, Sq, Sk, D, int(bool(causal)),
@@ -264,6 +352,66 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
                                        ctypes.c_void_p(stats.data_ptr() if stats is not None else 0),
                                        _stream(stream)), "fsa_attention_fwd_ex")
     return out
+
+
+def fsa_attention_fwd_layers(layers, *, out_dtype=None, stream=None, **opt_kw) -> list:
+    """Several attention layers, each with its own formats and margin, back to back on one
+    stream (fsa_attention_fwd_layers).  layers: dicts with q, k, v (MxTensor), causal,
+    scale, fmt_qk, fmt_pv, delta, optional out and stats.  Returns the outputs."""
+    od, tdt = _out_dtype(out_dtype)
+    n = len(layers)
+    arr = (fsa_layer * max(n, 1))()
+    keep, outs = [], []
+    for i, L in enumerate(layers):
+        q, k, v = L["q"], L["k"], L["v"]
+        out = L.get("out")
+        if out is None:
+            out = torch.empty((q.B, q.H, q.S, q.D), dtype=tdt, device=q.codes.device)
+        _need_cuda(out, "out", tdt)
+        if out.numel() < q.B * q.H * q.S * q.D:
+            raise FsaError(FSA_ERR_INVALID_ARG, "out is smaller than B*H*Sq*D")
+        for m, nm in ((q, "q"), (k, "k"), (v, "v")):
+            _need_mx(m, nm, out.device)
+        st = L.get("stats")
+        if st is not None:
+            _need_cuda(st, "stats")
+            if st.device != out.device or st.numel() * st.element_size() < STATS_BYTES:
+                raise FsaError(FSA_ERR_INVALID_ARG, f"stats must hold {STATS_BYTES} bytes on {out.device}")
+        structs = (q.struct(), k.struct(), v.struct())
+        keep.append(structs)
+        fq = q.fmt if L.get("fmt_qk") is None else _fmt(L["fmt_qk"])
+        fp = v.fmt if L.get("fmt_pv") is None else _fmt(L["fmt_pv"])
+        scale = L.get("scale") or q.D ** -0.5
+        arr[i] = fsa_layer(ctypes.pointer(structs[0]), ctypes.pointer(structs[1]), ctypes.pointer(structs[2]),
+                           out.data_ptr(), q.B, q.H, k.H, q.S, k.S, q.D, int(bool(L.get("causal", False))),
+                           float(scale), fq, fp, float(L.get("delta", 8.0)), st.data_ptr() if st is not None else 0)
+        outs.append(out)
+    o = _opts(out_dtype=od, **opt_kw)
+    _check(load().fsa_attention_fwd_layers(arr, n, ctypes.byref(o), _stream(stream)), "fsa_attention_fwd_layers")
+    return outs
+
+
+def fsa_tune_delta(stats: list, deltas: list, target_rate=0.01, step=4.0, max_delta=64.0) -> list:
+    """Host-side margin update from per-layer stats dicts (read_stats); returns new margins."""
+    n = len(stats)
+    sarr = (fsa_stats * max(n, 1))()
+    for i, st in enumerate(stats):
+        sarr[i] = fsa_stats(int(st["fallback_events"]), int(st["row_tiles"]), int(st["status"]), 0)
+    d = (ctypes.c_float * max(n, 1))(*[float(x) for x in deltas])
+    _check(load().fsa_tune_delta(sarr, n, float(target_rate), float(step), float(max_delta), d), "fsa_tune_delta")
+    return [float(d[i]) for i in range(n)]
+
+
+def fsa_mma_peak(kind: int, n_ctas: int, iters: int, status: torch.Tensor | None = None, stream=None) -> float:
+    """Launch the tensor-core throughput probe; returns the launch's FLOPs (time it with events)."""
+    fl = ctypes.c_double()
+    ptr = 0
+    if status is not None:
+        _need_cuda(status, "status", torch.int32)
+        ptr = status.data_ptr()
+    _check(load().fsa_mma_peak(int(kind), int(n_ctas), int(iters), ctypes.c_void_p(ptr), ctypes.byref(fl),
+                               _stream(stream)), "fsa_mma_peak")
+    return fl.value
 
 
 def fsa_bf16_transpose_v(v: torch.Tensor, vt: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -32,7 +32,8 @@ def _nvcc() -> str:
 
 def _units():
     units = [("fsa_api", os.path.join(CSRC, "fsa_api.cu"), []),
-             ("fsa_quant", os.path.join(CSRC, "fsa_quant.cu"), [])]
+             ("fsa_quant", os.path.join(CSRC, "fsa_quant.cu"), []),
+             ("fsa_peak", os.path.join(CSRC, "fsa_peak.cu"), [])]
     for qk, pv in ATTN_PAIRS:
         units.append((f"fsa_attn_{qk}{pv}", os.path.join(CSRC, "fsa_attn.cu"),
                       [f"-DFSA_INST_QK={qk}", f"-DFSA_INST_PV={pv}"]))

@@ -5,7 +5,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <climits>
 #include <mutex>
+#include <unordered_map>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "fsa.h"
@@ -34,37 +36,94 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensor maps are a pure function of (base, type, dims, strides, box, swizzle):
+// encoded once per distinct key and reused, so repeated calls on the same buffers
+// skip the driver's encode.  The cache is bounded (cleared when full).
+struct TmapKey {
+  uintptr_t base;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  int dtype, swizzle, promo;
+  bool operator==(const TmapKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+struct TmapKeyHash {
+  size_t operator()(const TmapKey& k) const {
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;                     // FNV-1a over the key bytes
+    for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return (size_t)h;
+  }
+};
+
+bool encode_cached(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                   const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw,
+                   CUtensorMapL2promotion promo) {
+  static std::mutex mu;
+  static std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> cache;
+  TmapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = reinterpret_cast<uintptr_t>(base);
+  for (int i = 0; i < 3; ++i) { key.dims[i] = dims[i]; key.box[i] = box[i]; }
+  key.strides[0] = strides[0]; key.strides[1] = strides[1];
+  key.dtype = (int)dtype; key.swizzle = (int)sw; key.promo = (int)promo;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) { *m = it->second; return true; }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(m, dtype, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache.size() >= 512) cache.clear();
+  cache.emplace(key, *m);
+  return true;
+}
+
 // 3-D byte tensor {inner bytes, rows, planes}, box {width, box_rows, 1}, swizzle by width.
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t planes, uint32_t width,
                uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {inner, rows, planes};
-  const cuuint64_t strides[2] = {inner, inner * rows};
-  const cuuint32_t box[3] = {width, box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const uint64_t dims[3] = {inner, rows, planes};
+  const uint64_t strides[2] = {inner, inner * rows};
+  const uint32_t box[3] = {width, box_rows, 1};
   const CUtensorMapSwizzle sw = width == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : width == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box, sw,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-// Tensor map of the fp32 output O [planes][rows][D]: boxes of 32 rows x 32 floats
-// (128 bytes), 128B swizzle, written by TMA stores from the kernel's epilogue.
-// fp32 output [planes][rows][D]: 32x32 boxes with 128B swizzle (one CTA per query
-// tile), or 16x32 boxes with 64B swizzle (the persistent schedule's staging box)
-bool make_tmap_out(CUtensorMap* m, float* base, uint64_t D, uint64_t rows, uint64_t planes, bool persistent) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {D, rows, planes};
-  const cuuint64_t strides[2] = {D * 4, D * 4 * rows};
-  const cuuint32_t box[3] = {persistent ? 16u : 32u, 32, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            persistent ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// Output O [planes][rows][D], written by TMA stores from the epilogue.
+//   one CTA per query tile: fp32 boxes of 32 rows x 32 floats (128B swizzle); bf16
+//     boxes of 32 rows x D/2 values (128B swizzle for D = 128, 64B for D = 64)
+//   persistent schedule: boxes of 32 rows x 16 values, fp32 (64B swizzle) or bf16
+//     (32B swizzle)
+bool make_tmap_out(CUtensorMap* m, void* base, uint64_t D, uint64_t rows, uint64_t planes, bool persistent,
+                   bool bf16) {
+  const uint64_t esz = bf16 ? 2 : 4;
+  const uint64_t dims[3] = {D, rows, planes};
+  const uint64_t strides[2] = {D * esz, D * esz * rows};
+  uint32_t bw;
+  CUtensorMapSwizzle sw;
+  if (!bf16) {
+    bw = persistent ? 16u : 32u;
+    sw = persistent ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  } else if (persistent) {
+    bw = 16u;
+    sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  } else {
+    bw = (uint32_t)(D / 2);
+    sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  }
+  const uint32_t box[3] = {bw, 32, 1};
+  return encode_cached(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims,
+                       strides, box, sw, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // storage bits per element * 2, as the kernels store them
@@ -76,9 +135,12 @@ bool valid_fmt(int f) { return f >= FSA_FMT_E4M3 && f <= FSA_FMT_E2M1; }
 
 int storage_fmt(int f) { return f == FSA_FMT_E2M1_EFQ ? FSA_FMT_E2M1 : f; }
 
+// The query-tile count B*H*ceil(Sq/128) must fit an int (the persistent schedule
+// indexes its work list with it).
 bool shape_ok(int B, int H, int Hkv, int Sq, int Sk, int D) {
   return B > 0 && H > 0 && Hkv > 0 && H % Hkv == 0 && Sq > 0 && Sk > 0 && (D == 64 || D == 128) &&
-         (int64_t)B * H <= 65535 && (int64_t)Sq <= 65535 * 128 && (int64_t)Sk <= (1 << 24);
+         (int64_t)B * H <= 65535 && (int64_t)Sq <= 65535 * 128 && (int64_t)Sk <= (1 << 24) &&
+         (int64_t)B * H * ((Sq + 127) / 128) <= INT_MAX;
 }
 
 using ImplFn = cudaError_t (*)(const AttnLaunch&);
@@ -122,8 +184,13 @@ void fill_common(fsa::KParams& p, int B, int H, int Hkv, int Sq, int Sk, int cau
   p.causal = causal ? 1 : 0;
   p.c = (float)((double)scale * 1.4426950408889634073599246810018921);   // log2(e)
   p.delta = o->delta;
-  p.efq_beta = o->efq_beta;
-  p.efq_fast = (o->efq_beta <= 2 && o->delta <= 120.0f) ? 1 : 0;
+  // EFQ constants scaled by 1/8 (exact): A = fp32(a c), a, b; phi as given
+  const float A = o->efq_a * p.c;
+  p.efq_A8 = A * 0.125f;
+  p.efq_a8 = o->efq_a * 0.125f;
+  p.efq_b8 = o->efq_b * 0.125f;
+  p.efq_phi = o->efq_phi;
+  p.out_bf16 = o->out_dtype == FSA_OUT_BF16 ? 1 : 0;
   p.timeout_ns = (uint64_t)(o->timeout_ms ? o->timeout_ms : 4000u) * 1000000ull;
   p.row_fallbacks = o->row_fallbacks;
   p.stat_fallbacks = stats ? &stats->fallback_events : nullptr;
@@ -141,11 +208,14 @@ void fsa_default_opts(fsa_opts* o) {
   std::memset(o, 0, sizeof(*o));
   o->delta = 8.0f;
   o->exp_mode = FSA_EXP_MUFU;
-  o->efq_beta = 2;
+  o->efq_a = FSA_EFQ_A_DEFAULT;
+  o->efq_b = FSA_EFQ_B_DEFAULT;
+  o->efq_phi = FSA_EFQ_PHI_DEFAULT;
   o->timeout_ms = 4000;
+  o->out_dtype = FSA_OUT_F32;
 }
 
-int fsa_version(void) { return 100; }
+int fsa_version(void) { return 200; }
 
 const char* fsa_status_string(int s) {
   switch (s) {
@@ -224,7 +294,7 @@ int fsa_bf16_transpose_v(const void* v, void* vt, int B, int Hkv, int S, int D, 
   return launch_status(fsa::launch_transpose_v(v, vt, B * Hkv, S, D, static_cast<cudaStream_t>(stream)));
 }
 
-int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, float* out,
+int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, void* out,
                          int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale, int fmt_qk,
                          int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream) {
   if (!q || !k || !v || !out) return FSA_ERR_INVALID_ARG;
@@ -243,10 +313,20 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
   fsa_opts o;
   fsa_default_opts(&o);
   if (opts) o = *opts;
-  if (o.exp_mode < 0 || o.exp_mode > 2 || o.efq_beta < -16 || o.efq_beta > 16 || !std::isfinite(o.delta) ||
-      o.schedule < FSA_SCHED_AUTO || o.schedule > FSA_SCHED_PERSISTENT)
+  // a negative margin would make nearly every tile fall back; the EFQ constants keep
+  // the code domain finite and the block exponent's reference point within one binade
+  if (o.exp_mode < 0 || o.exp_mode > 2 || !std::isfinite(o.delta) || o.delta < 0.0f ||
+      !(o.efq_a > 0.0f && o.efq_a <= 16.0f) || !(std::fabs(o.efq_b) <= 64.0f) ||
+      !(o.efq_phi >= 0.0f && o.efq_phi < 1.0f) || o.schedule < FSA_SCHED_AUTO || o.schedule > FSA_SCHED_PERSISTENT ||
+      (o.out_dtype != FSA_OUT_F32 && o.out_dtype != FSA_OUT_BF16))
     return FSA_ERR_INVALID_ARG;
-  const bool persistent = persistent_schedule(o.schedule, Sq, Sk, causal);
+  const fsa_debug_dump* dbg = o.debug;
+  if (dbg && (!dbg->s || !dbg->m || !dbg->p || !dbg->p_scales)) return FSA_ERR_INVALID_ARG;
+  if (dbg && !(fmt_qk == storage_fmt(fmt_pv) || (fmt_qk == FSA_FMT_E2M1 && fmt_pv == FSA_FMT_E2M1_EFQ)))
+    return FSA_ERR_UNSUPPORTED_FMT;
+  if (dbg && fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode == FSA_EXP_SPLIT) return FSA_ERR_UNSUPPORTED_FMT;
+  const bool persistent = !dbg && persistent_schedule(o.schedule, Sq, Sk, causal);
+  const bool bf16 = o.out_dtype == FSA_OUT_BF16;
 
   AttnLaunch a;
   std::memset(&a, 0, sizeof(a));
@@ -259,16 +339,21 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
   if (!make_tmap(&a.tq, q->codes, rbq, Sq, (uint64_t)B * H, wq, 128) ||
       !make_tmap(&a.tk, k->codes, rbq, Sk, (uint64_t)B * Hkv, wq, 128) ||
       !make_tmap(&a.tv, v->codes, rbv_total, D, (uint64_t)B * Hkv, wv, D) ||
-      !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H, persistent))
+      !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H, persistent, bf16))
     return FSA_ERR_LAUNCH;
   fill_common(a.p, B, H, Hkv, Sq, Sk, causal, scale, &o, stats);
   a.p.sf_q = q->scales; a.p.sf_k = k->scales; a.p.sf_v = v->scales;
-  a.p.out = out;
+  if (dbg) {
+    a.dbg.s = dbg->s; a.dbg.m = dbg->m; a.dbg.p = dbg->p; a.dbg.sf = dbg->p_scales; a.dbg.row_slot = dbg->row_slot;
+    a.debug = 1;
+  }
   a.D = D;
   a.exp_mode = o.exp_mode;
   a.persistent = persistent ? 1 : 0;
   a.stream = static_cast<cudaStream_t>(stream);
-  return launch_status(impl_for(fmt_qk, fmt_pv)(a));
+  const cudaError_t e = impl_for(fmt_qk, fmt_pv)(a);
+  if (e == cudaErrorNotSupported) return FSA_ERR_UNSUPPORTED_FMT;
+  return launch_status(e);
 }
 
 int fsa_attention_fwd(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, float* out, int B,
@@ -294,14 +379,64 @@ int fsa_attention_fwd_bf16(const void* q, const void* k, const void* vt, float* 
   if (!make_tmap(&a.tq, q, 2 * D, Sq, (uint64_t)B * H, 128, 128) ||
       !make_tmap(&a.tk, k, 2 * D, Sk, (uint64_t)B * Hkv, 128, 128) ||
       !make_tmap(&a.tv, vt, 2 * Sp, D, (uint64_t)B * Hkv, 128, D) ||
-      !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H, persistent))
+      !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H, persistent, false))
     return FSA_ERR_LAUNCH;
   fill_common(a.p, B, H, Hkv, Sq, Sk, causal, scale, &o, stats);
-  a.p.out = out;
   a.D = D;
   a.persistent = persistent ? 1 : 0;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_status(fsa::launch_attn_impl<fsa::F_BF16, fsa::F_BF16>(a));
+}
+
+int fsa_attention_fwd_layers(const fsa_layer* layers, int n_layers, const fsa_opts* opts, void* stream) {
+  if (n_layers < 0 || (n_layers > 0 && !layers)) return FSA_ERR_INVALID_ARG;
+  // every layer is checked before the first launch, so an argument error enqueues nothing
+  for (int l = 0; l < n_layers; ++l) {
+    const fsa_layer& L = layers[l];
+    if (!L.q || !L.k || !L.v || !L.out || !std::isfinite(L.delta) || L.delta < 0.0f) return FSA_ERR_INVALID_ARG;
+    if (!shape_ok(L.B, L.H, L.Hkv, L.Sq, L.Sk, L.D) || !(L.scale > 0.0f) || !std::isfinite(L.scale))
+      return FSA_ERR_INVALID_ARG;
+    if (!valid_fmt(L.fmt_qk) || L.fmt_pv < FSA_FMT_E4M3 || L.fmt_pv > FSA_FMT_E2M1_EFQ)
+      return FSA_ERR_UNSUPPORTED_FMT;
+    if (L.q->fmt != L.fmt_qk || L.k->fmt != L.fmt_qk || L.v->fmt != storage_fmt(L.fmt_pv))
+      return FSA_ERR_UNSUPPORTED_FMT;
+  }
+  fsa_opts o;
+  fsa_default_opts(&o);
+  if (opts) o = *opts;
+  if (o.debug) return FSA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const fsa_layer& L = layers[l];
+    o.delta = L.delta;
+    o.row_fallbacks = nullptr;
+    const int st = fsa_attention_fwd_ex(L.q, L.k, L.v, L.out, L.B, L.H, L.Hkv, L.Sq, L.Sk, L.D, L.causal, L.scale,
+                                        L.fmt_qk, L.fmt_pv, &o, L.stats, stream);
+    if (st != FSA_OK) return st;
+  }
+  return FSA_OK;
+}
+
+int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, float step, float max_delta,
+                   float* delta) {
+  if (n_layers < 0 || (n_layers > 0 && (!stats || !delta)) || !(target_rate >= 0.0f) || !(step > 0.0f) ||
+      !std::isfinite(step) || !(max_delta >= 0.0f) || !std::isfinite(max_delta))
+    return FSA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (!std::isfinite(delta[l]) || delta[l] < 0.0f || delta[l] > max_delta) return FSA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    if (stats[l].status != FSA_OK || stats[l].row_tiles == 0) continue;   // no evidence from this layer
+    const double rate = (double)stats[l].fallback_events / (double)stats[l].row_tiles;
+    if (rate > (double)target_rate) delta[l] = std::min(max_delta, delta[l] + step);
+  }
+  return FSA_OK;
+}
+
+int fsa_mma_peak(int kind, int n_ctas, long long iters, int32_t* status, double* flops, void* stream) {
+  if (kind < 0 || kind > 2 || n_ctas <= 0 || n_ctas > 65535 || iters <= 0 || iters > (1ll << 40))
+    return FSA_ERR_INVALID_ARG;
+  if (flops) *flops = fsa::mma_peak_flops_per_iter(kind) * (double)iters * (double)n_ctas;
+  return launch_status(fsa::launch_mma_peak(kind, n_ctas, iters, status, 2000000000ull,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

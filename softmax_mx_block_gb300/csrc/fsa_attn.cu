@@ -159,45 +159,58 @@ __device__ __forceinline__ int block_exp(float bmax, float c, float M, float& nb
   return E;
 }
 
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // P codes of one 32-key block, in place: v[0..32) holds the raw scores (masked =
 // -inf) on entry and is clobbered.  Writes 8 packed words (one byte per code) or 4
 // (E2M1) to out[] and returns the scale byte E + 127.
 template <int FPV, int EXPM>
-__device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, float M, int beta, uint32_t* out) {
-  float nb;
-  const int E = block_exp<FPV>(bmax, c, M, nb);
-  const uint64_t c2 = pk2(c, c), nb2 = pk2(nb, nb);
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) upk2(ffma2(pk2(v[i], v[i + 1]), c2, nb2), v[i], v[i + 1]);
+__device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, float M, const KParams& p, uint32_t* out) {
   if constexpr (FPV == F_EFQ) {
-    // k = clamp(rne(2 r + beta), 0, 7): fma onto the integer grid of 1.5*2^23, whose
-    // low bits then hold k; nibble pairs combine by shift-add, bytes merge by permute
-    const float magic = 12582912.0f;
-    const uint64_t two2 = pk2(2.0f, 2.0f), kb2 = pk2(magic + (float)beta, magic + (float)beta);
-    // EXPM 1: beta <= 2 and a fallback margin delta <= 120, so E = floor(tmax) - 2 <=
-    // 125 is never clamped from above, r < 3 (up to rounding), 2 r + beta < 8.5 and a
-    // rounded code is at most 8: clamp below only, then turn the nibbles equal to 8
-    // into 7 on the packed word (8 - 1; no nibble of 0..7 has bit 3 set).
-    // EXPM 0: any beta and delta, both sides clamped.
-    constexpr bool one_sided = EXPM == 1;
-    uint32_t y[32];
+    // EFQ: block exponent E = clamp(floor(fp32(tmax + phi)) - 2, -127, 127) from the
+    // block maximum; then one fused multiply-add per score maps it to the code domain,
+    // y = s * A + Bk with A = fp32(a c) and Bk = fp32(b - fp32(a fp32(M + E))), and
+    // code = clamp(rne(y), 0, 7).  Computed as z = sat(y / 8) (the scaling by 1/8 is
+    // exact, so z is fp32(y) / 8 clamped to [0, 1]); then z + 1.5*2^20 rounds 8z to
+    // the nearest integer (ties to even) in the low bits of the sum.  A block with no
+    // visible key has M + E = -inf, Bk = +inf and y NaN: sat gives 0.
+    const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
+    int E = (int)fmaxf(floorf(__fadd_rn(tmax, p.efq_phi)), -256.0f) - 2;
+    E = E < -127 ? -127 : (E > 127 ? 127 : E);
+    const float bE = __fadd_rn(M, (float)E);
+    // Bk / 8 = fp32(b/8 - fp32(a/8 * bE)): the same roundings as fp32(b - fp32(a bE)), scaled
+    const float b8 = __fsub_rn(p.efq_b8, __fmul_rn(p.efq_a8, bE));
+    const float a8 = p.efq_A8;
+    const uint64_t mg = pk2(1572864.0f, 1572864.0f);                       // 1.5 * 2^20
+    uint32_t t[32];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-      float y0, y1;
-      upk2(ffma2(two2, pk2(v[i], v[i + 1]), kb2), y0, y1);
-      y[i] = __float_as_uint(one_sided ? fmaxf(y0, magic) : fminf(fmaxf(y0, magic), magic + 7.0f));
-      y[i + 1] = __float_as_uint(one_sided ? fmaxf(y1, magic) : fminf(fmaxf(y1, magic), magic + 7.0f));
+      float k0, k1;
+      upk2(fadd2(pk2(fma_sat(v[i], a8, b8), fma_sat(v[i + 1], a8, b8)), mg), k0, k1);
+      t[i] = __float_as_uint(k0);
+      t[i + 1] = __float_as_uint(k1);
     }
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const uint32_t* t = y + 8 * w;
-      // low byte of (t1 << 4) + t0 is k0 | k1 << 4 (the magic's bits stay above bit 21)
-      const uint32_t a01 = (t[1] << 4) + t[0], a23 = (t[3] << 4) + t[2];
-      const uint32_t a45 = (t[5] << 4) + t[4], a67 = (t[7] << 4) + t[6];
+      const uint32_t* u = t + 8 * w;
+      // the low byte of (u1 << 4) + u0 is k0 | k1 << 4 (the magic's bits stay above bit 21)
+      const uint32_t a01 = (u[1] << 4) + u[0], a23 = (u[3] << 4) + u[2];
+      const uint32_t a45 = (u[5] << 4) + u[4], a67 = (u[7] << 4) + u[6];
       const uint32_t wv = prmt(prmt(a01, a23, 0x0040u), prmt(a45, a67, 0x0040u), 0x5410u);
-      out[w] = one_sided ? wv - ((wv >> 3) & 0x11111111u) : wv;
+      // codes are 0..8: turn each nibble equal to 8 into 7 (no nibble of 0..7 has bit 3)
+      out[w] = wv - ((wv >> 3) & 0x11111111u);
     }
+    return (uint32_t)(E + 127);
   } else {
+    float nb;
+    const int E = block_exp<FPV>(bmax, c, M, nb);
+    const uint64_t c2 = pk2(c, c), nb2 = pk2(nb, nb);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) upk2(ffma2(pk2(v[i], v[i + 1]), c2, nb2), v[i], v[i + 1]);
     exp2_block<EXPM>(v);
     if constexpr (FPV == F_E4M3) {
 #pragma unroll
@@ -216,19 +229,21 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
         out[w] = prmt(prmt(b01, b23, 0x0040u), prmt(b45, b67, 0x0040u), 0x5410u);
       }
     }
+    return (uint32_t)(E + 127);
   }
-  return (uint32_t)(E + 127);
 }
 
 }  // namespace fsa
 
 namespace fsa {
 
-template <int FQK, int FPV, int D, int EXPM>
+// DBG: the debug instance, which also writes each tile's raw scores, its frozen
+// maximum and its P~ code and scale words to the dump buffers of KParams (tests).
+template <int FQK, int FPV, int D, int EXPM, bool DBG = false>
 __global__ void __launch_bounds__(Cfg<FQK, FPV, D>::NTHREADS, 1)
 fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                const KParams p) {
+                const KParams p, const DbgParams dbg) {
   using C = Cfg<FQK, FPV, D>;
   constexpr int KIND_QK = Fmt<FQK>::kind, KIND_PV = Fmt<FPV>::kind;
   constexpr bool MX = C::MX;
@@ -534,6 +549,15 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int rl = 32 * qd + lane;                  // row within the tile
     const int row = q0 + rl;
     const bool row_valid = row < p.Sq;
+    // debug dumps: this row's slot (negative: not dumped)
+    long long dbg_row = -1;
+    if constexpr (DBG) {
+      if (row_valid) {
+        const long long grow = ((long long)b * p.H + h) * p.Sq + row;
+        dbg_row = dbg.row_slot ? (long long)dbg.row_slot[grow] : grow;
+      }
+    }
+    const bool dbg_on = DBG && dbg_row >= 0;
     const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16);
     int lim = p.Sk - 1;
     if (p.causal) lim = min(lim, row + p.Sk - p.Sq);
@@ -582,6 +606,13 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int b = 0; b < NBLK; ++b) bm[b] = bmr[b];
         }
+        if constexpr (DBG) {
+          if (dbg_on) {
+            float4* ds = reinterpret_cast<float4*>(dbg.s + dbg_row * nkt * 128 + 128 * j);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ds[i] = make_float4(sv[4 * i], sv[4 * i + 1], sv[4 * i + 2], sv[4 * i + 3]);
+          }
+        }
       }
       // M after tile j-1 comes from the other part (NaN: it has stopped working)
       if (j > 0) {
@@ -611,6 +642,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const float alpha = rescale ? ex2_approx(__fsub_rn(M, Mn)) : 1.0f;
       if (rescale) ++nfb;
       M = Mn;
+      if constexpr (DBG) {
+        if (ok && dbg_on) dbg.m[dbg_row * nkt + j] = M;
+      }
       if constexpr (!MX) {
         if (Ml != kNegInf && M != Ml) lsum *= ex2_approx(__fsub_rn(Ml, M));
         Ml = M;
@@ -629,7 +663,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             constexpr int WB = C::P_COLS / NBLK;       // words per block: 8, or 4 for E2M1
 #pragma unroll
             for (int b = 0; b < 2; ++b)
-              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p.efq_beta, pw + WB * b)
+              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p, pw + WB * b)
                     << (8 * (2 * hf + b));
           } else {
             const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
@@ -643,8 +677,19 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
           }
         };
+        auto dbg_words = [&](int hf, const uint32_t* pw) {
+          if constexpr (DBG) {
+            if (dbg_on) {
+#pragma unroll
+              for (int w = 0; w < HW; ++w) dbg.p[(dbg_row * nkt + j) * 32 + HW * hf + w] = pw[w];
+            }
+          }
+        };
         uint32_t pw[HW];
-        if constexpr (MX) gen_half(0, pw);           // (BF16: too many registers to hold across)
+        if constexpr (MX) {
+          gen_half(0, pw);                           // (BF16: too many registers to hold across)
+          dbg_words(0, pw);
+        }
         // fallback: O_aug row *= 2^(M_old - M) once PV(j-1) has landed.  tcgen05.ld/st
         // are warp-collective, so the whole warp rescales when any of its rows falls
         // back; the other rows multiply by exactly 1.
@@ -675,9 +720,13 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if constexpr (!MX) gen_half(0, pw);
           tmem_st_cols<HW>(tp, pw);
           gen_half(1, pw);
+          dbg_words(1, pw);
           tmem_st_cols<HW>(tp + HW, pw);
           // A scales of the PV MMA: lane quadrant q reads column base + q
           if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
+          if constexpr (DBG) {
+            if (dbg_on) dbg.sf[dbg_row * nkt + j] = sw;
+          }
           if constexpr (!MX) {
             float a0, a1;
             upk2(acc, a0, a1);
@@ -728,6 +777,31 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const bool lpos = l > 0.f;
       const float rinv = lpos ? __frcp_rn(l) : 0.f;
       fence_proxy_async_smem();                      // the ring was last written by TMA loads
+      if (p.out_bf16) {
+        // bf16 output: the same fp32 quotients rounded to nearest even, one box of 32
+        // rows x DP bf16 per warp (128B swizzle for 128-byte rows, else 64B)
+        uint8_t* box = sm + C::OFF_OSTAGE + (qd * 2 + pp) * 4096;
+        auto qv = [&](uint32_t x) { return lpos ? __fmul_rn(__uint_as_float(x), rinv) : 0.f; };
+#pragma unroll
+        for (int ch = 0; ch < DP / 8; ++ch) {
+          const uint32_t* src = o + 8 * ch;
+          uint4 wv;
+          wv.x = cvt_bf16x2(qv(src[0]), qv(src[1]));
+          wv.y = cvt_bf16x2(qv(src[2]), qv(src[3]));
+          wv.z = cvt_bf16x2(qv(src[4]), qv(src[5]));
+          wv.w = cvt_bf16x2(qv(src[6]), qv(src[7]));
+          const int off = DP == 64 ? lane * 128 + ((ch ^ (lane & 7)) << 4) : lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4);
+          *reinterpret_cast<uint4*>(box + off) = wv;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, box, DP * pp, q0 + 32 * qd, b * p.H + h);
+          bulk_commit_group();
+          bulk_wait_all();
+        }
+        __syncwarp();
+      } else {
 #pragma unroll
       for (int t = 0; t < NBOX; ++t) {
         uint8_t* box = sm + C::OFF_OSTAGE + (qd * (D / 32) + (DP * pp) / 32 + t) * 4096;
@@ -755,6 +829,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bulk_wait_all();                             // before the CTA (and its shared memory) ends
       }
       __syncwarp();
+      }
     }
     // ---- statistics: each part counted the tiles it owns
     int* nfb_other = reinterpret_cast<int*>(red) + 128 + rl;
@@ -788,16 +863,16 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 namespace fsa {
 
 // ----------------------------------------------------------------------------- host launch
-template <int FQK, int FPV, int D, int EXPM>
+template <int FQK, int FPV, int D, int EXPM, bool DBG = false>
 static cudaError_t launch_one(const AttnLaunch& a) {
   using C = Cfg<FQK, FPV, D>;
   // at least 116 KB so that one CTA (and its 512 tensor-memory columns) owns an SM
   constexpr int smem = (C::SMEM > 116 * 1024 ? C::SMEM : 116 * 1024);
-  auto kern = fsa_attn_kernel<FQK, FPV, D, EXPM>;
+  auto kern = fsa_attn_kernel<FQK, FPV, D, EXPM, DBG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid = a.p.causal ? dim3(a.p.H * a.p.B, a.p.n_qtiles, 1) : dim3(a.p.n_qtiles, a.p.H, a.p.B);
-  kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.to, a.p);
+  kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.to, a.p, a.dbg);
   return cudaGetLastError();
 }
 
@@ -821,27 +896,34 @@ static cudaError_t launch_persistent(const AttnLaunch& a) {
   return cudaGetLastError();
 }
 
+// The debug instance exists for the pairs whose QK^T and PV formats agree and for
+// E2M1 QK^T with EFQ P (the P~ generation depends on the PV format only), with the
+// cubic or the hardware exp2, under the per-query-tile schedule.
+template <int FQK, int FPV>
+constexpr bool kHasDebug = FQK != F_BF16 && (FQK == FPV || (FQK == F_E2M1 && FPV == F_EFQ));
+
 template <int FQK, int FPV, int D, int EXPM>
 static cudaError_t launch_sched(const AttnLaunch& a) {
+  if (a.debug) {
+    if constexpr (kHasDebug<FQK, FPV> && EXPM < 2) return launch_one<FQK, FPV, D, EXPM, true>(a);
+    return cudaErrorNotSupported;
+  }
   return a.persistent ? launch_persistent<FQK, FPV, D, EXPM>(a) : launch_one<FQK, FPV, D, EXPM>(a);
 }
 
 template <int FQK, int FPV>
 cudaError_t launch_attn_impl(const AttnLaunch& a) {
-  constexpr bool efq_or_bf16 = FPV == F_EFQ || FPV == F_BF16;
-  if constexpr (FPV == F_EFQ) {             // EFQ: the exp-mode slot selects the clamp (see pgen_block)
-    if (a.D == 64) return a.p.efq_fast ? launch_sched<FQK, FPV, 64, 1>(a) : launch_sched<FQK, FPV, 64, 0>(a);
-    return a.p.efq_fast ? launch_sched<FQK, FPV, 128, 1>(a) : launch_sched<FQK, FPV, 128, 0>(a);
-  }
+  // EFQ and BF16 have one P path (the exp-mode slot is unused)
+  constexpr bool one_path = FPV == F_EFQ || FPV == F_BF16;
   if (a.D == 64) {
-    if constexpr (efq_or_bf16) return launch_sched<FQK, FPV, 64, 1>(a);
+    if constexpr (one_path) return launch_sched<FQK, FPV, 64, 1>(a);
     else {
       if (a.exp_mode == 0) return launch_sched<FQK, FPV, 64, 0>(a);
       if (a.exp_mode == 1) return launch_sched<FQK, FPV, 64, 1>(a);
       return launch_sched<FQK, FPV, 64, 2>(a);
     }
   }
-  if constexpr (efq_or_bf16) return launch_sched<FQK, FPV, 128, 1>(a);
+  if constexpr (one_path) return launch_sched<FQK, FPV, 128, 1>(a);
   else {
     if (a.exp_mode == 0) return launch_sched<FQK, FPV, 128, 0>(a);
     if (a.exp_mode == 1) return launch_sched<FQK, FPV, 128, 1>(a);

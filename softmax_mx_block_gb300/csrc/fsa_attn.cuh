@@ -99,23 +99,35 @@ struct Cfg {
   static constexpr int NTHREADS = 64 + 32 * NSW;   // warp 0 TMA, warp 1 MMA, then the softmax warps
 };
 
-struct KParams {
+struct KParams {          // kept within 128 bytes: larger parameter blocks measured more spills
   int B, H, Hkv, Sq, Sk, n_qtiles, causal;
   int n_items;            // query tiles over all (batch, head): B * H * n_qtiles
   float c;                // fp32(scale * log2 e)
   float delta;
-  int efq_beta;
-  int efq_fast;           // EFQ codes cannot exceed 8 (beta <= 2, delta <= 120): one-sided clamp
-  uint64_t timeout_ns;
+  // EFQ rule (see pgen_block): A8 = fp32(a c) / 8, a8 = a / 8, b8 = b / 8 (all exact
+  // scalings by 1/8), phi the block scale's reference point
+  float efq_A8, efq_a8, efq_b8, efq_phi;
   const uint8_t* sf_q;    // [B*H][ceil(Sq/128)][512]
   const uint8_t* sf_k;    // [B*Hkv][ceil(Sk/128)][512]
   const uint8_t* sf_v;    // [B*Hkv][Sp/128][512]
-  float* out;             // [B][H][Sq][D]
+  uint64_t timeout_ns;
   int32_t* row_fallbacks; // optional [B][H][Sq]
   unsigned long long* stat_fallbacks;
   unsigned long long* stat_row_tiles;
   int* status;
   int inject_stall;
+  int out_bf16;           // 1: O is written as bf16 (round to nearest even), else fp32
+};
+static_assert(sizeof(KParams) <= 128, "kernel parameter block");
+
+// Dump pointers of the debug instance (fsa_debug_dump): raw scores [slot][nkt*128],
+// M [slot][nkt], P~ words [slot][nkt][32], P~ scale word [slot][nkt]; null otherwise.
+struct DbgParams {
+  float* s;
+  float* m;
+  uint32_t* p;
+  uint32_t* sf;
+  const int32_t* row_slot;   // dump slot of each query row (null: the row itself; < 0: none)
 };
 
 }  // namespace fsa

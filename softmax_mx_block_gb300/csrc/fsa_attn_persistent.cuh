@@ -23,7 +23,8 @@ namespace fsa {
 // A query tile without key tiles gets zeros.
 template <int D, bool MX>
 __device__ __forceinline__ void write_rows(uint32_t t_o, int pp, int qd, int lane, float lb, bool done, bool has_keys,
-                                           uint8_t* stage, const CUtensorMap* tm_o, int q0, int bhq, uint64_t* o_free) {
+                                           uint8_t* stage, const CUtensorMap* tm_o, int q0, int bhq, uint64_t* o_free,
+                                           bool bf16) {
   constexpr int DP = D / 2;
   if (!done && has_keys) {                           // aborted: release O_aug, write nothing
     tc_fence_before();
@@ -65,15 +66,32 @@ __device__ __forceinline__ void write_rows(uint32_t t_o, int pp, int qd, int lan
     }
     if (lane == 0) bulk_wait_read();                 // the previous chunk's store has read the box
     __syncwarp();
+    if (bf16) {
+      // bf16: the same fp32 quotients rounded to nearest even, 32 bytes per row (32B
+      // swizzle: 16-byte chunk ch of row `lane` sits at chunk ch ^ ((lane / 4) % 2))
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      const float4 v = lpos ? make_float4(__fmul_rn(__uint_as_float(o[4 * ch]), rinv),
-                                          __fmul_rn(__uint_as_float(o[4 * ch + 1]), rinv),
-                                          __fmul_rn(__uint_as_float(o[4 * ch + 2]), rinv),
-                                          __fmul_rn(__uint_as_float(o[4 * ch + 3]), rinv))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      // 64B swizzle: 16-byte chunk ch of row `lane` sits at chunk ch ^ ((lane / 2) % 4)
-      *reinterpret_cast<float4*>(stage + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) = v;
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = lpos ? __fmul_rn(__uint_as_float(o[8 * ch + 2 * e]), rinv) : 0.f;
+          const float b = lpos ? __fmul_rn(__uint_as_float(o[8 * ch + 2 * e + 1]), rinv) : 0.f;
+          w[e] = cvt_bf16x2(a, b);
+        }
+        *reinterpret_cast<uint4*>(stage + lane * 32 + ((ch ^ ((lane >> 2) & 1)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const float4 v = lpos ? make_float4(__fmul_rn(__uint_as_float(o[4 * ch]), rinv),
+                                            __fmul_rn(__uint_as_float(o[4 * ch + 1]), rinv),
+                                            __fmul_rn(__uint_as_float(o[4 * ch + 2]), rinv),
+                                            __fmul_rn(__uint_as_float(o[4 * ch + 3]), rinv))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        // 64B swizzle: 16-byte chunk ch of row `lane` sits at chunk ch ^ ((lane / 2) % 4)
+        *reinterpret_cast<float4*>(stage + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) = v;
+      }
     }
     fence_proxy_async_smem();                        // generic writes -> TMA reads
     __syncwarp();
@@ -131,11 +149,12 @@ struct TileState {
 };
 template <int FQK, int FPV, int D, int EXPM>
 __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full, uint64_t* pv_done, volatile float* m_slot,
-                                                AbortCtl ac, float c, float delta, int efq_beta, int pp, int qd,
+                                                AbortCtl ac, const KParams& p, int pp, int qd,
                                                 int lim, int nT, int g0, bool ok) {
   using C = Cfg<FQK, FPV, D, true>;
   constexpr bool MX = C::MX;
   constexpr int NBLK = 4;                         // 32-key blocks per tile
+  const float c = p.c;
   uint64_t* s_free = s_full + 2;
   uint64_t* p_full = s_full + 4;
   const int bar_in = 1 + qd + 4 * pp, bar_out = 1 + qd + 4 * (1 - pp);
@@ -195,7 +214,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
         const float x = __fmul_rn(hm, c);
         if (M == kNegInf) {
           Mn = x;
-        } else if (MX ? (x > __fadd_rn(M, delta)) : (__fsub_rn(x, M) > 8.0f)) {
+        } else if (MX ? (x > __fadd_rn(M, p.delta)) : (__fsub_rn(x, M) > 8.0f)) {
           rescale = true;
           Mn = x;
         }
@@ -225,7 +244,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
             constexpr int WB = C::P_COLS / NBLK;       // words per block: 8, or 4 for E2M1
 #pragma unroll
             for (int b = 0; b < 2; ++b)
-              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, efq_beta, pw + WB * b)
+              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p, pw + WB * b)
                     << (8 * (2 * hf + b));
           } else {
             const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
@@ -661,7 +680,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     if (item_at(r, n_items) < 0) break;
     int lim = p.Sk - 1;
     if (p.causal) lim = min(lim, items[r].q0 + rl + p.Sk - p.Sq);
-    const TileState ts = softmax_tiles<FQK, FPV, D, EXPM>(tl, s_full, pv_done, m_slot, ac, c, p.delta, p.efq_beta, pp, qd,
+    const TileState ts = softmax_tiles<FQK, FPV, D, EXPM>(tl, s_full, pv_done, m_slot, ac, p, pp, qd,
                                                           lim, items[r].nT, g0, ok);
     const Item it = items[r];                       // re-read: not held across the key-tile loop
     const int nT = it.nT;
@@ -690,7 +709,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     const bool done = ok && nT > 0 && (gl < 1 || wait0(pv_done + (gl - 1) % C::NS, ((gl - 1) / C::NS) & 1)) &&
                       wait0(pv_done + gl % C::NS, (gl / C::NS) & 1);
     write_rows<D, MX>(tl + C::T_O, pp, qd, lane, lb, done, nT > 0, sm + C::OFF_OSTAGE + (warp - 2) * 2048, &tm_o,
-                      it.q0, it.bhq, o_free);
+                      it.q0, it.bhq, o_free, p.out_bf16 != 0);
     // ---- statistics: each part counted the key tiles it owns
     int* nfb_other = reinterpret_cast<int*>(red) + 128 + rl;
     if (pp == 1) *nfb_other = nfb;

@@ -42,7 +42,22 @@ def test_sizes_and_status(lib):
         fsa.fsa_mx_sizes(1, 1, 128, 96, 0, "E4M3")
     assert fsa.status_string(fsa.FSA_ERR_TIMEOUT) == "on-chip wait timed out"
     o = fsa.default_opts()
-    assert (o.exp_mode, o.efq_beta, o.timeout_ms, o.delta) == (fsa.FSA_EXP_MUFU, 2, 4000, 8.0)
+    assert (o.exp_mode, o.timeout_ms, o.delta, o.out_dtype) == (fsa.FSA_EXP_MUFU, 4000, 8.0, fsa.FSA_OUT_F32)
+    assert not o.debug
+    assert lib.fsa_version() == 200
+
+
+def test_efq_defaults_match_the_oracle_reading(lib):
+    """The EFQ rule's constants in the library's defaults are the ones the oracle
+    uses (both follow the scan in oracle/efq_scan.py)."""
+    import oracle
+    import softmax_mx_block_gb300 as fsa
+    o = fsa.default_opts()
+    assert (o.efq_a, o.efq_b, o.efq_phi) == (oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI)
+    hdr = open(os.path.join(ROOT, "include", "fsa.h")).read()
+    for name, val in (("A", oracle.EFQ_A), ("B", oracle.EFQ_B), ("PHI", oracle.EFQ_PHI)):
+        m = re.search(rf"#define FSA_EFQ_{name}_DEFAULT\s+([0-9.]+)f", hdr)
+        assert m and float(m.group(1)) == val
 
 
 def test_argument_checks_reject_before_launch(lib):
@@ -127,3 +142,93 @@ def test_binding_checks_mx_buffers(lib):
                 _check_mx_buffers(bad, "t")
         with pytest.raises(fsa.FsaError, match="CUDA tensor"):
             _need_mx(ok, "t", torch.device("cpu"))
+
+
+def _attn_args(fsa, opts):
+    from softmax_mx_block_gb300._binding import fsa_mx_tensor
+    t = fsa_mx_tensor(16, 16, 0, 0, 1, 1, 128, 128)
+    v = fsa_mx_tensor(16, 16, 0, 1, 1, 1, 128, 128)
+    keep = (t, v, opts)
+    return keep, (ctypes.byref(t), ctypes.byref(t), ctypes.byref(v), ctypes.c_void_p(16), 1, 1, 1, 128, 128, 128, 0,
+                  ctypes.c_float(0.125), 0, 0, ctypes.byref(opts), ctypes.c_void_p(0), ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("field,value", [("delta", -1.0), ("delta", float("inf")), ("efq_a", 0.0), ("efq_a", 17.0),
+                                         ("efq_b", 100.0), ("efq_phi", 1.0), ("efq_phi", -0.25), ("out_dtype", 2),
+                                         ("exp_mode", 3), ("schedule", 5)])
+def test_options_out_of_range_are_rejected(lib, field, value):
+    """A negative margin (nearly every tile would fall back), EFQ constants outside
+    their documented range, an unknown output dtype: INVALID_ARG before any launch."""
+    import softmax_mx_block_gb300 as fsa
+    o = fsa.default_opts()
+    setattr(o, field, value)
+    keep, a = _attn_args(fsa, o)
+    assert lib.fsa_attention_fwd_ex(*a) == fsa.FSA_ERR_INVALID_ARG
+
+
+def test_debug_dump_format_checks(lib):
+    """The debug instance exists for matching format pairs (and E2M1 with EFQ) and the
+    POLY / MUFU exp modes only; other requests are refused before any launch."""
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import fsa_debug_dump, fsa_mx_tensor
+    d = fsa_debug_dump(16, 16, 16, 16)
+    o = fsa.default_opts()
+    o.debug = ctypes.pointer(d)
+    t = fsa_mx_tensor(16, 16, 0, 0, 1, 1, 128, 128)
+    v2 = fsa_mx_tensor(16, 16, 2, 1, 1, 1, 128, 128)
+    args = (ctypes.byref(t), ctypes.byref(t), ctypes.byref(v2), ctypes.c_void_p(16), 1, 1, 1, 128, 128, 128, 0,
+            ctypes.c_float(0.125), 0, 2, ctypes.byref(o), ctypes.c_void_p(0), ctypes.c_void_p(0))
+    assert lib.fsa_attention_fwd_ex(*args) == fsa.FSA_ERR_UNSUPPORTED_FMT        # E4M3 QK^T with E2M1 P
+    v0 = fsa_mx_tensor(16, 16, 0, 1, 1, 1, 128, 128)
+    o.exp_mode = fsa.FSA_EXP_SPLIT
+    args = (ctypes.byref(t), ctypes.byref(t), ctypes.byref(v0), ctypes.c_void_p(16), 1, 1, 1, 128, 128, 128, 0,
+            ctypes.c_float(0.125), 0, 0, ctypes.byref(o), ctypes.c_void_p(0), ctypes.c_void_p(0))
+    assert lib.fsa_attention_fwd_ex(*args) == fsa.FSA_ERR_UNSUPPORTED_FMT        # split exp mode
+    d0 = fsa_debug_dump(16, 0, 16, 16)
+    o.debug = ctypes.pointer(d0)
+    o.exp_mode = fsa.FSA_EXP_MUFU
+    assert lib.fsa_attention_fwd_ex(*args) == fsa.FSA_ERR_INVALID_ARG            # a null dump pointer
+
+
+def test_layers_are_checked_before_any_launch(lib):
+    """fsa_attention_fwd_layers checks every layer first: a bad later layer means no
+    launch at all (the first layer's fake device pointers are never touched)."""
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import fsa_layer, fsa_mx_tensor
+    t = fsa_mx_tensor(16, 16, 0, 0, 1, 1, 128, 128)
+    v = fsa_mx_tensor(16, 16, 0, 1, 1, 1, 128, 128)
+    arr = (fsa_layer * 2)()
+    good = fsa_layer(ctypes.pointer(t), ctypes.pointer(t), ctypes.pointer(v), 16, 1, 1, 1, 128, 128, 128, 0, 0.125,
+                     0, 0, 8.0, 0)
+    arr[0] = good
+    arr[1] = fsa_layer(ctypes.pointer(t), ctypes.pointer(t), ctypes.pointer(v), 16, 1, 1, 1, 128, 128, 128, 0, 0.125,
+                       0, 0, -1.0, 0)                                          # negative margin
+    assert lib.fsa_attention_fwd_layers(arr, 2, None, None) == fsa.FSA_ERR_INVALID_ARG
+    arr[1] = fsa_layer(ctypes.pointer(t), ctypes.pointer(t), ctypes.pointer(v), 16, 1, 1, 1, 128, 128, 128, 0, 0.125,
+                       0, 3, 8.0, 0)                                           # P format does not match V
+    assert lib.fsa_attention_fwd_layers(arr, 2, None, None) == fsa.FSA_ERR_UNSUPPORTED_FMT
+    assert lib.fsa_attention_fwd_layers(None, 1, None, None) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_attention_fwd_layers(None, 0, None, None) == fsa.FSA_OK
+
+
+def test_tune_delta_host_logic(lib):
+    """Layers whose fallback rate is above the target get a larger margin (capped);
+    layers without evidence (timeout, no visited tiles) and quiet layers keep theirs."""
+    import softmax_mx_block_gb300 as fsa
+    st = [dict(fallback_events=50, row_tiles=1000, status=0),     # 5% > 1%: raise
+          dict(fallback_events=5, row_tiles=1000, status=0),      # 0.5%: keep
+          dict(fallback_events=900, row_tiles=1000, status=-4),   # timed out: no evidence
+          dict(fallback_events=0, row_tiles=0, status=0),         # nothing visited
+          dict(fallback_events=500, row_tiles=1000, status=0)]    # at the cap
+    assert fsa.fsa_tune_delta(st, [8.0, 8.0, 8.0, 8.0, 62.0], 0.01, 4.0, 64.0) == [12.0, 8.0, 8.0, 8.0, 64.0]
+    with pytest.raises(fsa.FsaError):
+        fsa.fsa_tune_delta(st[:1], [70.0], 0.01, 4.0, 64.0)     # margin above the maximum
+    with pytest.raises(fsa.FsaError):
+        fsa.fsa_tune_delta(st[:1], [8.0], 0.01, 0.0, 64.0)      # no step
+
+
+def test_mma_peak_argument_checks(lib):
+    import softmax_mx_block_gb300 as fsa
+    fl = ctypes.c_double()
+    for kind, n, it in ((3, 1, 1), (-1, 1, 1), (1, 0, 1), (1, 1, 0), (1, 70000, 1)):
+        assert lib.fsa_mma_peak(kind, n, it, None, ctypes.byref(fl), None) == fsa.FSA_ERR_INVALID_ARG

@@ -12,6 +12,11 @@ pytestmark = pytest.mark.gpu
 FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
 SPLIT_MASK = 0x77777777          # key positions 4k+3 use the cubic, the rest the hardware exp2
 TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
+# error vs fp64 exact over the error of exact softmax with the same MX operands (the
+# floor): 1.1 for the exp-then-round paths; for the EFQ direct codes the largest ratio
+# the chosen rule reaches on the parity cases (1.117, small 300-key case at delta 8)
+# plus 5%
+FLOOR_EXP, FLOOR_EFQ = 1.1, 1.17
 
 
 def _fsa():
@@ -57,7 +62,7 @@ def rel_err(a, ref):
     return np.linalg.norm(a - ref) / np.linalg.norm(ref)
 
 
-def check(w, gpu, orc, rows, floor_ratio=1.1):
+def check(w, gpu, orc, rows, floor_ratio=FLOOR_EXP):
     o = gpu["out"][rows]
     emu = orc["emu"]
     rms = np.sqrt(np.mean(emu ** 2))
@@ -93,7 +98,7 @@ def test_small_formats(fq, fp, D, causal):
     rows = sample_rows(w)
     gpu = run_mx(w, q, k, v, row_fb=True)
     orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK)
-    ratio = 2.0 if fp == "E2M1_EFQ" else 1.1
+    ratio = FLOOR_EFQ if fp == "E2M1_EFQ" else FLOOR_EXP
     check(w, gpu, orc, rows, ratio)
     assert np.array_equal(gpu["row_fallbacks"][rows], orc["fallbacks"])
 
@@ -205,24 +210,31 @@ def test_bf16_transpose_v():
     assert not got[..., 200:].any()
 
 
-@pytest.mark.parametrize("beta,delta", [(2, 8.0), (0, 8.0), (-3, 8.0), (2, 120.0), (3, 8.0), (5, 50.0), (2, 200.0)])
-def test_efq_offset_and_margin(beta, delta):
-    """EFQ codes rne(2 r + beta) clamped to [0, 7], for offsets and fallback margins on
-    both sides of the kernel's one-sided-clamp condition (beta <= 2, delta <= 120),
-    on inputs with planted keys that lift late tiles far above the frozen maximum."""
-    w = Workload("efq_beta", 1, 4, 2, 512, 1024, 128, False, "E2M1", "E2M1_EFQ", 11, "planted")
+EFQ_RULES = [(oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI, 8.0), (oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI, 0.0),
+             (2.0, 2.0, 0.0, 8.0), (2.0, -3.0, 0.0, 8.0), (1.5, 3.0, 0.75, 120.0), (3.0, 5.5, 0.25, 50.0),
+             (2.0, 2.0, 0.0, 200.0)]
+
+
+@pytest.mark.parametrize("a,b,phi,delta", EFQ_RULES)
+def test_efq_rule_constants_and_margin(a, b, phi, delta):
+    """EFQ codes clamp(rne(a r + b), 0, 7) under E = floor(tmax + phi) - 2, for the
+    library's constants and others (codes clamped at either end, large fallback
+    margins that leave the block exponent far above the frozen maximum), on inputs with
+    planted keys that lift late tiles far above it."""
+    w = Workload("efq_rule", 1, 4, 2, 512, 1024, 128, False, "E2M1", "E2M1_EFQ", 11, "planted")
     q, k, v = generate(w)
     rows = sample_rows(w, per_head=128)
-    gpu = run_mx(w, q, k, v, exp_mode=None, delta=delta, efq_beta=beta)
+    gpu = run_mx(w, q, k, v, exp_mode=None, delta=delta, efq_a=a, efq_b=b, efq_phi=phi)
     assert gpu["stats"]["status"] == 0
     mx = oracle.MxInputs.from_bf16(q, k, v, FMT[w.fmt_qk], 2)
-    orc = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, 3, rows, delta=delta, beta=beta, ambiguity=True)
+    orc = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, 3, rows, delta=delta, beta=b, efq_a=a, phi=phi,
+                             ambiguity=True)
     emu, amb = orc["out"], orc["amb"]
     undetermined = np.isinf(amb).any(axis=1)
     assert np.mean(undetermined) < 0.01
     tol = TOL_EMU * np.sqrt(np.mean(emu ** 2))
     excess = (np.abs(gpu["out"][rows] - emu) - amb - tol)[~undetermined]
-    assert np.all(excess <= 0.0), f"beta {beta} delta {delta}: exceeds by {excess.max():.3e}"
+    assert np.all(excess <= 0.0), f"rule {(a, b, phi)} delta {delta}: exceeds by {excess.max():.3e}"
 
 
 SCHED_CASES = [

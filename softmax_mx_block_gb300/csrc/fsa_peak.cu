@@ -25,7 +25,10 @@ namespace {
 constexpr int kPeakThreads = 128;
 constexpr int kTileBytes = 128 * 256;       // up to 256 bytes per row (bf16, K = 128)
 constexpr int kOffA = 0, kOffB = kTileBytes, kOffSF = 2 * kTileBytes, kOffBar = kOffSF + 1024;
-constexpr int kPeakSmem = kOffBar + 64 + 1024;
+// more shared memory than two CTAs could share, so that each CTA (and its 512
+// tensor-memory columns) has an SM to itself
+constexpr int kPeakSmem = 120 * 1024;
+static_assert(kOffBar + 64 + 1024 <= kPeakSmem, "shared memory");
 
 template <int KIND>
 __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long iters, int* status,

@@ -247,6 +247,18 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
                          int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
                          int fmt_qk, int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream);
 
+/* As fsa_attention_fwd_ex, with Q given as bf16 [B][H][Sq][D] (device, 16-byte
+ * aligned) and quantised to fmt_qk inside the attention kernel's prologue, so Q
+ * makes no round trip through HBM as MX codes (the Fused-Softmax brief, abstract:
+ * MX operands of the attention GEMMs; the codes and scales are those of
+ * fsa_mx_quantize, so the output is bit-identical to quantising Q first).  Runs
+ * one CTA per query tile with the hardware exp2 (or EFQ P codes): a request for
+ * the persistent schedule, another exp mode or a debug dump returns
+ * FSA_ERR_UNSUPPORTED_FMT.  Other errors as fsa_attention_fwd_ex. */
+int fsa_attention_fwd_qbf16(const void* q_bf16, const fsa_mx_tensor* k, const fsa_mx_tensor* v, void* out,
+                            int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale,
+                            int fmt_qk, int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream);
+
 /* Rearrange V [B][Hkv][S][D] bf16 into V^T [B][Hkv][D][Sp] bf16 (Sp = S
  * rounded up to 128, zero padded) for the BF16 kernel. */
 int fsa_bf16_transpose_v(const void* v, void* vt, int B, int Hkv, int S, int D, void* stream);
@@ -301,15 +313,15 @@ int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, floa
 /* ------------------------------------------------------ tensor-core peak probe */
 /* Measurement instrument (the roofline denominator of the attention kernels; the
  * Fused-Softmax brief, abstract, quotes its kernels' throughput on the block-
- * scaled matrix cores).  Launches n_ctas CTAs (one per SM is the intent) that
- * each issue `iters` iterations of dense M=128, N=128, K=128 products from
+ * scaled matrix cores).  Launches n_ctas CTAs (one per SM) that each issue
+ * `iters` iterations of dense M=128, N=n (128 or 256), K=128 products from
  * shared-memory operand tiles into tensor memory, as 8 kind::f16 bf16 MMAs
  * (kind 0), 4 kind::mxf8f6f4 E4M3 block-scaled MMAs (kind 1) or 2 kind::mxf4
  * E2M1 block-scaled MMAs (kind 2).  *flops (host, optional) receives the
  * launch's 2*M*N*K*iters*n_ctas; time the launch with events on `stream`.
  * status: optional device int32, set to FSA_ERR_TIMEOUT if the final wait
  * (2 s) expires.  Errors: FSA_ERR_INVALID_ARG, FSA_ERR_LAUNCH. */
-int fsa_mma_peak(int kind, int n_ctas, long long iters, int32_t* status, double* flops, void* stream);
+int fsa_mma_peak(int kind, int n, int n_ctas, long long iters, int32_t* status, double* flops, void* stream);
 
 const char* fsa_status_string(int status);
 int fsa_version(void);

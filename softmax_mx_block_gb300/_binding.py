@@ -92,8 +92,10 @@ def load(build_if_missing: bool = True):
             L.fsa_attention_fwd_ex.argtypes = [ctypes.POINTER(fsa_mx_tensor)] * 3 + \
                 [vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, vp]
             L.fsa_attention_fwd_layers.argtypes = [ctypes.POINTER(fsa_layer), i, ctypes.POINTER(fsa_opts), vp]
+            L.fsa_attention_fwd_qbf16.argtypes = [vp] + [ctypes.POINTER(fsa_mx_tensor)] * 2 + \
+                [vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, vp]
             L.fsa_tune_delta.argtypes = [ctypes.POINTER(fsa_stats), i, f, f, f, ctypes.POINTER(ctypes.c_float)]
-            L.fsa_mma_peak.argtypes = [i, i, ctypes.c_longlong, vp, ctypes.POINTER(ctypes.c_double), vp]
+            L.fsa_mma_peak.argtypes = [i, i, i, ctypes.c_longlong, vp, ctypes.POINTER(ctypes.c_double), vp]
             L.fsa_bf16_transpose_v.argtypes = [vp, vp, i, i, i, i, vp]
             L.fsa_attention_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp]
             L.fsa_default_opts.argtypes = [ctypes.POINTER(fsa_opts)]
@@ -102,7 +104,7 @@ def load(build_if_missing: bool = True):
             L.fsa_status_string.restype = ctypes.c_char_p
             for n in ("fsa_mx_sizes", "fsa_mx_quantize", "fsa_mx_quantize_qkv", "fsa_attention_fwd",
                       "fsa_attention_fwd_ex", "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version",
-                      "fsa_attention_fwd_layers", "fsa_tune_delta", "fsa_mma_peak"):
+                      "fsa_attention_fwd_layers", "fsa_tune_delta", "fsa_mma_peak", "fsa_attention_fwd_qbf16"):
                 getattr(L, n).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -301,13 +303,22 @@ class DebugDump:
                               self.row_slot.data_ptr() if self.row_slot is not None else 0)
 
 
-def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
+def fsa_attention_fwd(q, k: MxTensor, v: MxTensor, out: torch.Tensor | None = None, *, Hkv=None,
                       causal=False, scale=None, fmt_qk=None, fmt_pv=None, delta=None, exp_mode=None,
                       efq_a=None, efq_b=None, efq_phi=None, timeout_ms=0,
                       row_fallbacks: torch.Tensor | None = None, stats=None, inject_stall=False, schedule=None,
                       out_dtype=None, debug: DebugDump | None = None, stream=None) -> torch.Tensor:
-    """O [B,H,Sq,D] (fp32, or bf16 with out_dtype="bf16") by the fused MX forward (fsa_attention_fwd_ex)."""
-    B, H, Sq, D = q.B, q.H, q.S, q.D
+    """O [B,H,Sq,D] (fp32, or bf16 with out_dtype="bf16") by the fused MX forward.  q is an
+    MxTensor (fsa_attention_fwd_ex) or a bf16 [B,H,Sq,D] CUDA tensor, quantised to fmt_qk
+    in the kernel's prologue (fsa_attention_fwd_qbf16)."""
+    q_raw = isinstance(q, torch.Tensor)
+    if q_raw:
+        _need_cuda(q, "q", torch.bfloat16)
+        B, H, Sq, D = q.shape
+        if fmt_qk is None:
+            raise FsaError(FSA_ERR_INVALID_ARG, "a bf16 q needs fmt_qk")
+    else:
+        B, H, Sq, D = q.B, q.H, q.S, q.D
     Hkv = k.H if Hkv is None else Hkv
     Sk = k.S
     scale = D ** -0.5 if scale is None else scale
@@ -315,12 +326,14 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
     fmt_pv = v.fmt if fmt_pv is None else _fmt(fmt_pv)
     od, tdt = _out_dtype(out_dtype if out is None or out_dtype is not None else out.dtype)
     if out is None:
-        out = torch.empty((B, H, Sq, D), dtype=tdt, device=q.codes.device)
+        out = torch.empty((B, H, Sq, D), dtype=tdt, device=k.codes.device)
     _need_cuda(out, "out", tdt)
     if out.numel() < B * H * Sq * D:
         raise FsaError(FSA_ERR_INVALID_ARG, "out is smaller than B*H*Sq*D")
-    for m, n in ((q, "q"), (k, "k"), (v, "v")):
+    for m, n in (((k, "k"), (v, "v")) if q_raw else ((q, "q"), (k, "k"), (v, "v"))):
         _need_mx(m, n, out.device)
+    if q_raw and q.device != out.device:
+        raise FsaError(FSA_ERR_INVALID_ARG, f"q is on {q.device}, the call on {out.device}")
     if stats is not None:
         _need_cuda(stats, "stats")
         if stats.device != out.device or stats.numel() * stats.element_size() < STATS_BYTES:
@@ -345,12 +358,16 @@ def fsa_attention_fwd(q: MxTensor, k: MxTensor, v: MxTensor, out: torch.Tensor |
             raise FsaError(FSA_ERR_INVALID_ARG, "debug.row_slot must hold B*H*Sq slots on the output's device")
         dd = debug.struct()
         o.debug = ctypes.pointer(dd)
-    qs, ks, vs = q.struct(), k.struct(), v.struct()
-    _check(load().fsa_attention_fwd_ex(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs),
-                                       ctypes.c_void_p(out.data_ptr()), B, H, Hkv, Sq, Sk, D, int(bool(causal)),
-                                       float(scale), fmt_qk, fmt_pv, ctypes.byref(o),
-                                       ctypes.c_void_p(stats.data_ptr() if stats is not None else 0),
-                                       _stream(stream)), "fsa_attention_fwd_ex")
+    ks, vs = k.struct(), v.struct()
+    tail = (ctypes.c_void_p(out.data_ptr()), B, H, Hkv, Sq, Sk, D, int(bool(causal)), float(scale), fmt_qk, fmt_pv,
+            ctypes.byref(o), ctypes.c_void_p(stats.data_ptr() if stats is not None else 0), _stream(stream))
+    if q_raw:
+        _check(load().fsa_attention_fwd_qbf16(ctypes.c_void_p(q.data_ptr()), ctypes.byref(ks), ctypes.byref(vs),
+                                              *tail), "fsa_attention_fwd_qbf16")
+    else:
+        qs = q.struct()
+        _check(load().fsa_attention_fwd_ex(ctypes.byref(qs), ctypes.byref(ks), ctypes.byref(vs), *tail),
+               "fsa_attention_fwd_ex")
     return out
 
 
@@ -402,14 +419,16 @@ def fsa_tune_delta(stats: list, deltas: list, target_rate=0.01, step=4.0, max_de
     return [float(d[i]) for i in range(n)]
 
 
-def fsa_mma_peak(kind: int, n_ctas: int, iters: int, status: torch.Tensor | None = None, stream=None) -> float:
-    """Launch the tensor-core throughput probe; returns the launch's FLOPs (time it with events)."""
+def fsa_mma_peak(kind: int, n_ctas: int, iters: int, status: torch.Tensor | None = None, n: int = 128,
+                 stream=None) -> float:
+    """Launch the tensor-core throughput probe (M=128, N=n); returns the launch's FLOPs
+    (time it with events)."""
     fl = ctypes.c_double()
     ptr = 0
     if status is not None:
         _need_cuda(status, "status", torch.int32)
         ptr = status.data_ptr()
-    _check(load().fsa_mma_peak(int(kind), int(n_ctas), int(iters), ctypes.c_void_p(ptr), ctypes.byref(fl),
+    _check(load().fsa_mma_peak(int(kind), int(n), int(n_ctas), int(iters), ctypes.c_void_p(ptr), ctypes.byref(fl),
                                _stream(stream)), "fsa_mma_peak")
     return fl.value
 

@@ -99,6 +99,16 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+// 3-D byte tensor loaded unswizzled: box {inner bytes (<= 256), box_rows, 1}.
+bool make_tmap_plain(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t planes,
+                     uint32_t box_rows) {
+  const uint64_t dims[3] = {inner, rows, planes};
+  const uint64_t strides[2] = {inner, inner * rows};
+  const uint32_t box[3] = {(uint32_t)inner, box_rows, 1};
+  return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 // Output O [planes][rows][D], written by TMA stores from the epilogue.
 //   one CTA per query tile: fp32 boxes of 32 rows x 32 floats (128B swizzle); bf16
 //     boxes of 32 rows x D/2 values (128B swizzle for D = 128, 64B for D = 64)
@@ -294,21 +304,29 @@ int fsa_bf16_transpose_v(const void* v, void* vt, int B, int Hkv, int S, int D, 
   return launch_status(fsa::launch_transpose_v(v, vt, B * Hkv, S, D, static_cast<cudaStream_t>(stream)));
 }
 
-int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, void* out,
-                         int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale, int fmt_qk,
-                         int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream) {
-  if (!q || !k || !v || !out) return FSA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Both attention entry points: q (MX) or q_bf16 (bf16 [B][H][Sq][D], quantised in the
+// kernel's prologue into fmt_qk) -- exactly one of them is non-null.
+int attention_impl(const fsa_mx_tensor* q, const void* q_bf16, const fsa_mx_tensor* k, const fsa_mx_tensor* v,
+                   void* out, int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale, int fmt_qk,
+                   int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream) {
+  if (!(q || q_bf16) || !k || !v || !out) return FSA_ERR_INVALID_ARG;
   if (!shape_ok(B, H, Hkv, Sq, Sk, D) || !(scale > 0.0f) || !std::isfinite(scale)) return FSA_ERR_INVALID_ARG;
   if (!valid_fmt(fmt_qk) || fmt_pv < FSA_FMT_E4M3 || fmt_pv > FSA_FMT_E2M1_EFQ) return FSA_ERR_UNSUPPORTED_FMT;
   const int fv = storage_fmt(fmt_pv);
   // operand descriptors must match the call
-  if (q->layout != FSA_MX_ROWS || k->layout != FSA_MX_ROWS || v->layout != FSA_MX_COLS_T) return FSA_ERR_INVALID_ARG;
-  if (q->fmt != fmt_qk || k->fmt != fmt_qk || v->fmt != fv) return FSA_ERR_UNSUPPORTED_FMT;
-  if (q->B != B || q->H != H || q->S != Sq || q->D != D || k->B != B || k->H != Hkv || k->S != Sk || k->D != D ||
-      v->B != B || v->H != Hkv || v->S != Sk || v->D != D)
+  if (q && q->layout != FSA_MX_ROWS) return FSA_ERR_INVALID_ARG;
+  if (k->layout != FSA_MX_ROWS || v->layout != FSA_MX_COLS_T) return FSA_ERR_INVALID_ARG;
+  if ((q && q->fmt != fmt_qk) || k->fmt != fmt_qk || v->fmt != fv) return FSA_ERR_UNSUPPORTED_FMT;
+  if ((q && (q->B != B || q->H != H || q->S != Sq || q->D != D)) || k->B != B || k->H != Hkv || k->S != Sk ||
+      k->D != D || v->B != B || v->H != Hkv || v->S != Sk || v->D != D)
     return FSA_ERR_INVALID_ARG;
-  if (!aligned16(q->codes) || !aligned16(k->codes) || !aligned16(v->codes) || !aligned16(q->scales) ||
-      !aligned16(k->scales) || !aligned16(v->scales) || !aligned16(out))
+  if ((q && (!aligned16(q->codes) || !aligned16(q->scales))) || (q_bf16 && !aligned16(q_bf16)) ||
+      !aligned16(k->codes) || !aligned16(v->codes) || !aligned16(k->scales) || !aligned16(v->scales) ||
+      !aligned16(out))
     return FSA_ERR_INVALID_ARG;
   fsa_opts o;
   fsa_default_opts(&o);
@@ -325,7 +343,11 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
   if (dbg && !(fmt_qk == storage_fmt(fmt_pv) || (fmt_qk == FSA_FMT_E2M1 && fmt_pv == FSA_FMT_E2M1_EFQ)))
     return FSA_ERR_UNSUPPORTED_FMT;
   if (dbg && fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode == FSA_EXP_SPLIT) return FSA_ERR_UNSUPPORTED_FMT;
-  const bool persistent = !dbg && persistent_schedule(o.schedule, Sq, Sk, causal);
+  // Q quantised in the prologue: one CTA per query tile, the hardware exp2 (or EFQ)
+  if (q_bf16 && (dbg || o.schedule == FSA_SCHED_PERSISTENT ||
+                 (fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode != FSA_EXP_MUFU)))
+    return FSA_ERR_UNSUPPORTED_FMT;
+  const bool persistent = !dbg && !q_bf16 && persistent_schedule(o.schedule, Sq, Sk, causal);
   const bool bf16 = o.out_dtype == FSA_OUT_BF16;
 
   AttnLaunch a;
@@ -336,13 +358,15 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
   const uint64_t rbv_total = Sp * bits2_of(fv) / 16;
   const int rbv_tile = 128 * bits2_of(fv) / 16;
   const uint32_t wv = rbv_tile < 128 ? rbv_tile : 128;
-  if (!make_tmap(&a.tq, q->codes, rbq, Sq, (uint64_t)B * H, wq, 128) ||
-      !make_tmap(&a.tk, k->codes, rbq, Sk, (uint64_t)B * Hkv, wq, 128) ||
+  const bool tq_ok = q ? make_tmap(&a.tq, q->codes, rbq, Sq, (uint64_t)B * H, wq, 128)
+                      : make_tmap_plain(&a.tq, q_bf16, (uint64_t)2 * D, Sq, (uint64_t)B * H, 128);
+  if (!tq_ok || !make_tmap(&a.tk, k->codes, rbq, Sk, (uint64_t)B * Hkv, wq, 128) ||
       !make_tmap(&a.tv, v->codes, rbv_total, D, (uint64_t)B * Hkv, wv, D) ||
       !make_tmap_out(&a.to, out, D, Sq, (uint64_t)B * H, persistent, bf16))
     return FSA_ERR_LAUNCH;
   fill_common(a.p, B, H, Hkv, Sq, Sk, causal, scale, &o, stats);
-  a.p.sf_q = q->scales; a.p.sf_k = k->scales; a.p.sf_v = v->scales;
+  a.p.sf_q = q ? q->scales : nullptr; a.p.sf_k = k->scales; a.p.sf_v = v->scales;
+  a.q_fused = q ? 0 : 1;
   if (dbg) {
     a.dbg.s = dbg->s; a.dbg.m = dbg->m; a.dbg.p = dbg->p; a.dbg.sf = dbg->p_scales; a.dbg.row_slot = dbg->row_slot;
     a.debug = 1;
@@ -354,6 +378,26 @@ int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const f
   const cudaError_t e = impl_for(fmt_qk, fmt_pv)(a);
   if (e == cudaErrorNotSupported) return FSA_ERR_UNSUPPORTED_FMT;
   return launch_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fsa_attention_fwd_ex(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, void* out,
+                         int B, int H, int Hkv, int Sq, int Sk, int D, int causal, float scale, int fmt_qk,
+                         int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream) {
+  if (!q) return FSA_ERR_INVALID_ARG;
+  return attention_impl(q, nullptr, k, v, out, B, H, Hkv, Sq, Sk, D, causal, scale, fmt_qk, fmt_pv, opts, stats,
+                        stream);
+}
+
+int fsa_attention_fwd_qbf16(const void* q_bf16, const fsa_mx_tensor* k, const fsa_mx_tensor* v, void* out, int B,
+                            int H, int Hkv, int Sq, int Sk, int D, int causal, float scale, int fmt_qk, int fmt_pv,
+                            const fsa_opts* opts, fsa_stats* stats, void* stream) {
+  if (!q_bf16) return FSA_ERR_INVALID_ARG;
+  return attention_impl(nullptr, q_bf16, k, v, out, B, H, Hkv, Sq, Sk, D, causal, scale, fmt_qk, fmt_pv, opts, stats,
+                        stream);
 }
 
 int fsa_attention_fwd(const fsa_mx_tensor* q, const fsa_mx_tensor* k, const fsa_mx_tensor* v, float* out, int B,
@@ -431,11 +475,12 @@ int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, floa
   return FSA_OK;
 }
 
-int fsa_mma_peak(int kind, int n_ctas, long long iters, int32_t* status, double* flops, void* stream) {
-  if (kind < 0 || kind > 2 || n_ctas <= 0 || n_ctas > 65535 || iters <= 0 || iters > (1ll << 40))
+int fsa_mma_peak(int kind, int n, int n_ctas, long long iters, int32_t* status, double* flops, void* stream) {
+  if (kind < 0 || kind > 2 || (n != 128 && n != 256) || n_ctas <= 0 || n_ctas > 65535 || iters <= 0 ||
+      iters > (1ll << 40))
     return FSA_ERR_INVALID_ARG;
-  if (flops) *flops = fsa::mma_peak_flops_per_iter(kind) * (double)iters * (double)n_ctas;
-  return launch_status(fsa::launch_mma_peak(kind, n_ctas, iters, status, 2000000000ull,
+  if (flops) *flops = fsa::mma_peak_flops_per_iter(kind, n) * (double)iters * (double)n_ctas;
+  return launch_status(fsa::launch_mma_peak(kind, n, n_ctas, iters, status, 2000000000ull,
                                             static_cast<cudaStream_t>(stream)));
 }
 

@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "fsa_launch.h"
+#include "fsa_mx.cuh"
 
 namespace fsa {
 
@@ -237,14 +238,58 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
 
 namespace fsa {
 
+// Q quantised in the prologue: thread u of the 256 softmax threads takes row u % 128
+// and half u / 128 of the bf16 tile `raw` (128 rows x 2D bytes), quantises its
+// 32-element blocks exactly as the quantisation kernel does (quant_block32), and
+// writes the codes into the MMA's K-major swizzled Q tile and the scale bytes into
+// the tile's 128x4 scale atom (unused slots 0x7F).  Rows past Sq arrive as zeros.
+template <int FQK, int D>
+__device__ __forceinline__ void quantize_q_tile(const uint8_t* raw, uint8_t* sQ, uint8_t* sfq, int u) {
+  using C = Cfg<FQK, FQK == F_E2M1 ? F_E2M1 : FQK, D>;
+  constexpr int W = C::W_QK;
+  constexpr int NB = D / 64;                       // blocks per thread
+  constexpr int BB = FQK == F_E2M1 ? 16 : 32;      // code bytes per block
+  const int r = u & 127, hf = u >> 7;
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    const int blk = hf * NB + i;
+    const uint4* src = reinterpret_cast<const uint4*>(raw + r * (2 * D) + blk * 64);
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x = src[c];
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * c + 2 * e] = bf16_to_f32((uint16_t)(xs[e] & 0xFFFFu));
+        v[8 * c + 2 * e + 1] = bf16_to_f32((uint16_t)(xs[e] >> 16));
+      }
+    }
+    uint32_t w[8];
+    const uint32_t sb = quant_block32<FQK>(v, w);
+#pragma unroll
+    for (int cc = 0; cc < BB / 16; ++cc) {
+      const int o = blk * BB + 16 * cc;            // byte offset within the row
+      const int ka = o / W, c = (o % W) / 16;
+      const int sc = W == 128 ? (c ^ (r & 7)) : (W == 64 ? (c ^ ((r >> 1) & 3)) : (c ^ ((r >> 2) & 1)));
+      *reinterpret_cast<uint4*>(sQ + ka * 128 * W + r * W + (sc << 4)) =
+          make_uint4(w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+    }
+    sfq[(r & 31) * 16 + (r >> 5) * 4 + blk] = (uint8_t)sb;
+    if constexpr (D == 64) sfq[(r & 31) * 16 + (r >> 5) * 4 + blk + 2] = 0x7F;
+  }
+}
+
 // DBG: the debug instance, which also writes each tile's raw scores, its frozen
 // maximum and its P~ code and scale words to the dump buffers of KParams (tests).
-template <int FQK, int FPV, int D, int EXPM, bool DBG = false>
+// QF: Q is given as bf16 (tm_q maps it) and quantised by the softmax warps in the
+// prologue, so it makes no round trip through HBM as MX codes.
+template <int FQK, int FPV, int D, int EXPM, bool DBG = false, bool QF = false>
 __global__ void __launch_bounds__(Cfg<FQK, FPV, D>::NTHREADS, 1)
 fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                 const KParams p, const DbgParams dbg) {
-  using C = Cfg<FQK, FPV, D>;
+  using C = Cfg<FQK, FPV, D, false, QF>;
   constexpr int KIND_QK = Fmt<FQK>::kind, KIND_PV = Fmt<FPV>::kind;
   constexpr bool MX = C::MX;
   extern __shared__ uint8_t smem_raw[];
@@ -283,12 +328,14 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* p_full = s_full + 4;
   uint64_t* drain = s_full + 6;
   uint64_t* stall = s_full + 7;
+  uint64_t* qraw_full = s_full + 8;             // QF: the bf16 Q tile landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, QF ? 8 : 1);                // QF: one arrival per softmax warp
+    if constexpr (QF) mbar_init(qraw_full, 1);
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(k_full + i, 1); mbar_init(v_full + i, 1); mbar_init(pv_done + i, 1); mbar_init(k_empty + i, 1);
     }
@@ -303,11 +350,16 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (nT > 0) {
       // the first loads overlap the rest of the setup (tensor memory, constant rows)
       const int bhq = b * p.H + h, bhk = b * p.Hkv + kvh;
-      mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
+      if constexpr (QF) {
+        mbar_expect_tx(qraw_full, 128 * D * 2);
+        tma_load_3d(sm + C::OFF_QRAW, &tm_q, qraw_full, 0, q0, bhq);
+      } else {
+        mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
 #pragma unroll
-      for (int ka = 0; ka < C::NKA_QK; ++ka)
-        tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
-      if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
+        for (int ka = 0; ka < C::NKA_QK; ++ka)
+          tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
+        if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
+      }
       for (int j = 0; j < C::NS && j < nT; ++j) {
         mbar_expect_tx(k_full + j, C::TILE_QK + (MX ? 512 : 0));
 #pragma unroll
@@ -381,7 +433,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (MX) bulk_load(sm + C::OFF_SFK + st * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + st);
           ++nk;
         }
-        mbar_wait_drain(q_full, 0, p.timeout_ns);
+        mbar_wait_drain(QF ? qraw_full : q_full, 0, p.timeout_ns);
         for (int st = 0; st < C::NS && st < nk; ++st)
           mbar_wait_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, p.timeout_ns);
       } else {
@@ -575,6 +627,19 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
       return __all_sync(0xffffffffu, mbar_wait<false>(bar, parity, ac));
     };
+    if constexpr (QF) {
+      // the bf16 Q tile -> MX codes and scale atom, then the MMA warp may read them
+      if (nT > 0) {
+        if (wait0(qraw_full, 0)) {
+          quantize_q_tile<FQK, D>(sm + C::OFF_QRAW, sQ, sm + C::OFF_SFQ, (int)threadIdx.x - 64);
+          fence_proxy_async_smem();
+          __syncwarp();
+          mbar_arrive_elect(q_full);
+        } else {
+          ok = false;
+        }
+      }
+    }
     for (int j = pp; j < nT; j += 2) {
       const int s = pp;
       const bool got = ok && wait0(s_full + s, (j >> 1) & 1);
@@ -863,12 +928,12 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 namespace fsa {
 
 // ----------------------------------------------------------------------------- host launch
-template <int FQK, int FPV, int D, int EXPM, bool DBG = false>
+template <int FQK, int FPV, int D, int EXPM, bool DBG = false, bool QF = false>
 static cudaError_t launch_one(const AttnLaunch& a) {
-  using C = Cfg<FQK, FPV, D>;
+  using C = Cfg<FQK, FPV, D, false, QF>;
   // at least 116 KB so that one CTA (and its 512 tensor-memory columns) owns an SM
   constexpr int smem = (C::SMEM > 116 * 1024 ? C::SMEM : 116 * 1024);
-  auto kern = fsa_attn_kernel<FQK, FPV, D, EXPM, DBG>;
+  auto kern = fsa_attn_kernel<FQK, FPV, D, EXPM, DBG, QF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid = a.p.causal ? dim3(a.p.H * a.p.B, a.p.n_qtiles, 1) : dim3(a.p.n_qtiles, a.p.H, a.p.B);
@@ -906,6 +971,12 @@ template <int FQK, int FPV, int D, int EXPM>
 static cudaError_t launch_sched(const AttnLaunch& a) {
   if (a.debug) {
     if constexpr (kHasDebug<FQK, FPV> && EXPM < 2) return launch_one<FQK, FPV, D, EXPM, true>(a);
+    return cudaErrorNotSupported;
+  }
+  // Q quantised in the prologue: the library's default exp2 path (and EFQ), one CTA
+  // per query tile
+  if (a.q_fused) {
+    if constexpr (EXPM == 1 && FQK != F_BF16) return launch_one<FQK, FPV, D, EXPM, false, true>(a);
     return cudaErrorNotSupported;
   }
   return a.persistent ? launch_persistent<FQK, FPV, D, EXPM>(a) : launch_one<FQK, FPV, D, EXPM>(a);

@@ -23,7 +23,9 @@ __host__ __device__ constexpr int swz_code(int width) { return width == 128 ? 2 
 
 // PERSIST: the persistent schedule (one CTA per SM walking a list of query tiles),
 // which adds a second Q buffer, an output staging area and the list.
-template <int FQK, int FPV, int D_, bool PERSIST = false>
+// QF: Q arrives as bf16 and is quantised in the kernel's prologue, which adds a
+// staging area for the bf16 tile and its barrier (one CTA per query tile only).
+template <int FQK, int FPV, int D_, bool PERSIST = false, bool QF = false>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int BM = 128, BN = 128;
@@ -71,7 +73,8 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_RED + (256 + 4 * 128) * 4;
   // q full (+ q empty x2 when persistent), k/v full, pv done, k empty x NS, s full/free,
   // p full x2, (o free,) drain, stall
-  static constexpr int NBAR = PERSIST ? 4 + 4 * NS + 3 * 2 + 3 : 1 + 4 * NS + 3 * 2 + 2;
+  static_assert(!(PERSIST && QF), "Q quantised in the prologue: one CTA per query tile");
+  static constexpr int NBAR = PERSIST ? 4 + 4 * NS + 3 * 2 + 3 : 1 + 4 * NS + 3 * 2 + 2 + (QF ? 1 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
   // output staging: one CTA per query tile stages O (128 rows x D fp32, 32x32 boxes)
   // in the K/V ring, free by then; the persistent schedule has one 32-row x 16-column
@@ -81,7 +84,10 @@ struct Cfg {
   // persistent: the CTA's query tiles in processing order (at most MAX_ITEMS)
   static constexpr int MAX_ITEMS = 256;
   static constexpr int OFF_ITEMS = OFF_OSTAGE + NSW * 2048;
-  static constexpr int SMEM = PERSIST ? OFF_ITEMS + MAX_ITEMS * 16 + 1024 : OFF_MISC + 64 + 1024;   // + alignment slack
+  // QF: the bf16 Q tile, 128 rows x 2D bytes, unswizzled
+  static constexpr int OFF_QRAW = (OFF_MISC + 64 + 1023) / 1024 * 1024;
+  static constexpr int SMEM = PERSIST ? OFF_ITEMS + MAX_ITEMS * 16 + 1024
+                                      : (QF ? OFF_QRAW + 128 * D * 2 : OFF_MISC + 64) + 1024;   // + alignment slack
   static_assert(SMEM <= 227 * 1024, "shared memory");
   // ---- tensor memory columns
   static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256)

@@ -13,7 +13,8 @@ struct AttnLaunch {
   int D;
   int exp_mode;          // 0 poly, 1 MUFU, 2 split (ignored for EFQ and BF16)
   int persistent;        // 1: the persistent schedule (tq..to built for it), 0: one CTA per query tile
-  int debug;             // 1: the debug instance (per-tile dumps into KParams::dbg_*)
+  int debug;             // 1: the debug instance (per-tile dumps into dbg)
+  int q_fused;           // 1: tq maps bf16 Q, quantised in the kernel's prologue
   cudaStream_t stream;
 };
 
@@ -32,7 +33,8 @@ cudaError_t launch_mx_quant_qkv(const void* q, const void* k, const void* v, int
 cudaError_t launch_transpose_v(const void* v, void* vt, int BH, int S, int D, cudaStream_t st);
 
 // Tensor-core throughput probe (fsa_peak.cu): kind 0 bf16, 1 MXFP8 E4M3, 2 MXFP4 E2M1.
-double mma_peak_flops_per_iter(int kind);
-cudaError_t launch_mma_peak(int kind, int n_ctas, long long iters, int* status, uint64_t timeout_ns, cudaStream_t st);
+double mma_peak_flops_per_iter(int kind, int n);
+cudaError_t launch_mma_peak(int kind, int n, int n_ctas, long long iters, int* status, uint64_t timeout_ns,
+                            cudaStream_t st);
 
 }  // namespace fsa

@@ -5,9 +5,10 @@
 // throughputs against the block-scaled matrix cores; this probe measures what
 // those cores deliver on this GPU.  One CTA per SM keeps operand tiles resident in
 // shared memory and scale factors in tensor memory and issues `iters` MMAs of
-// M = 128, N = 128 from one elected thread, rotating over three accumulators in
-// tensor memory (the attention kernel's score MMA: SS form, K-major swizzled
-// tiles):
+// M = 128 and N = 128 (the attention kernel's score MMA; three accumulators in
+// rotation) or N = 256 (one accumulator) from one elected thread, SS form, K-major
+// swizzled tiles.  At N = 128 an MXFP4 MMA reads 8 KB of shared memory per 2 MFLOP,
+// which is near the shared-memory bandwidth; N = 256 halves the A traffic per FLOP:
 //   kind 0  kind::f16, bf16 x bf16,                         K = 16 per MMA
 //   kind 1  kind::mxf8f6f4 block_scale scale_vec::1X, E4M3, K = 32 per MMA
 //   kind 2  kind::mxf4 block_scale scale_vec::2X, E2M1,     K = 64 per MMA
@@ -23,14 +24,14 @@ namespace fsa {
 namespace {
 
 constexpr int kPeakThreads = 128;
-constexpr int kTileBytes = 128 * 256;       // up to 256 bytes per row (bf16, K = 128)
-constexpr int kOffA = 0, kOffB = kTileBytes, kOffSF = 2 * kTileBytes, kOffBar = kOffSF + 1024;
+constexpr int kTileBytes = 128 * 256;       // A: 128 rows of up to 256 bytes (bf16, K = 128)
+constexpr int kOffA = 0, kOffB = kTileBytes, kOffSF = kOffB + 2 * kTileBytes, kOffBar = kOffSF + 1024;
 // more shared memory than two CTAs could share, so that each CTA (and its 512
 // tensor-memory columns) has an SM to itself
-constexpr int kPeakSmem = 120 * 1024;
+constexpr int kPeakSmem = 120 * 1024;   // B: up to 256 rows of 256 bytes
 static_assert(kOffBar + 64 + 1024 <= kPeakSmem, "shared memory");
 
-template <int KIND>
+template <int KIND, int N>
 __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long iters, int* status,
                                                                        uint64_t timeout_ns) {
   // bytes per operand row (K = 128 elements) and the swizzle atom of the tiles
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long
   const int warp = threadIdx.x >> 5;
   // finite operand bytes (every byte <= 0x3F: no E4M3 NaN, bf16 magnitudes < 2) and
   // scale atoms of 2^0
-  for (int i = threadIdx.x; i < 2 * kTileBytes / 4; i += kPeakThreads) {
+  for (int i = threadIdx.x; i < 3 * kTileBytes / 4; i += kPeakThreads) {
     uint32_t h = (uint32_t)i * 0x9E3779B1u;
     h ^= h >> 15;
     reinterpret_cast<uint32_t*>(sm)[i] = h & 0x3F3F3F3Fu;
@@ -68,6 +69,9 @@ __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long
       tc_cp_sf_atom_p(elect_u32(), tbase + T_SFA, smem_desc(smem_u32(sm + kOffSF), 16, 128, 0));
       tc_cp_sf_atom_p(elect_u32(), tbase + T_SFB, smem_desc(smem_u32(sm + kOffSF + 512), 16, 128, 0));
     }
+    // N = 128: accumulators at columns 0, 128, 256; N = 256: one at column 0 (the scale
+    // columns 400..411 stay clear of both)
+    constexpr int NACC = N == 128 ? 3 : 1;
     int acc_buf = 0;
     for (long long it = 0; it < iters; ++it) {
       const uint32_t d = tbase + 128u * (uint32_t)acc_buf;
@@ -75,18 +79,18 @@ __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long
       for (int i = 0; i < STEPS; ++i) {
         const int ka = (i * 32) / W, off = (i * 32) % W;
         const uint64_t ad = smem_desc(sA + ka * 128 * W + off, 16, 8 * W, SWZ);
-        const uint64_t bd = smem_desc(sB + ka * 128 * W + off, 16, 8 * W, SWZ);
-        const uint32_t acc = (it > 2 || i > 0) ? 1u : 0u;
+        const uint64_t bd = smem_desc(sB + ka * N * W + off, 16, 8 * W, SWZ);
+        const uint32_t acc = (it >= NACC || i > 0) ? 1u : 0u;
         const uint32_t e = elect_u32();
         if constexpr (KIND == 0) {
-          mma_f16_ss_p(e, d, ad, bd, idesc_f16_bf16(128), acc);
+          mma_f16_ss_p(e, d, ad, bd, idesc_f16_bf16(N), acc);
         } else if constexpr (KIND == 1) {
-          mma_mxf8f6f4_ss_p(e, d, ad, bd, idesc_bs(128, 0, i, i), tbase + T_SFA, tbase + T_SFB, acc);
+          mma_mxf8f6f4_ss_p(e, d, ad, bd, idesc_bs(N, 0, i, i), tbase + T_SFA, tbase + T_SFB, acc);
         } else {
-          mma_mxf4_ss_p(e, d, ad, bd, idesc_bs(128, 1, 2 * i, 2 * i), tbase + T_SFA, tbase + T_SFB, acc);
+          mma_mxf4_ss_p(e, d, ad, bd, idesc_bs(N, 1, 2 * i, 2 * i), tbase + T_SFA, tbase + T_SFB, acc);
         }
       }
-      acc_buf = acc_buf == 2 ? 0 : acc_buf + 1;
+      acc_buf = acc_buf == NACC - 1 ? 0 : acc_buf + 1;
     }
     tc_commit_p(elect_u32(), done);
     // every MMA of this warp has completed before tensor memory is freed
@@ -101,12 +105,12 @@ __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long
 
 }  // namespace
 
-double mma_peak_flops_per_iter(int kind) {
-  // 2 * M * N * K per MMA, STEPS MMAs (K = 128 elements in total) per iteration
-  return 2.0 * 128.0 * 128.0 * 128.0;
+double mma_peak_flops_per_iter(int kind, int n) {
+  // 2 * M * N * K per iteration (its MMAs cover K = 128 elements)
+  return 2.0 * 128.0 * (double)n * 128.0;
 }
 
-cudaError_t launch_mma_peak(int kind, int n_ctas, long long iters, int* status, uint64_t timeout_ns,
+cudaError_t launch_mma_peak(int kind, int n, int n_ctas, long long iters, int* status, uint64_t timeout_ns,
                             cudaStream_t st) {
   auto run = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPeakSmem);
@@ -114,9 +118,14 @@ cudaError_t launch_mma_peak(int kind, int n_ctas, long long iters, int* status, 
     kern<<<n_ctas, kPeakThreads, kPeakSmem, st>>>(iters, status, timeout_ns);
     return cudaGetLastError();
   };
-  if (kind == 0) return run(fsa_mma_peak_kernel<0>);
-  if (kind == 1) return run(fsa_mma_peak_kernel<1>);
-  return run(fsa_mma_peak_kernel<2>);
+  if (n == 256) {
+    if (kind == 0) return run(fsa_mma_peak_kernel<0, 256>);
+    if (kind == 1) return run(fsa_mma_peak_kernel<1, 256>);
+    return run(fsa_mma_peak_kernel<2, 256>);
+  }
+  if (kind == 0) return run(fsa_mma_peak_kernel<0, 128>);
+  if (kind == 1) return run(fsa_mma_peak_kernel<1, 128>);
+  return run(fsa_mma_peak_kernel<2, 128>);
 }
 
 }  // namespace fsa

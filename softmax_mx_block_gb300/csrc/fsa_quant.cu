@@ -10,71 +10,9 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include "fsa_launch.h"
+#include "fsa_mx.cuh"
 
 namespace fsa {
-
-__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
-
-// Block exponent from the fp32 bit pattern of amax (exact for bf16 inputs).
-// Returns the scale byte; 0xFF for a non-finite block.
-__device__ __forceinline__ uint32_t block_scale_byte(float amax, int emax) {
-  const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-  if (ef == 0xFF) return 0xFFu;
-  int E = ef - 127 - emax;      // zero and subnormal amax fall below -127 and clamp
-  E = E < -127 ? -127 : (E > 127 ? 127 : E);
-  return (uint32_t)(E + 127);
-}
-
-// 2^-E as fp32 for E in [-127, 127] (2^-127..2^127, exact).
-__device__ __forceinline__ float pow2_neg(int E) {
-  return E == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - E) << 23);
-}
-
-template <int FMT>
-__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
-  if constexpr (FMT == 0) return cvt_e4m3x2(lo, hi);
-  else if constexpr (FMT == 1) return cvt_e2m3x2(lo, hi);
-  else return cvt_e2m1x2(lo, hi);
-}
-
-// Codes of one 32-element block held by one thread, v[0..32): 8 words (E4M3:
-// one code per byte; E2M3: two 16-code groups of 12 packed bytes and 4 zero
-// bytes) or 4 words (E2M1, two codes per byte, even index in the low nibble).
-// Returns the scale byte (0xFF and NaN / zero codes for a non-finite block).
-template <int FMT>
-__device__ __forceinline__ uint32_t quant_block32(const float* v, uint32_t* w) {
-  constexpr int emax = FMT == 0 ? 8 : 2;
-  float amax = 0.f;
-  bool nonfinite = false;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float a = fabsf(v[i]);
-    nonfinite |= !(a <= 3.4e38f);
-    amax = fmaxf(amax, a);
-  }
-  const uint32_t sbyte = nonfinite ? 0xFFu : block_scale_byte(amax, emax);
-  const float mul = nonfinite ? 1.0f : pow2_neg((int)sbyte - 127);
-  uint32_t q[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    q[i] = nonfinite ? (FMT == 0 ? 0x7F7Fu : 0u) : cvt_pair<FMT>(__fmul_rn(v[2 * i], mul), __fmul_rn(v[2 * i + 1], mul));
-  if constexpr (FMT == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = q[2 * i] | (q[2 * i + 1] << 16);
-  } else if constexpr (FMT == 1) {
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const uint32_t g[4] = {q[8 * gi] | (q[8 * gi + 1] << 16), q[8 * gi + 2] | (q[8 * gi + 3] << 16),
-                             q[8 * gi + 4] | (q[8 * gi + 5] << 16), q[8 * gi + 6] | (q[8 * gi + 7] << 16)};
-      pack6x16(g, w + 4 * gi);
-      w[4 * gi + 3] = 0u;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = q[4 * i] | (q[4 * i + 1] << 8) | (q[4 * i + 2] << 16) | (q[4 * i + 3] << 24);
-  }
-  return sbyte;
-}
 
 // --------------------------------------------------------------------------
 // Rows layout (Q, K): one CTA per (128-row tile, b*h), 256 threads.  Chunk =

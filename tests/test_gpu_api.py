@@ -45,8 +45,9 @@ BF16_CASES = [
 def test_bf16_output_is_the_rounded_fp32_output(w, schedule):
     """out_dtype bf16 writes the same fp32 quotients rounded to nearest even: bit for bit
     the RNE of the fp32 output, under both schedules; against the oracle's emulation the
-    tolerance grows by the bf16 rounding, |O - O_emu| <= 2e-3 rms + 2^-8 |O_emu| (bf16
-    keeps 8 significant bits, so rounding moves a value by at most 2^-8 of it)."""
+    tolerance grows by the bf16 rounding, |O - O_emu| <= (2e-3 rms + amb)(1 + 2^-8) +
+    2^-8 |O_emu| (bf16 keeps 8 significant bits, so rounding moves a value by at most
+    2^-8 of it; amb is the oracle's bound of what fp32 scores leave undetermined)."""
     fsa = _fsa()
     q, k, v = generate(w)
     mq, mk, mv = _mx(w, q, k, v)
@@ -60,10 +61,15 @@ def test_bf16_output_is_the_rounded_fp32_output(w, schedule):
     f32 = o32.cpu().numpy().reshape(-1, w.D)
     assert np.array_equal(b16, _bf16_rne_bits(f32))
     rows = sample_rows(w)
-    emu = oracle_mx(w, q, k, v, rows, 0xFFFFFFFF, delta=8.0, with_floor=False)["emu"]
+    mx = oracle.MxInputs.from_bf16(q, k, v, fq, 2 if fp == 3 else fp)
+    orc = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=8.0, mufu_mask=0xFFFFFFFF, ambiguity=True)
+    emu, amb = orc["out"], orc["amb"]
+    det = ~np.isinf(amb).any(axis=1)
     o = (b16.astype(np.uint32) << 16).view(np.float32)[rows]
-    tol = TOL_EMU * np.sqrt(np.mean(emu ** 2)) * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(emu)
-    assert np.all(np.abs(o - emu) <= tol)
+    # the fp32 output's bound (2e-3 rms plus what fp32 leaves undetermined), then the rounding
+    tol = (TOL_EMU * np.sqrt(np.mean(emu ** 2)) + amb) * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(emu)
+    assert np.all((np.abs(o - emu) <= tol)[det])
+    assert det.mean() > 0.99
 
 
 def test_layer_schedule_matches_single_calls():
@@ -97,19 +103,62 @@ def test_layer_schedule_matches_single_calls():
     assert rates[0]["fallback_events"] > 0                  # delta 0 on planted keys falls back
 
 
+@pytest.mark.parametrize("n", [128, 256])
 @pytest.mark.parametrize("kind", [0, 1, 2])
-def test_mma_peak_probe_runs(kind):
+def test_mma_peak_probe_runs(kind, n):
     """The throughput probe completes without a timeout on every SM and reports a
     plausible rate (a few hundred TFLOP/s at least for a short launch)."""
     fsa = _fsa()
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fsa.fsa_mma_peak(kind, n_sm, 200, status)                 # warm-up
+    fsa.fsa_mma_peak(kind, n_sm, 200, status, n=n)            # warm-up
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    flops = fsa.fsa_mma_peak(kind, n_sm, 20000, status)
+    flops = fsa.fsa_mma_peak(kind, n_sm, 20000, status, n=n)
     e1.record()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     tflops = flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
     assert 200.0 < tflops < 30000.0, tflops
+
+
+FUSED_Q_CASES = [
+    Workload("fq_e4m3_causal", 1, 4, 2, 300, 300, 128, True, "E4M3", "E4M3", 51, "k_outliers"),
+    Workload("fq_e2m3_d64", 1, 2, 1, 256, 700, 64, False, "E2M3", "E2M1", 52),
+    Workload("fq_efq", 1, 4, 2, 520, 1100, 128, True, "E2M1", "E2M1_EFQ", 53),
+    Workload("fq_efq_d64_rect", 1, 3, 3, 700, 300, 64, True, "E2M1", "E2M1_EFQ", 54),
+    Workload("fq_e2m1_e4m3", 2, 2, 2, 200, 200, 128, False, "E2M1", "E4M3", 55),
+]
+
+
+@pytest.mark.parametrize("w", FUSED_Q_CASES, ids=lambda w: w.name)
+def test_fused_q_quantisation_is_bit_identical(w):
+    """fsa_attention_fwd_qbf16 quantises bf16 Q in the attention kernel's prologue: the
+    output, per-row fallback counts and stats equal those of quantising Q with
+    fsa_mx_quantize first, bit for bit (ragged tails, rows without keys, both head
+    dimensions, every QK^T format)."""
+    fsa = _fsa()
+    q, k, v = generate(w)
+    mq, mk, mv = _mx(w, q, k, v)
+    fq, fp = FMT[w.fmt_qk], FMT[w.fmt_pv]
+    kw = dict(causal=w.causal, scale=w.scale, fmt_qk=fq, fmt_pv=fp, schedule=1)
+    res = []
+    for qq in (mq, _dev(q)):
+        st = fsa.new_stats()
+        rf = torch.zeros((w.B, w.H, w.Sq), dtype=torch.int32, device="cuda")
+        o = fsa.fsa_attention_fwd(qq, mk, mv, stats=st, row_fallbacks=rf, **kw)
+        torch.cuda.synchronize()
+        res.append((o, fsa.read_stats(st), rf))
+    assert torch.equal(res[0][0].view(torch.int32), res[1][0].view(torch.int32))
+    assert res[0][1] == res[1][1] and torch.equal(res[0][2], res[1][2])
+    assert res[1][1]["status"] == 0
+
+
+def test_fused_q_refuses_unsupported_options():
+    fsa = _fsa()
+    w = FUSED_Q_CASES[0]
+    q, k, v = generate(w)
+    _, mk, mv = _mx(w, q, k, v)
+    for kw in (dict(schedule=2), dict(exp_mode=0)):
+        with pytest.raises(fsa.FsaError, match="unsupported"):
+            fsa.fsa_attention_fwd(_dev(q), mk, mv, causal=True, fmt_qk=0, fmt_pv=0, **kw)

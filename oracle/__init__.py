@@ -29,8 +29,8 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E8M0": 3, "E2M1_EFQ": 3}
-EMAX = {0: 8, 1: 2, 2: 2}
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E8M0": 3, "E2M1_EFQ": 3, "E3M2": 4}
+EMAX = {0: 8, 1: 2, 2: 2, 4: 4}
 
 
 def build(force: bool = False) -> str:
@@ -225,7 +225,7 @@ EFQ_A, EFQ_B, EFQ_PHI = 1.6875, 3.5, 0.5625      # the EFQ rule's constants (see
 
 def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_mask=0, beta=EFQ_B,
                 efq_a=EFQ_A, phi=EFQ_PHI, dump=False, ambiguity=False, s_perturb=0.0, s_in=None, nthreads=None):
-    """Step-by-step emulation of the fused MX forward.  fmt_p: 0/1/2 exp path, 3 EFQ.
+    """Step-by-step emulation of the fused MX forward.  fmt_p: 0/1/2/4 exp path, 3 EFQ.
 
     EFQ codes are clamp(rne(fmaf(s, fp32(efq_a c), fp32(beta - fp32(efq_a (M + E))))), 0, 7)
     with the block exponent E = floor(tmax + phi) - 2 (phi applies to EFQ only; the exp

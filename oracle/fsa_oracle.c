@@ -40,6 +40,8 @@
 /*      1 = E2M3 (bias 1, 3 mantissa bits, max 7.5, 6-bit code, no NaN/inf)    */
 /*      2 = E2M1 (bias 1, 1 mantissa bit,  max 6,   4-bit code, no NaN/inf)    */
 /*      3 = E8M0 scale (2^(code-127); 0xFF = NaN)                              */
+/*      4 = E3M2 (bias 3, 2 mantissa bits, max 28,  6-bit code, no NaN/inf):   */
+/*          the other MXFP6 element type of [OCP-MX]                            */
 /* ------------------------------------------------------------------------- */
 typedef struct { int ebits, mbits, bias; double maxv; int sign_shift; } fmt_info;
 
@@ -48,13 +50,14 @@ static fmt_info info_of(int fmt) {
   switch (fmt) {
     case 0: f.ebits = 4; f.mbits = 3; f.bias = 7; f.maxv = 448.0; f.sign_shift = 7; break;
     case 1: f.ebits = 2; f.mbits = 3; f.bias = 1; f.maxv = 7.5;   f.sign_shift = 5; break;
+    case 4: f.ebits = 3; f.mbits = 2; f.bias = 3; f.maxv = 28.0;  f.sign_shift = 5; break;
     default: f.ebits = 2; f.mbits = 1; f.bias = 1; f.maxv = 6.0;  f.sign_shift = 3; break;
   }
   return f;
 }
 
 /* exponent of the largest normal power of two of each element format */
-int orc_emax(int fmt) { return fmt == 0 ? 8 : 2; }
+int orc_emax(int fmt) { return fmt == 0 ? 8 : (fmt == 4 ? 4 : 2); }
 
 double orc_decode(int fmt, uint32_t code) {
   if (fmt == 3) {
@@ -499,7 +502,7 @@ float orc_exp2_poly(float r) {
 /* The per-element exp2approx is chosen by bit (j % 32) of mufu_mask: set ->     */
 /* modelled as exact 2^r rounded to fp32 (the hardware approximation on the      */
 /* GPU differs in the last bits); clear -> orc_exp2_poly (bit-reproducible).     */
-/* fmt_p: 0 E4M3, 1 E2M3, 2 E2M1, 3 E2M1 by the EFQ rule.                        */
+/* fmt_p: 0 E4M3, 1 E2M3, 2 E2M1, 3 E2M1 by the EFQ rule, 4 E3M2.               */
 /* ------------------------------------------------------------------------- */
 typedef struct {
   float delta;        /* fallback margin, log2 units: fall back when x > M + delta */

@@ -26,6 +26,8 @@ EQUIVALENT = {"no final saturation"}
 M = [
  ("e4m3 bias", "f.bias = 7;", "f.bias = 8;"),
  ("e2m3 max", "f.maxv = 7.5;", "f.maxv = 7.0;"),
+ ("e3m2 bias", "f.ebits = 3; f.mbits = 2; f.bias = 3;", "f.ebits = 3; f.mbits = 2; f.bias = 2;"),
+ ("e3m2 emax", "return fmt == 0 ? 8 : (fmt == 4 ? 4 : 2);", "return fmt == 0 ? 8 : 2;"),
  ("subnormal decode", "ldexp((double)m, 1 - f.bias - f.mbits)", "ldexp((double)m, -f.bias - f.mbits)"),
  ("ties away", "nearbyint(a / q) * q", "round(a / q) * q"),
  ("no final saturation", "    if (v > f.maxv) v = f.maxv;\n", ""),

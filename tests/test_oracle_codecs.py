@@ -13,7 +13,7 @@ import oracle
 from workloads import to_bf16_bits, bf16_bits_to_f32
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
-NBITS = {0: 8, 1: 6, 2: 4}
+NBITS = {0: 8, 1: 6, 2: 4, 4: 6}
 
 
 def test_e2m1_table_matches_ocp():
@@ -38,11 +38,11 @@ def test_format_limits_match_ocp():
         nan_codes = [c for c, v in enumerate(vals) if math.isnan(v)]
         assert nan_codes == ([] if nans == "none" else [int(x, 16) for x in nans.split(",")])
         # smallest normal: exponent field 1, mantissa 0
-        mbits = {0: 3, 1: 3, 2: 1}[f]
+        mbits = {0: 3, 1: 3, 2: 1, 4: 2}[f]
         assert oracle.decode(f, 1 << mbits) == float(mn)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 4])
 def test_roundtrip_every_code(fmt):
     for c in range(1 << NBITS[fmt]):
         v = oracle.decode(fmt, c)
@@ -66,7 +66,7 @@ def _nearest_even_bruteforce(fmt, x):
     return best[1]
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 4])
 def test_encode_matches_bruteforce_nearest(fmt):
     rng = np.random.default_rng(5)
     mx = oracle.decode(fmt, (1 << (NBITS[fmt] - 1)) - (2 if fmt == 0 else 1))
@@ -83,7 +83,7 @@ def test_encode_matches_bruteforce_nearest(fmt):
         assert oracle.encode(fmt, x) == _nearest_even_bruteforce(fmt, x), (fmt, x)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 4])
 def test_saturation_and_signed_zero(fmt):
     n = NBITS[fmt]
     sign = 1 << (n - 1)
@@ -110,7 +110,7 @@ def _bf16(x):
     return to_bf16_bits(np.asarray(x, np.float32))
 
 
-@pytest.mark.parametrize("fmt,emax", [(0, 8), (1, 2), (2, 2)])
+@pytest.mark.parametrize("fmt,emax", [(0, 8), (1, 2), (2, 2), (4, 4)])
 def test_mx_scale_hand_cases(fmt, emax):
     # amax = 1.0 -> floor(log2) = 0 -> E = -emax; amax = 3.0 -> 1 - emax; amax = 0.75 -> -1 - emax
     for amax, fl in [(1.0, 0), (3.0, 1), (0.75, -1), (2.0 ** -20, -20), (1000.0, 9)]:
@@ -123,7 +123,7 @@ def test_mx_scale_hand_cases(fmt, emax):
     assert s[0, 0] == 0 and not c.any()
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 4])
 def test_mx_scale_clamps_at_minus_127(fmt):
     """E8M0 has no scale below 2^-127: a block whose max is 2^-126 (the smallest
     normal bf16) would want E = -126 - emax and gets -127 (scale byte 0); the max
@@ -135,7 +135,7 @@ def test_mx_scale_clamps_at_minus_127(fmt):
     assert oracle.decode(fmt, int(c[0, 5])) == 2.0
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 4])
 def test_mx_exact_roundtrip_on_representable(fmt):
     """x = decode(code) * 2^E with the block max at the format's top binade
     quantises back to the same codes and the scale byte E + 127."""
@@ -162,7 +162,7 @@ def test_mx_exact_roundtrip_on_representable(fmt):
 def test_mx_error_bound_and_padding():
     rng = np.random.default_rng(3)
     x = _bf16(rng.standard_normal((7, 50)).astype(np.float32) * 5)
-    for fmt, mbits in [(0, 3), (1, 3), (2, 1)]:
+    for fmt, mbits in [(0, 3), (1, 3), (2, 1), (4, 2)]:
         c, s = oracle.mx_quantize_rows(x, fmt)
         assert c.shape == (7, 64) and s.shape == (7, 2)
         assert not c[:, 50:].any()                                       # zero padding
@@ -172,7 +172,7 @@ def test_mx_error_bound_and_padding():
         # error <= half a grid step at the block's top binade (or saturation at 2^(emax+1))
         Ee = np.repeat(E, 32, axis=1)[:, :50]
         step = 2.0 ** (Ee + oracle.EMAX[fmt] - mbits)
-        top = {0: 448.0, 1: 7.5, 2: 6.0}[fmt] * 2.0 ** Ee
+        top = {0: 448.0, 1: 7.5, 2: 6.0, 4: 28.0}[fmt] * 2.0 ** Ee
         inside = np.abs(xf) <= top
         assert np.all(np.abs(dec - xf)[inside] <= step[inside] * 0.5)
         assert np.array_equal(dec[~inside], np.sign(xf[~inside]) * top[~inside])   # satfinite
@@ -187,7 +187,7 @@ def test_mx_cols_blocks_along_sequence():
     assert np.array_equal(c, c2) and np.array_equal(s, s2)
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 4])
 def test_mx_nonfinite_block(fmt):
     """A block with an Inf takes the E8M0 NaN scale 0xFF (OCP MX: the whole block
     then decodes to NaN).  Its element codes: the E4M3 NaN code 0x7F, or 0 in the

@@ -38,9 +38,9 @@ DEFAULT_WORKLOAD = "long_efq_128k"
 # further workloads reported in the same line (kernel throughput, fraction of the
 # measured peak, speedup over the BF16 kernel, fallback rate)
 EXTRA_WORKLOADS = ["long_fp8_16k", "long_fp8_128k", "long_efq_16k", "video_dit", "adversarial"]
-FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4}
 # tensor-core kind of each operand format: 0 kind::f16, 1 kind::mxf8f6f4, 2 kind::mxf4
-KIND = {"E4M3": 1, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 2}
+KIND = {"E4M3": 1, "E2M3": 1, "E3M2": 1, "E2M1": 2, "E2M1_EFQ": 2}
 # nominal dense ratio of each kind to BF16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s): used
 # only when the probe could not run
 KIND_RATIO = {0: 1.0, 1: 2.0, 2: 6.0}

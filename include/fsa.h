@@ -60,7 +60,8 @@ typedef enum {
   FSA_FMT_E4M3 = 0,      /* MXFP8 */
   FSA_FMT_E2M3 = 1,      /* MXFP6 */
   FSA_FMT_E2M1 = 2,      /* MXFP4, P by exp then round-to-nearest-even */
-  FSA_FMT_E2M1_EFQ = 3   /* MXFP4, P by the EFQ affine rule (fmt_pv only) */
+  FSA_FMT_E2M1_EFQ = 3,  /* MXFP4, P by the EFQ affine rule (fmt_pv only) */
+  FSA_FMT_E3M2 = 4       /* MXFP6, the OCP MX E3M2 element type (bias 3, max 28) */
 } fsa_fmt;
 
 /* ------------------------------------------------------------ MX tensors */
@@ -68,11 +69,11 @@ typedef enum {
  * per 32 consecutive elements along the contraction dimension.
  *
  * FSA_MX_ROWS (Q and K; blocks along D).  Source x[B][H][S][D] bf16.
- *   codes : [B*H][S][row_bytes], row_bytes = D (E4M3, E2M3) or D/2 (E2M1).
- *           E4M3: one byte per element.  E2M3: each group of 16 elements is
- *           12 bytes of 6-bit codes packed least-significant-bit first,
- *           followed by 4 zero bytes.  E2M1: two elements per byte, the even
- *           element in the low nibble.
+ *   codes : [B*H][S][row_bytes], row_bytes = D (E4M3, E2M3, E3M2) or D/2
+ *           (E2M1).  E4M3: one byte per element.  E2M3 and E3M2: each group of
+ *           16 elements is 12 bytes of 6-bit codes packed least-significant-bit
+ *           first, followed by 4 zero bytes.  E2M1: two elements per byte, the
+ *           even element in the low nibble.
  *   scales: [B*H][ceil(S/128)][512] bytes: for row r of a 128-row tile and
  *           block b (b < D/32), byte (r%32)*16 + (r/32)*4 + b.  Slots with no
  *           data (rows >= S, blocks >= D/32) hold 0x7F.
@@ -83,14 +84,14 @@ typedef enum {
  *           a 128-key tile, byte (d%32)*16 + (d/32)*4 + b.  Rows d >= D hold
  *           0x7F; blocks of keys wholly >= S hold 0x7F.
  * The block scale is E = clamp(floor(log2 amax) - emax, -127, 127) (emax 8
- * for E4M3, 2 for E2M3/E2M1), codes = round-to-nearest-even, saturating, of
+ * for E4M3, 4 for E3M2, 2 for E2M3/E2M1), codes = round-to-nearest-even, saturating, of
  * x * 2^-E; a block with a non-finite element gets scale 0xFF.           */
 typedef enum { FSA_MX_ROWS = 0, FSA_MX_COLS_T = 1 } fsa_mx_layout;
 
 typedef struct {
   void*    codes;    /* device, 16-byte aligned */
   uint8_t* scales;   /* device, 16-byte aligned */
-  int32_t  fmt;      /* fsa_fmt of the codes (E4M3, E2M3 or E2M1) */
+  int32_t  fmt;      /* fsa_fmt of the codes (E4M3, E2M3, E2M1 or E3M2) */
   int32_t  layout;   /* fsa_mx_layout */
   int32_t  B, H, S, D;
 } fsa_mx_tensor;

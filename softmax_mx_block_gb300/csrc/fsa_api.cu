@@ -141,7 +141,9 @@ int bits2_of(int fmt) { return fmt == FSA_FMT_E2M1 || fmt == FSA_FMT_E2M1_EFQ ? 
 
 int row_bytes(int D, int fmt) { return D * bits2_of(fmt) / 16; }
 
-bool valid_fmt(int f) { return f >= FSA_FMT_E4M3 && f <= FSA_FMT_E2M1; }
+// storage formats of MX tensors (E2M1_EFQ is a P format only)
+bool valid_fmt(int f) { return (f >= FSA_FMT_E4M3 && f <= FSA_FMT_E2M1) || f == FSA_FMT_E3M2; }
+bool valid_pv(int f) { return f >= FSA_FMT_E4M3 && f <= FSA_FMT_E3M2; }
 
 int storage_fmt(int f) { return f == FSA_FMT_E2M1_EFQ ? FSA_FMT_E2M1 : f; }
 
@@ -155,12 +157,19 @@ bool shape_ok(int B, int H, int Hkv, int Sq, int Sk, int D) {
 
 using ImplFn = cudaError_t (*)(const AttnLaunch&);
 
+// fsa.h format numbers are the kernels' template arguments (fsa_attn.cuh)
 ImplFn impl_for(int fqk, int fpv) {
   using namespace fsa;
-  static const ImplFn table[3][4] = {
-      {launch_attn_impl<0, 0>, launch_attn_impl<0, 1>, launch_attn_impl<0, 2>, launch_attn_impl<0, 3>},
-      {launch_attn_impl<1, 0>, launch_attn_impl<1, 1>, launch_attn_impl<1, 2>, launch_attn_impl<1, 3>},
-      {launch_attn_impl<2, 0>, launch_attn_impl<2, 1>, launch_attn_impl<2, 2>, launch_attn_impl<2, 3>}};
+  static const ImplFn table[5][5] = {
+      {launch_attn_impl<0, 0>, launch_attn_impl<0, 1>, launch_attn_impl<0, 2>, launch_attn_impl<0, 3>,
+       launch_attn_impl<0, 4>},
+      {launch_attn_impl<1, 0>, launch_attn_impl<1, 1>, launch_attn_impl<1, 2>, launch_attn_impl<1, 3>,
+       launch_attn_impl<1, 4>},
+      {launch_attn_impl<2, 0>, launch_attn_impl<2, 1>, launch_attn_impl<2, 2>, launch_attn_impl<2, 3>,
+       launch_attn_impl<2, 4>},
+      {nullptr, nullptr, nullptr, nullptr, nullptr},
+      {launch_attn_impl<4, 0>, launch_attn_impl<4, 1>, launch_attn_impl<4, 2>, launch_attn_impl<4, 3>,
+       launch_attn_impl<4, 4>}};
   return table[fqk][fpv];
 }
 
@@ -315,7 +324,7 @@ int attention_impl(const fsa_mx_tensor* q, const void* q_bf16, const fsa_mx_tens
                    int fmt_pv, const fsa_opts* opts, fsa_stats* stats, void* stream) {
   if (!(q || q_bf16) || !k || !v || !out) return FSA_ERR_INVALID_ARG;
   if (!shape_ok(B, H, Hkv, Sq, Sk, D) || !(scale > 0.0f) || !std::isfinite(scale)) return FSA_ERR_INVALID_ARG;
-  if (!valid_fmt(fmt_qk) || fmt_pv < FSA_FMT_E4M3 || fmt_pv > FSA_FMT_E2M1_EFQ) return FSA_ERR_UNSUPPORTED_FMT;
+  if (!valid_fmt(fmt_qk) || !valid_pv(fmt_pv)) return FSA_ERR_UNSUPPORTED_FMT;
   const int fv = storage_fmt(fmt_pv);
   // operand descriptors must match the call
   if (q && q->layout != FSA_MX_ROWS) return FSA_ERR_INVALID_ARG;
@@ -440,8 +449,7 @@ int fsa_attention_fwd_layers(const fsa_layer* layers, int n_layers, const fsa_op
     if (!L.q || !L.k || !L.v || !L.out || !std::isfinite(L.delta) || L.delta < 0.0f) return FSA_ERR_INVALID_ARG;
     if (!shape_ok(L.B, L.H, L.Hkv, L.Sq, L.Sk, L.D) || !(L.scale > 0.0f) || !std::isfinite(L.scale))
       return FSA_ERR_INVALID_ARG;
-    if (!valid_fmt(L.fmt_qk) || L.fmt_pv < FSA_FMT_E4M3 || L.fmt_pv > FSA_FMT_E2M1_EFQ)
-      return FSA_ERR_UNSUPPORTED_FMT;
+    if (!valid_fmt(L.fmt_qk) || !valid_pv(L.fmt_pv)) return FSA_ERR_UNSUPPORTED_FMT;
     if (L.q->fmt != L.fmt_qk || L.k->fmt != L.fmt_qk || L.v->fmt != storage_fmt(L.fmt_pv))
       return FSA_ERR_UNSUPPORTED_FMT;
   }

@@ -142,6 +142,11 @@ __device__ __forceinline__ uint16_t cvt16_e2m3x2(float lo, float hi) {
   asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+__device__ __forceinline__ uint16_t cvt16_e3m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -222,6 +227,10 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
 #pragma unroll
       for (int w = 0; w < 8; ++w)
         out[w] = pack_b16x2(cvt16_e2m3x2(v[4 * w], v[4 * w + 1]), cvt16_e2m3x2(v[4 * w + 2], v[4 * w + 3]));
+    } else if constexpr (FPV == F_E3M2) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        out[w] = pack_b16x2(cvt16_e3m2x2(v[4 * w], v[4 * w + 1]), cvt16_e3m2x2(v[4 * w + 2], v[4 * w + 3]));
     } else {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -381,7 +390,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t one4;
     if constexpr (FPV == F_BF16) one4 = 0x3F803F80u;
     else if constexpr (FPV == F_E4M3) one4 = 0x38383838u;
-    else if constexpr (FPV == F_E2M3) one4 = 0u;   // set per word below (packed 6-bit)
+    else if constexpr (FPV == F_E2M3 || FPV == F_E3M2) one4 = 0u;   // set per word below (packed 6-bit)
     else one4 = 0x22222222u;
     constexpr int ROWW = C::W_V / 4;                 // words per row per atom
     constexpr int PER_STAGE = C::NKA_V * 16 * ROWW;
@@ -393,6 +402,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if constexpr (FPV == F_E2M3) {
           const int wg = w & 3;                      // 16-byte group: bytes (08 82 20) x 4, then 4 zero bytes
           val = wg == 0 ? 0x08208208u : (wg == 1 ? 0x82082082u : (wg == 2 ? 0x20820820u : 0u));
+        } else if constexpr (FPV == F_E3M2) {
+          const int wg = w & 3;                      // 1.0 = code 0x0C: bytes (0C C3 30) x 4, then 4 zero bytes
+          val = wg == 0 ? 0x0C30C30Cu : (wg == 1 ? 0xC30C30C3u : (wg == 2 ? 0x30C30C30u : 0u));
         } else {
           val = one4;
         }

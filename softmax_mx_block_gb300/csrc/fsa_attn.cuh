@@ -6,16 +6,18 @@
 
 namespace fsa {
 
-// Operand formats.  F_EFQ stores E2M1 like F_E2M1; it only changes how the
-// softmax warps produce P.
-enum : int { F_E4M3 = 0, F_E2M3 = 1, F_E2M1 = 2, F_EFQ = 3, F_BF16 = 4 };
+// Operand formats (0..4 as fsa.h numbers them).  F_EFQ stores E2M1 like F_E2M1;
+// it only changes how the softmax warps produce P.
+enum : int { F_E4M3 = 0, F_E2M3 = 1, F_E2M1 = 2, F_EFQ = 3, F_E3M2 = 4, F_BF16 = 5 };
 
 template <int F> struct Fmt;
 // kind: 0 = kind::f16, 1 = kind::mxf8f6f4 (scale_vec 1X, K = 32), 2 = kind::mxf4 (2X, K = 64)
+// code: the element type field of the block-scaled instruction descriptor
 // bits2: storage bits per element * 2 (E2M1 packs two per byte)
 template <> struct Fmt<F_BF16> { static constexpr int kind = 0, bits2 = 32, code = 0, emax = 0; };
 template <> struct Fmt<F_E4M3> { static constexpr int kind = 1, bits2 = 16, code = 0, emax = 8; };
 template <> struct Fmt<F_E2M3> { static constexpr int kind = 1, bits2 = 16, code = 3, emax = 2; };  // 16 codes / 16 bytes
+template <> struct Fmt<F_E3M2> { static constexpr int kind = 1, bits2 = 16, code = 4, emax = 4; };  // 16 codes / 16 bytes
 template <> struct Fmt<F_E2M1> { static constexpr int kind = 2, bits2 = 8, code = 1, emax = 2; };
 template <> struct Fmt<F_EFQ>  { static constexpr int kind = 2, bits2 = 8, code = 1, emax = 2; };
 

@@ -414,7 +414,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     uint32_t one4;
     if constexpr (FPV == F_BF16) one4 = 0x3F803F80u;
     else if constexpr (FPV == F_E4M3) one4 = 0x38383838u;
-    else if constexpr (FPV == F_E2M3) one4 = 0u;   // set per word below (packed 6-bit)
+    else if constexpr (FPV == F_E2M3 || FPV == F_E3M2) one4 = 0u;   // set per word below (packed 6-bit)
     else one4 = 0x22222222u;
     constexpr int ROWW = C::W_V / 4;                 // words per row per atom
     constexpr int PER_STAGE = C::NKA_V * 16 * ROWW;
@@ -426,6 +426,9 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         if constexpr (FPV == F_E2M3) {
           const int wg = w & 3;                      // 16-byte group: bytes (08 82 20) x 4, then 4 zero bytes
           val = wg == 0 ? 0x08208208u : (wg == 1 ? 0x82082082u : (wg == 2 ? 0x20820820u : 0u));
+        } else if constexpr (FPV == F_E3M2) {
+          const int wg = w & 3;                      // 1.0 = code 0x0C: bytes (0C C3 30) x 4, then 4 zero bytes
+          val = wg == 0 ? 0x0C30C30Cu : (wg == 1 ? 0xC30C30C3u : (wg == 2 ? 0x30C30C30u : 0u));
         } else {
           val = one4;
         }

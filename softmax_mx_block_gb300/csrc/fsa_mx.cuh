@@ -3,14 +3,18 @@
 // fused quantisation of Q (fsa_attn.cu), so both write the same codes and scales.
 //
 // Blocks of 32 elements share one E8M0 scale 2^E with
-// E = clamp(floor(log2 amax) - emax, -127, 127) (emax 8 for E4M3, 2 for E2M3 and
-// E2M1); element codes are x * 2^-E rounded to nearest even with saturation
+// E = clamp(floor(log2 amax) - emax, -127, 127) (emax 8 for E4M3, 4 for E3M2, 2 for
+// E2M3 and E2M1); element codes are x * 2^-E rounded to nearest even with saturation
 // (cvt.rn.satfinite); a block with a non-finite element gets scale 0xFF.
 #pragma once
 #include <cstdint>
 #include "fsa_ptx.cuh"
 
 namespace fsa {
+
+// Storage formats (fsa.h numbering): 0 E4M3, 1 E2M3, 2 E2M1, 4 E3M2.
+__host__ __device__ constexpr int mx_emax(int fmt) { return fmt == 0 ? 8 : (fmt == 4 ? 4 : 2); }
+__host__ __device__ constexpr bool mx_six_bit(int fmt) { return fmt == 1 || fmt == 4; }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
@@ -33,6 +37,7 @@ template <int FMT>
 __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
   if constexpr (FMT == 0) return cvt_e4m3x2(lo, hi);
   else if constexpr (FMT == 1) return cvt_e2m3x2(lo, hi);
+  else if constexpr (FMT == 4) return cvt_e3m2x2(lo, hi);
   else return cvt_e2m1x2(lo, hi);
 }
 
@@ -42,7 +47,7 @@ __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
 // Returns the scale byte (0xFF and NaN / zero codes for a non-finite block).
 template <int FMT>
 __device__ __forceinline__ uint32_t quant_block32(const float* v, uint32_t* w) {
-  constexpr int emax = FMT == 0 ? 8 : 2;
+  constexpr int emax = mx_emax(FMT);
   float amax = 0.f;
   bool nonfinite = false;
 #pragma unroll
@@ -60,7 +65,7 @@ __device__ __forceinline__ uint32_t quant_block32(const float* v, uint32_t* w) {
   if constexpr (FMT == 0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = q[2 * i] | (q[2 * i + 1] << 16);
-  } else if constexpr (FMT == 1) {
+  } else if constexpr (FMT == 1 || FMT == 4) {
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
       const uint32_t g[4] = {q[8 * gi] | (q[8 * gi + 1] << 16), q[8 * gi + 2] | (q[8 * gi + 3] << 16),

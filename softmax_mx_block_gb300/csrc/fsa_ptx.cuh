@@ -359,6 +359,11 @@ __device__ __forceinline__ uint32_t cvt_e2m3x2(float lo, float hi) {   // each c
   asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+__device__ __forceinline__ uint32_t cvt_e3m2x2(float lo, float hi) {   // each code in a byte, low 6 bits
+  uint16_t r;
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {   // one byte, lo in the low nibble
   uint32_t r;
   asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));

@@ -25,7 +25,7 @@ namespace fsa {
 template <int FMT, int D>
 __device__ __forceinline__ void quant_rows_tile(const uint16_t* __restrict__ x, int S, uint8_t* __restrict__ codes,
                                                 uint8_t* __restrict__ scales, int64_t tile_id, uint8_t* atom) {
-  constexpr int emax = FMT == 0 ? 8 : 2;
+  constexpr int emax = mx_emax(FMT);
   constexpr int CPR = D / 8;                       // chunks per row
   constexpr int NCH = 128 * CPR / 256;             // chunks per thread
   constexpr int RB = FMT == 2 ? D / 2 : D;         // code bytes per row
@@ -77,7 +77,7 @@ __device__ __forceinline__ void quant_rows_tile(const uint16_t* __restrict__ x, 
       if (nf) q[e] = FMT == 0 ? 0x7F7Fu : 0u;
       else q[e] = cvt_pair<FMT>(__fmul_rn(v[2 * e], mul), __fmul_rn(v[2 * e + 1], mul));
     }
-    if constexpr (FMT == 1) {
+    if constexpr (mx_six_bit(FMT)) {
       // 16-element groups: the even chunk packs its and its neighbour's codes
       uint32_t w[4] = {q[0] | (q[1] << 16), q[2] | (q[3] << 16), 0u, 0u};
       w[2] = __shfl_down_sync(0xffffffffu, w[0], 1);
@@ -263,6 +263,7 @@ cudaError_t launch_mx_quant_rows(const void* x, int BH, int S, int D, int fmt, v
   switch (fmt) {
     case 0: return quant_rows_d<0>(xs, BH, S, D, c, s, st);
     case 1: return quant_rows_d<1>(xs, BH, S, D, c, s, st);
+    case 4: return quant_rows_d<4>(xs, BH, S, D, c, s, st);
     default: return quant_rows_d<2>(xs, BH, S, D, c, s, st);
   }
 }
@@ -275,6 +276,7 @@ cudaError_t launch_mx_quant_cols(const void* x, int BH, int S, int D, int fmt, v
   switch (fmt) {
     case 0: return quant_cols_d<0>(xs, BH, S, D, c, s, st);
     case 1: return quant_cols_d<1>(xs, BH, S, D, c, s, st);
+    case 4: return quant_cols_d<4>(xs, BH, S, D, c, s, st);
     default: return quant_cols_d<2>(xs, BH, S, D, c, s, st);
   }
 }
@@ -291,6 +293,7 @@ static cudaError_t quant_qkv_fv(const QkvArgs& a, int64_t n, int D, int fv, cuda
   switch (fv) {
     case 0: return quant_qkv_d<FQK, 0>(a, n, D, st);
     case 1: return quant_qkv_d<FQK, 1>(a, n, D, st);
+    case 4: return quant_qkv_d<FQK, 4>(a, n, D, st);
     default: return quant_qkv_d<FQK, 2>(a, n, D, st);
   }
 }
@@ -315,6 +318,7 @@ cudaError_t launch_mx_quant_qkv(const void* q, const void* k, const void* v, int
   switch (fqk) {
     case 0: return quant_qkv_fv<0>(a, n, D, fv, st);
     case 1: return quant_qkv_fv<1>(a, n, D, fv, st);
+    case 4: return quant_qkv_fv<4>(a, n, D, fv, st);
     default: return quant_qkv_fv<2>(a, n, D, fv, st);
   }
 }

@@ -19,9 +19,9 @@ def unpack_codes(raw, fmt, n_elems):
     """raw: [..., row_bytes] -> [..., n_elems] logical codes."""
     if fmt == 0:
         return raw[..., :n_elems].copy()
-    if fmt == 1:
+    if fmt in (1, 4):
         g = raw.reshape(raw.shape[:-1] + (raw.shape[-1] // 16, 16))
-        assert not g[..., 12:].any(), "E2M3 padding bytes must be zero"
+        assert not g[..., 12:].any(), "6-bit group padding bytes must be zero"
         return _unpack6(g).reshape(raw.shape[:-1] + (-1,))[..., :n_elems]
     lo, hi = raw & 0x0F, raw >> 4
     return np.stack([lo, hi], axis=-1).reshape(raw.shape[:-1] + (-1,))[..., :n_elems]
@@ -29,7 +29,7 @@ def unpack_codes(raw, fmt, n_elems):
 
 def unpack_rows(codes, scales, fmt, B, H, S, D):
     """FSA_MX_ROWS device buffers -> (codes [B,H,S,D], scales [B,H,S,D/32]); checks padding slots."""
-    rb = D if fmt in (0, 1) else D // 2
+    rb = D if fmt in (0, 1, 4) else D // 2
     c = unpack_codes(np.asarray(codes).reshape(B, H, S, rb), fmt, D)
     nt = (S + 127) // 128
     flat = np.asarray(scales).reshape(-1)
@@ -48,7 +48,7 @@ def unpack_cols(codes, scales, fmt, B, H, S, D):
     """FSA_MX_COLS_T device buffers -> (codes [B,H,D,S32], scales [B,H,D,S32/32]), S32 = S rounded up to 32."""
     Sp = (S + 127) // 128 * 128
     S32 = (S + 31) // 32 * 32
-    rb = Sp if fmt in (0, 1) else Sp // 2
+    rb = Sp if fmt in (0, 1, 4) else Sp // 2
     c = unpack_codes(np.asarray(codes).reshape(B, H, D, rb), fmt, Sp)
     assert not c[..., S:].any(), "codes past the sequence end must be zero"
     nt = Sp // 128

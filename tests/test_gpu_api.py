@@ -128,6 +128,7 @@ FUSED_Q_CASES = [
     Workload("fq_efq", 1, 4, 2, 520, 1100, 128, True, "E2M1", "E2M1_EFQ", 53),
     Workload("fq_efq_d64_rect", 1, 3, 3, 700, 300, 64, True, "E2M1", "E2M1_EFQ", 54),
     Workload("fq_e2m1_e4m3", 2, 2, 2, 200, 200, 128, False, "E2M1", "E4M3", 55),
+    Workload("fq_e3m2", 1, 2, 2, 300, 400, 128, True, "E3M2", "E3M2", 56),
 ]
 
 

@@ -9,7 +9,7 @@ from workloads import WORKLOADS, Workload, generate, sample_rows, small, to_bf16
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3}
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4}
 SPLIT_MASK = 0x77777777          # key positions 4k+3 use the cubic, the rest the hardware exp2
 TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
 # error vs fp64 exact over the error of exact softmax with the same MX operands (the
@@ -86,7 +86,7 @@ def test_tiny_config_all_rows():
 
 
 PAIRS = [("E4M3", "E4M3"), ("E2M3", "E2M1"), ("E2M1", "E2M1_EFQ"), ("E2M3", "E2M3"), ("E2M1", "E2M1"),
-         ("E4M3", "E2M1"), ("E2M1", "E4M3")]
+         ("E4M3", "E2M1"), ("E2M1", "E4M3"), ("E3M2", "E3M2"), ("E3M2", "E2M1_EFQ"), ("E2M3", "E3M2")]
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -31,7 +31,7 @@ MASK = {0: 0x00000000, 1: 0xFFFFFFFF}          # exp mode -> hardware-exp2 posit
 def _codes_from_words(words, fmt_pv):
     """[R, nkt, 32] uint32 words -> [R, nkt*128] codes in key order."""
     b = np.ascontiguousarray(words.astype(np.uint32)).view(np.uint8).reshape(words.shape[0], words.shape[1], 128)
-    if fmt_pv in ("E4M3", "E2M3"):
+    if fmt_pv in ("E4M3", "E2M3", "E3M2"):
         return b.reshape(words.shape[0], -1)
     nib = b[:, :, :64]
     return np.stack([nib & 0x0F, nib >> 4], axis=-1).reshape(words.shape[0], -1)
@@ -113,6 +113,8 @@ SMALL = [
     (Workload("pg_e2m1_mufu", 1, 2, 2, 300, 300, 64, True, "E2M1", "E2M1", 34), 1, 8.0),
     (Workload("pg_efq", 1, 4, 2, 512, 1024, 128, True, "E2M1", "E2M1_EFQ", 35, "planted"), 1, 0.0),
     (Workload("pg_efq_d64", 1, 2, 1, 200, 700, 64, False, "E2M1", "E2M1_EFQ", 36), 1, 8.0),
+    (Workload("pg_e3m2", 1, 2, 1, 256, 520, 128, True, "E3M2", "E3M2", 38, "planted"), 0, 0.0),
+    (Workload("pg_e3m2_mufu", 1, 2, 1, 300, 300, 64, False, "E3M2", "E3M2", 39), 1, 8.0),
 ]
 
 

@@ -10,7 +10,7 @@ from gpu_layout import unpack_rows, unpack_cols
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-FMTS = [0, 1, 2]
+FMTS = [0, 1, 2, 4]
 
 
 def _fsa():
@@ -110,6 +110,8 @@ def test_quant_full_workloads(name):
     (1, 2, 1, 2, 2, 77, 200, 64),        # E2M3 / E2M1, rectangular, D 64
     (2, 2, 2, 3, 1, 129, 1, 128),        # one key
     (2, 0, 1, 1, 1, 512, 384, 64),
+    (4, 4, 1, 2, 1, 300, 260, 128),      # E3M2 both
+    (4, 2, 1, 2, 2, 100, 130, 64),
 ])
 def test_quant_qkv_one_launch(fq, fv, B, H, Hkv, Sq, Sk, D):
     """The one-launch Q/K/V form writes the codes and scales of three separate

@@ -193,8 +193,7 @@ typedef struct {
   int32_t  reserved;
   const fsa_debug_dump* debug;  /* optional (NULL: none): run the debug instance, which
                             also writes the per-tile dumps; per-query-tile schedule,
-                            formats with fmt_qk == fmt_pv or E2M1 with E2M1_EFQ, exp
-                            modes POLY and MUFU (else FSA_ERR_UNSUPPORTED_FMT) */
+                            exp modes POLY and MUFU (else FSA_ERR_UNSUPPORTED_FMT) */
 } fsa_opts;
 
 typedef enum {

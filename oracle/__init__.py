@@ -67,7 +67,7 @@ class FsaOpts(ctypes.Structure):
 class FsaDump(ctypes.Structure):
     _fields_ = [("s", ctypes.c_void_p), ("p_codes", ctypes.c_void_p), ("p_scales", ctypes.c_void_p),
                 ("m_frozen", ctypes.c_void_p), ("amb", ctypes.c_void_p), ("s_in", ctypes.c_void_p),
-                ("p_alt", ctypes.c_void_p)]
+                ("p_alt", ctypes.c_void_p), ("p_in", ctypes.c_void_p)]
 
 
 def lib():
@@ -224,7 +224,8 @@ EFQ_A, EFQ_B, EFQ_PHI = 1.6875, 3.5, 0.5625      # the EFQ rule's constants (see
 
 
 def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_mask=0, beta=EFQ_B,
-                efq_a=EFQ_A, phi=EFQ_PHI, dump=False, ambiguity=False, s_perturb=0.0, s_in=None, nthreads=None):
+                efq_a=EFQ_A, phi=EFQ_PHI, dump=False, ambiguity=False, s_perturb=0.0, s_in=None, p_in=None,
+                nthreads=None):
     """Step-by-step emulation of the fused MX forward.  fmt_p: 0/1/2/4 exp path, 3 EFQ.
 
     EFQ codes are clamp(rne(fmaf(s, fp32(efq_a c), fp32(beta - fp32(efq_a (M + E))))), 0, 7)
@@ -232,6 +233,9 @@ def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_ma
     path keeps the OCP rule).  s_in (float32 [rows, Skp], optional): raw scores to use
     instead of the emulation's own (a kernel's scores); with dump=True the result then
     also holds p_alt, the code at the other end of the hardware exp2's uncertainty.
+    p_in (uint8 [rows, Skp], optional): P codes to accumulate instead of the
+    emulation's own (a kernel's codes, once checked against p_codes / p_alt); the
+    ambiguity bound then leaves out code decisions.
 
     Returns dict(out, fallbacks, tiles); with dump=True also s/p_codes/p_scales/m_frozen;
     with ambiguity=True also amb [rows, D]: the bound on how far a kernel output may lie
@@ -248,8 +252,12 @@ def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_ma
     tv = np.zeros(n, np.int32)
     res = dict(out=out, fallbacks=fb, tiles=tv)
     d = None
-    if dump or ambiguity or s_in is not None:
-        d = FsaDump(None, None, None, None, None, None, None)
+    if dump or ambiguity or s_in is not None or p_in is not None:
+        d = FsaDump(None, None, None, None, None, None, None, None)
+    if p_in is not None:
+        p_in = np.ascontiguousarray(p_in, np.uint8)
+        assert p_in.shape == (n, Skp)
+        d.p_in = p_in.ctypes.data
     if s_in is not None:
         s_in = np.ascontiguousarray(s_in, np.float32)
         assert s_in.shape == (n, Skp)

@@ -523,6 +523,9 @@ typedef struct {      /* optional per-row dumps, NULL to skip */
                          (a kernel's own scores, so that steps 2-6 can be checked given them) */
   uint8_t* p_alt;     /* [nrows][Skp] the code at the other end of the exp2 uncertainty
                          (AMB_X) for hardware-exp2 positions; equal to p_codes elsewhere */
+  const uint8_t* p_in;/* optional input [nrows][Skp]: P codes to accumulate instead of step
+                         5's (a kernel's own codes, once checked against p_codes / p_alt);
+                         p_codes still reports the emulation's own */
 } orc_fsa_dump;
 
 /* Decisions the kernel takes in fp32 that this emulation cannot reproduce bit for
@@ -698,8 +701,9 @@ void orc_fsa_emulate(const orc_mx_operands* op, const orc_geom* g, float scale, 
                 }
               }
               if (dump && dump->p_alt) dump->p_alt[n * Skp + j] = (uint8_t)alt;
-              pt[j - j0] = orc_decode(efmt, code) * sc;
-              if (A && s[j - j0] != -INFINITY) {
+              const uint32_t used = (dump && dump->p_in) ? dump->p_in[n * Skp + j] : code;
+              pt[j - j0] = orc_decode(efmt, used) * sc;
+              if (A && s[j - j0] != -INFINITY && !(dump && dump->p_in)) {   /* given codes: determined */
                 double dp = 0.0;
                 if (blk_undet) {
                   /* requantised one exponent step finer or coarser */

@@ -84,6 +84,8 @@ M = [
  ("exact no max shift", "        if (s[j] > m) m = s[j];\n      }\n      double l = 0.0;",
   "        m = 0.0;\n      }\n      double l = 0.0;"),
  ("amb ignores fallback test", "<= dx + dM + rt * fabs(thr) && rt > 0.0) undetermined = 1;", "< 0.0) undetermined = 1;"),
+ ("given codes ignored", "const uint32_t used = (dump && dump->p_in) ? dump->p_in[n * Skp + j] : code;",
+  "const uint32_t used = code;"),
  ("given scores ignored", "            s[j - j0] = (dump && dump->s_in) ? dump->s_in[n * Skp + j] : (float)(acc * (1.0 + opt->s_perturb));",
   "            s[j - j0] = (float)(acc * (1.0 + opt->s_perturb));"),
  ("amb alpha exact", "const double ra = 0.6931471805599453 * (dM + dx) + AMB_X;", "const double ra = 0.0;"),

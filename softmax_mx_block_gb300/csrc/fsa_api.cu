@@ -349,8 +349,6 @@ int attention_impl(const fsa_mx_tensor* q, const void* q_bf16, const fsa_mx_tens
     return FSA_ERR_INVALID_ARG;
   const fsa_debug_dump* dbg = o.debug;
   if (dbg && (!dbg->s || !dbg->m || !dbg->p || !dbg->p_scales)) return FSA_ERR_INVALID_ARG;
-  if (dbg && !(fmt_qk == storage_fmt(fmt_pv) || (fmt_qk == FSA_FMT_E2M1 && fmt_pv == FSA_FMT_E2M1_EFQ)))
-    return FSA_ERR_UNSUPPORTED_FMT;
   if (dbg && fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode == FSA_EXP_SPLIT) return FSA_ERR_UNSUPPORTED_FMT;
   // Q quantised in the prologue: one CTA per query tile, the hardware exp2 (or EFQ)
   if (q_bf16 && (dbg || o.schedule == FSA_SCHED_PERSISTENT ||

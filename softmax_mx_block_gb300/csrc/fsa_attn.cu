@@ -973,11 +973,10 @@ static cudaError_t launch_persistent(const AttnLaunch& a) {
   return cudaGetLastError();
 }
 
-// The debug instance exists for the pairs whose QK^T and PV formats agree and for
-// E2M1 QK^T with EFQ P (the P~ generation depends on the PV format only), with the
-// cubic or the hardware exp2, under the per-query-tile schedule.
+// The debug instance exists for every MX format pair with the cubic or the hardware
+// exp2, under the per-query-tile schedule.
 template <int FQK, int FPV>
-constexpr bool kHasDebug = FQK != F_BF16 && (FQK == FPV || (FQK == F_E2M1 && FPV == F_EFQ));
+constexpr bool kHasDebug = FQK != F_BF16;
 
 template <int FQK, int FPV, int D, int EXPM>
 static cudaError_t launch_sched(const AttnLaunch& a) {

@@ -3,16 +3,19 @@
 seeded samples of query rows per head (256 where the oracle affords it).
 
 The tensor core's fp32 scores are the one input the oracle cannot reproduce bit for
-bit (the MMA's internal accumulation order is not specified).  So each case also runs
-the kernel's debug instance, which computes the same output bit for bit (asserted)
-and dumps, for the sampled rows, every tile's scores, frozen maximum and P~ words.
-Given those scores the oracle replays the algorithm: the frozen maxima, the block
-scales, the per-row fallback counts and the codes must agree exactly (a code at a
-hardware-exp2 position may also be the one at the other end of the exp2's
-uncertainty), and the output must agree within 2e-3 * rms plus `amb`, the bound of
-what the hardware exp2 alone leaves undetermined; that slack is capped and reported.
-Finally the error against fp64 exact attention must stay within the operand-
-quantisation floor (Fused-Softmax brief, abstract) on every sampled row."""
+bit (the MMA's internal accumulation order is not specified), and the hardware exp2
+is only specified to about 2 ulp.  So each case also runs the kernel's debug
+instance, which computes the same output bit for bit (asserted) and dumps, for the
+sampled rows, every tile's scores, frozen maximum and P~ words.  The scores are
+checked against the oracle's exactly rounded ones; given them, the oracle replays
+the algorithm: the frozen maxima, the block scales and the per-row fallback counts
+must agree exactly, and every code must be the oracle's, or at a hardware-exp2
+position the code at the other end of the exp2's uncertainty (counted and
+reported).  Given those codes, the oracle's accumulation must agree with the kernel's
+output within 2e-3 * rms plus `amb`, which is then only the hardware exp2 of a
+fallback's factor (capped: at most 2e-3 * rms).  Finally the error against fp64
+exact attention must stay within the operand-quantisation floor (Fused-Softmax
+brief, abstract) on every sampled row."""
 import numpy as np
 import pytest
 
@@ -61,22 +64,23 @@ def test_full_size_sampled_rows(name, per_head):
     assert np.array_equal(dout.cpu().numpy().reshape(-1, w.D).view(np.uint32), gpu["out"].view(np.uint32))
     assert dst == gpu["stats"]
     mx = oracle.MxInputs.from_bf16(q, k, v, fq, 2 if fp == 3 else fp)
-    res = compare_pgen(w, q, k, v, 1, 8.0, rows, dump, mx=mx, ambiguity=True, own_scores=False)
+    res = compare_pgen(w, q, k, v, 1, 8.0, rows, dump, mx=mx, score_rows=1024, outputs=True)
     del dump
-    given = res["given"]
-    assert np.array_equal(gpu["row_fallbacks"][rows], given["fallbacks"])
-    emu, amb = given["out"], given["amb"]
+    assert np.array_equal(gpu["row_fallbacks"][rows], res["given"]["fallbacks"])
+    emu, amb = res["replay"]["out"], res["replay"]["amb"]
     o = gpu["out"][rows]
     rms = np.sqrt(np.mean(emu ** 2))
-    # what the hardware exp2 leaves undetermined: few rows, small
     slack_rows = int(np.sum((amb > 0).any(axis=1)))
-    print(f"{name}: {len(rows)} rows, {slack_rows} with exp2 slack, max slack {amb.max() / rms:.2e} rms, "
-          f"{res['n_alt']} of {res['n']} codes at the exp2's other end")
-    assert np.isfinite(amb).all()
-    assert slack_rows <= 0.01 * len(rows)
-    assert amb.max() <= TOL_EMU * rms
+    print(f"{name}: {len(rows)} rows; {res['n_alt']} of {res['n']} codes at the exp2's other end; "
+          f"{slack_rows} rows with a fallback factor's slack, max {amb.max() / rms:.2e} rms; "
+          f"max |O - O_emu| {np.abs(o - emu).max() / rms:.2e} rms")
+    assert res["n_alt"] <= 1e-5 * res["n"]
+    assert np.isfinite(amb).all() and amb.max() <= TOL_EMU * rms
     excess = np.abs(o - emu) - amb - TOL_EMU * rms
     assert np.all(excess <= 0.0), f"{name}: |O-O_emu| exceeds 2e-3*rms + amb by {excess.max():.3e}"
+    # the kernel's output against the oracle's own codes: only the rare exp2-boundary codes differ
+    own = res["given"]["out"]
+    print(f"{name}: max |O - O_emu(own codes)| {np.abs(o - own).max() / rms:.2e} rms")
     # error against fp64 exact attention within the operand-quantisation floor
     fl = oracle.attn_floor(mx, w.Sk, w.causal, w.scale, 2 if fp == 3 else fp, rows)
     ex = oracle.attn_exact(q, k, v, w.causal, w.scale, rows)

@@ -58,29 +58,34 @@ def run_debug(w: Workload, q, k, v, exp_mode, delta, rows=None, mx_dev=None):
     return out, dump, st, rf
 
 
-def compare_pgen(w: Workload, q, k, v, exp_mode, delta, rows, dump, mx=None, ambiguity=False, own_scores=True):
+def compare_pgen(w: Workload, q, k, v, exp_mode, delta, rows, dump, mx=None, score_rows=None, outputs=False):
     """Checks the dumped M, scale bytes and codes of the sampled rows against the
-    oracle's replay on the dumped scores; returns the replay (with the ambiguity bound
-    when asked) and counts."""
+    oracle's replay on the dumped scores (after checking those scores against the
+    oracle's exactly rounded ones, on the first `score_rows` rows, all by default).
+    With outputs=True also replays the accumulation on the kernel's own codes (once
+    they are checked) and returns that output with its ambiguity bound (left: the
+    hardware exp2 of a fallback's factor)."""
     fq, fp = FMT[w.fmt_qk], FMT[w.fmt_pv]
     if mx is None:
         mx = oracle.MxInputs.from_bf16(q, k, v, fq, 2 if fp == 3 else fp)
     skp = (w.Sk + 31) // 32 * 32
     nkt = (w.Sk + 127) // 128
-    s_gpu = dump.s.cpu().numpy()
+    s_gpu = dump.s.cpu().numpy()[:, :skp]
     m_gpu = dump.m.cpu().numpy()
     p_gpu = _codes_from_words(dump.p.cpu().numpy(), w.fmt_pv)
     sf_gpu = dump.p_scales.cpu().numpy().astype(np.uint32).view(np.uint8).reshape(len(rows), -1)
     mask = MASK[exp_mode] if fp != 3 else 0
+    # the kernel's scores against the oracle's exactly rounded ones (a valid result of
+    # the unspecified fp32 accumulation order: within 2^-21 of the block partial sums)
+    ns = len(rows) if score_rows is None else min(score_rows, len(rows))
+    own = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows[:ns], delta=delta, mufu_mask=mask, dump=True)
+    vis = np.isfinite(own["s"])
+    assert np.array_equal(vis, np.isfinite(s_gpu[:ns])), "masked keys differ"
+    ds = np.abs(s_gpu[:ns][vis] - own["s"][vis])
+    assert ds.max() <= 1e-5 * np.abs(own["s"][vis]).max() + 1e-6
+    del own
     given = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=delta, mufu_mask=mask, dump=True,
-                               s_in=s_gpu[:, :skp], ambiguity=ambiguity)
-    if own_scores:
-        # the kernel's scores against the oracle's exactly rounded ones
-        own = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=delta, mufu_mask=mask, dump=True)
-        vis = np.isfinite(own["s"])
-        assert np.array_equal(vis, np.isfinite(s_gpu[:, :skp])), "masked keys differ"
-        ds = np.abs(s_gpu[:, :skp][vis] - own["s"][vis])
-        assert ds.max() <= 1e-5 * np.abs(own["s"][vis]).max() + 1e-6
+                               s_in=s_gpu)
     # frozen maximum of every visited tile, bit for bit
     seen = ~np.isnan(given["m_frozen"])
     assert np.array_equal(m_gpu[:, :nkt][seen].view(np.uint32), given["m_frozen"][seen].view(np.uint32))
@@ -93,7 +98,11 @@ def compare_pgen(w: Workload, q, k, v, exp_mode, delta, rows, dump, mx=None, amb
     assert np.all(exact | alt_ok), f"{int(np.sum(~(exact | alt_ok)))} codes outside the allowed set"
     if exp_mode == 0 or fp == 3:
         assert np.all(exact)
-    return dict(n_alt=int(np.sum(~exact)), n=int(exact.size), given=given)
+    res = dict(n_alt=int(np.sum(~exact)), n=int(exact.size), given=given)
+    if outputs:
+        res["replay"] = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=delta, mufu_mask=mask,
+                                           s_in=s_gpu, p_in=pg, ambiguity=True)
+    return res
 
 
 def check_pgen(w: Workload, q, k, v, exp_mode, delta, rows):

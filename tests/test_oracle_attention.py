@@ -507,3 +507,29 @@ def test_emulate_given_scores_drive_the_algorithm():
     assert moved["fallbacks"][row] == base["fallbacks"][row] + (0 if base["m_frozen"][row, 2] >= np.float32(s2[row, key] * c) else 1)
     assert moved["m_frozen"][row, 2] == np.float32(s2[row, key] * c)
     assert moved["p_codes"][row, key] == min(7, int(np.round(oracle.EFQ_A * 2 + oracle.EFQ_B)))
+
+
+def test_emulate_given_codes_are_accumulated():
+    """p_in replaces the P codes that are accumulated: the emulation's own codes back
+    give the same output; zeroing the code of one key removes exactly that key's term,
+    o' = (o l - p v) / (l - p), with p its decoded code times the block scale and l
+    the row's sum of decoded P."""
+    B, H, S, D = 1, 1, 128, 64
+    q, k, v = rnd((B, H, S, D), 41), rnd((B, H, S, D), 42), rnd((B, H, S, D), 43)
+    rows = allrows(B, H, S)
+    mx = oracle.MxInputs.from_bf16(q, k, v, 0, 0)
+    base = oracle.fsa_emulate(mx, S, False, 0.125, 0, rows, delta=8.0, dump=True)
+    same = oracle.fsa_emulate(mx, S, False, 0.125, 0, rows, delta=8.0, dump=True, p_in=base["p_codes"])
+    assert np.array_equal(base["out"], same["out"])
+    row, key = 17, 40
+    pc = base["p_codes"].copy()
+    pc[row, key] = 0
+    cut = oracle.fsa_emulate(mx, S, False, 0.125, 0, rows, delta=8.0, p_in=pc)
+    sc = 2.0 ** (base["p_scales"][row].astype(np.int64) - 127)
+    p = oracle.decode_array(0, base["p_codes"][row]) * np.repeat(sc, 32)
+    l = p.sum()
+    vh = oracle.decode_array(0, mx.vc[0, 0]) * 2.0 ** (np.repeat(mx.vs[0, 0].astype(np.int64), 32, -1) - 127)
+    expect = (base["out"][row] * l - p[key] * vh[:, key]) / (l - p[key])
+    assert np.allclose(cut["out"][row], expect, rtol=1e-12, atol=1e-15)
+    others = np.arange(S) != row
+    assert np.array_equal(cut["out"][others], base["out"][others])

@@ -316,8 +316,9 @@ int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, floa
  * scaled matrix cores).  Launches n_ctas CTAs (one per SM) that each issue
  * `iters` iterations of dense M=128, N=n (128 or 256), K=128 products from
  * shared-memory operand tiles into tensor memory, as 8 kind::f16 bf16 MMAs
- * (kind 0), 4 kind::mxf8f6f4 E4M3 block-scaled MMAs (kind 1) or 2 kind::mxf4
- * E2M1 block-scaled MMAs (kind 2).  *flops (host, optional) receives the
+ * (kind 0), 4 kind::mxf8f6f4 E4M3 block-scaled MMAs (kind 1), 2 kind::mxf4
+ * E2M1 block-scaled MMAs (kind 2) or 2 kind::mxf4nvf4 MMAs on the same MXFP4
+ * operands (E2M1, E8M0 scales, scale_vec::2X; kind 3).  *flops (host, optional) receives the
  * launch's 2*M*N*K*iters*n_ctas; time the launch with events on `stream`.
  * status: optional device int32, set to FSA_ERR_TIMEOUT if the final wait
  * (2 s) expires.  Errors: FSA_ERR_INVALID_ARG, FSA_ERR_LAUNCH. */

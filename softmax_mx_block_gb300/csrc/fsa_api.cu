@@ -482,7 +482,7 @@ int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, floa
 }
 
 int fsa_mma_peak(int kind, int n, int n_ctas, long long iters, int32_t* status, double* flops, void* stream) {
-  if (kind < 0 || kind > 2 || (n != 128 && n != 256) || n_ctas <= 0 || n_ctas > 65535 || iters <= 0 ||
+  if (kind < 0 || kind > 3 || (n != 128 && n != 256) || n_ctas <= 0 || n_ctas > 65535 || iters <= 0 ||
       iters > (1ll << 40))
     return FSA_ERR_INVALID_ARG;
   if (flops) *flops = fsa::mma_peak_flops_per_iter(kind, n) * (double)iters * (double)n_ctas;

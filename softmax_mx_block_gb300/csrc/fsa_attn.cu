@@ -445,9 +445,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (MX) bulk_load(sm + C::OFF_SFK + st * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + st);
           ++nk;
         }
-        mbar_wait_drain(QF ? qraw_full : q_full, 0, p.timeout_ns);
+        mbar_drain(QF ? qraw_full : q_full, 0, ac);
         for (int st = 0; st < C::NS && st < nk; ++st)
-          mbar_wait_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, p.timeout_ns);
+          mbar_drain(k_full + st, ((nk - 1 - st) / C::NS) & 1, ac);
       } else {
         // V(j) as soon as V slot j % NS is free (PV(j - NS) done)
         int nv = min(C::NS, nT);
@@ -462,7 +462,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ++nv;
         }
         for (int st = 0; st < C::NS && st < nv; ++st)
-          mbar_wait_drain(v_full + st, ((nv - 1 - st) / C::NS) & 1, p.timeout_ns);
+          mbar_drain(v_full + st, ((nv - 1 - st) / C::NS) & 1, ac);
       }
     }
     __syncwarp();
@@ -597,7 +597,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       // all MMAs and copies issued by this warp complete before tensor memory is freed
       tc_commit_p(elect_u32(), drain);
-      mbar_wait_drain(drain, 0, p.timeout_ns);
+      mbar_drain(drain, 0, ac);
     }
     __syncwarp();
   } else {

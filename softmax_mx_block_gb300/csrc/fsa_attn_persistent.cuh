@@ -487,12 +487,12 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       // (g counts the key tiles requested, those of the setup included)
       if (lane == 0) {
         for (int qb = 0; qb < 2 && qb < nq; ++qb)
-          mbar_wait_drain(q_full + qb, ((nq - 1 - qb) >> 1) & 1, p.timeout_ns);
+          mbar_drain(q_full + qb, ((nq - 1 - qb) >> 1) & 1, ac);
         for (int st = 0; st < C::NS && st < g; ++st)
-          mbar_wait_drain(k_full + st, ((g - 1 - st) / C::NS) & 1, p.timeout_ns);
+          mbar_drain(k_full + st, ((g - 1 - st) / C::NS) & 1, ac);
       } else {
         for (int st = 0; st < C::NS && st < g; ++st)
-          mbar_wait_drain(v_full + st, ((g - 1 - st) / C::NS) & 1, p.timeout_ns);
+          mbar_drain(v_full + st, ((g - 1 - st) / C::NS) & 1, ac);
       }
     }
     __syncwarp();
@@ -653,7 +653,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     // all MMAs and copies issued by this warp complete before tensor memory is freed
     tc_commit_p(elect_u32(), drain);
-    mbar_wait_drain(drain, 0, p.timeout_ns);
+    mbar_drain(drain, 0, ac);
     __syncwarp();
   } else {
     // =============================================================== softmax / epilogue

@@ -12,6 +12,8 @@
 //   kind 0  kind::f16, bf16 x bf16,                         K = 16 per MMA
 //   kind 1  kind::mxf8f6f4 block_scale scale_vec::1X, E4M3, K = 32 per MMA
 //   kind 2  kind::mxf4 block_scale scale_vec::2X, E2M1,     K = 64 per MMA
+//   kind 3  kind::mxf4nvf4 block_scale scale_vec::2X, E2M1 with E8M0 scales (the
+//           same MXFP4 operands through the NVFP4-capable kind), K = 64 per MMA
 // The operand bytes are a fixed finite pattern (values do not change the
 // instruction rate); scales are 2^0.  The final commit is awaited with a bounded
 // wait; on expiry the status word gets FSA_ERR_TIMEOUT.
@@ -35,7 +37,7 @@ template <int KIND, int N>
 __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long iters, int* status,
                                                                        uint64_t timeout_ns) {
   // bytes per operand row (K = 128 elements) and the swizzle atom of the tiles
-  constexpr int RB = KIND == 0 ? 256 : (KIND == 1 ? 128 : 64);
+  constexpr int RB = KIND == 0 ? 256 : (KIND == 1 ? 128 : 64);   // kinds 2, 3: packed E2M1
   constexpr int W = RB < 128 ? RB : 128;
   constexpr int STEPS = RB / 32;            // 32 bytes of K per MMA
   constexpr uint32_t SWZ = W == 128 ? 2u : 4u;
@@ -86,8 +88,10 @@ __global__ void __launch_bounds__(kPeakThreads, 1) fsa_mma_peak_kernel(long long
           mma_f16_ss_p(e, d, ad, bd, idesc_f16_bf16(N), acc);
         } else if constexpr (KIND == 1) {
           mma_mxf8f6f4_ss_p(e, d, ad, bd, idesc_bs(N, 0, i, i), tbase + T_SFA, tbase + T_SFB, acc);
-        } else {
+        } else if constexpr (KIND == 2) {
           mma_mxf4_ss_p(e, d, ad, bd, idesc_bs(N, 1, 2 * i, 2 * i), tbase + T_SFA, tbase + T_SFB, acc);
+        } else {
+          mma_mxf4nvf4_ss_p(e, d, ad, bd, idesc_bs(N, 1, 2 * i, 2 * i), tbase + T_SFA, tbase + T_SFB, acc);
         }
       }
       acc_buf = acc_buf == NACC - 1 ? 0 : acc_buf + 1;
@@ -121,11 +125,13 @@ cudaError_t launch_mma_peak(int kind, int n, int n_ctas, long long iters, int* s
   if (n == 256) {
     if (kind == 0) return run(fsa_mma_peak_kernel<0, 256>);
     if (kind == 1) return run(fsa_mma_peak_kernel<1, 256>);
-    return run(fsa_mma_peak_kernel<2, 256>);
+    if (kind == 2) return run(fsa_mma_peak_kernel<2, 256>);
+    return run(fsa_mma_peak_kernel<3, 256>);
   }
   if (kind == 0) return run(fsa_mma_peak_kernel<0, 128>);
   if (kind == 1) return run(fsa_mma_peak_kernel<1, 128>);
-  return run(fsa_mma_peak_kernel<2, 128>);
+  if (kind == 2) return run(fsa_mma_peak_kernel<2, 128>);
+  return run(fsa_mma_peak_kernel<3, 128>);
 }
 
 }  // namespace fsa

@@ -92,6 +92,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// Teardown wait for work this CTA still has in flight (copies, MMAs).  On expiry the
+// CTA is marked aborted and the status word gets FSA_ERR_TIMEOUT, so the caller
+// learns that the teardown was not clean (the output is then undefined).
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, const AbortCtl& ac) {
+  if (mbar_wait_drain(bar, parity, ac.limit_ns)) return true;
+  *ac.flag = 1;
+  if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
+  return false;
+}
+
 // One lane of a converged warp (the lowest active one) gets true.  The tcgen05
 // issuing warp runs converged and elects its issuing lane per instruction.
 __device__ __forceinline__ bool elect_one() {
@@ -250,6 +260,14 @@ __device__ __forceinline__ void mma_mxf4_ss_p(uint32_t e, uint32_t d, uint64_t a
                                               uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
                "@q tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
+}
+// kind::mxf4nvf4 with scale_vec::2X and E8M0 scales: the same MXFP4 operands (E2M1,
+// one scale per 32 elements) through the NVFP4-capable instruction kind.
+__device__ __forceinline__ void mma_mxf4nvf4_ss_p(uint32_t e, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                  uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}"
                ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
 }
 __device__ __forceinline__ void mma_mxf4_ts_p(uint32_t e, uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,

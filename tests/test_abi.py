@@ -229,6 +229,6 @@ def test_tune_delta_host_logic(lib):
 def test_mma_peak_argument_checks(lib):
     import softmax_mx_block_gb300 as fsa
     fl = ctypes.c_double()
-    for kind, nn, n, it in ((3, 128, 1, 1), (-1, 128, 1, 1), (1, 64, 1, 1), (1, 128, 0, 1), (1, 256, 1, 0),
+    for kind, nn, n, it in ((4, 128, 1, 1), (-1, 128, 1, 1), (1, 64, 1, 1), (1, 128, 0, 1), (1, 256, 1, 0),
                             (1, 128, 70000, 1)):
         assert lib.fsa_mma_peak(kind, nn, n, it, None, ctypes.byref(fl), None) == fsa.FSA_ERR_INVALID_ARG

@@ -104,7 +104,7 @@ def test_layer_schedule_matches_single_calls():
 
 
 @pytest.mark.parametrize("n", [128, 256])
-@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("kind", [0, 1, 2, 3])
 def test_mma_peak_probe_runs(kind, n):
     """The throughput probe completes without a timeout on every SM and reports a
     plausible rate (a few hundred TFLOP/s at least for a short launch)."""

@@ -155,13 +155,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 
 // Exponent-only block scale: E = clamp(floor(fp32(fp32(smax*c) - M)) - emax, -127, 127).
 // Returns E and writes -fp32(M + E).  A block with no visible key (smax = -inf)
-// gets E = -127; its scores are -inf, so every code comes out 0.
+// gets E = -127; its scores are -inf, so every code comes out 0.  A row with no
+// visible key at all so far (M = -inf: causal rows before the first key) gets the
+// shift 0, so that its residuals are -inf as well (not -inf + inf, whose NaN a
+// format without a NaN code would saturate to a nonzero code).
 template <int FPV>
 __device__ __forceinline__ int block_exp(float bmax, float c, float M, float& nbE) {
   const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
   int E = (int)fmaxf(floorf(tmax), -256.0f) - Fmt<FPV>::emax;
   E = E < -127 ? -127 : (E > 127 ? 127 : E);
-  nbE = -__fadd_rn(M, (float)E);
+  nbE = M == kNegInf ? 0.0f : -__fadd_rn(M, (float)E);
   return E;
 }
 

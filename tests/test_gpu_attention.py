@@ -112,13 +112,18 @@ def test_exp_modes(exp_mode, mask):
     check(w, gpu, oracle_mx(w, q, k, v, rows, mask), rows)
 
 
-def test_rectangular_causal_and_empty_rows():
-    # Sq > Sk with causal bottom-right alignment: the first Sq - Sk queries see no key
-    w = Workload("rect", 1, 2, 1, 300, 200, 128, True, "E4M3", "E4M3", 9)
+@pytest.mark.parametrize("fq,fp,exp_mode,mask", [("E4M3", "E4M3", 2, SPLIT_MASK), ("E2M3", "E2M1", 1, 0xFFFFFFFF),
+                                                 ("E3M2", "E3M2", 1, 0xFFFFFFFF), ("E2M1", "E2M1", 0, 0),
+                                                 ("E2M1", "E2M1_EFQ", 1, 0)])
+def test_rectangular_causal_and_empty_rows(fq, fp, exp_mode, mask):
+    """Sq > Sk with causal bottom-right alignment: the first Sq - Sk queries see no key
+    and get zero rows, also when they share a query tile with rows that have keys (a
+    row whose frozen maximum is still -inf must produce zero codes in every format)."""
+    w = Workload("rect", 1, 2, 1, 300, 200, 128, True, fq, fp, 9)
     q, k, v = generate(w)
     rows = sample_rows(w)
-    gpu = run_mx(w, q, k, v)
-    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK, with_floor=False)
+    gpu = run_mx(w, q, k, v, exp_mode=exp_mode)
+    orc = oracle_mx(w, q, k, v, rows, mask, with_floor=False)
     empty = [r for r in rows if (r % w.Sq) < w.Sq - w.Sk]
     assert np.all(gpu["out"][empty] == 0.0)
     check(w, gpu, orc, rows)

@@ -380,6 +380,13 @@ int attention_impl(const fsa_mx_tensor* q, const void* q_bf16, const fsa_mx_tens
   }
   a.D = D;
   a.exp_mode = o.exp_mode;
+  if (fmt_pv == FSA_FMT_E2M1_EFQ) {
+    // EFQ codes need no fix when they cannot exceed 7: every block's largest residual
+    // is below 3 - phi unless its exponent is clamped from above (margin <= 120 rules
+    // that out), so a (3 - phi) + b < 7.49 keeps every rounded code at 7 or below
+    const double top = (double)o.efq_a * (3.0 - (double)o.efq_phi) + (double)o.efq_b;
+    a.exp_mode = (o.delta <= 120.0f && top < 7.49) ? 1 : 0;
+  }
   a.persistent = persistent ? 1 : 0;
   a.stream = static_cast<cudaStream_t>(stream);
   const cudaError_t e = impl_for(fmt_qk, fmt_pv)(a);

@@ -187,6 +187,10 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
     // exact, so z is fp32(y) / 8 clamped to [0, 1]); then z + 1.5*2^20 rounds 8z to
     // the nearest integer (ties to even) in the low bits of the sum.  A block with no
     // visible key has M + E = -inf, Bk = +inf and y NaN: sat gives 0.
+    // EXPM 1: the host has checked that codes cannot exceed 7 (every residual is
+    // below 3 - phi when the block exponent is not clamped from above, i.e. margin
+    // delta <= 120, and a (3 - phi) + b < 7.49), so the nibbles need no fix; EXPM 0:
+    // any constants, nibbles equal to 8 become 7.
     const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
     int E = (int)fmaxf(floorf(__fadd_rn(tmax, p.efq_phi)), -256.0f) - 2;
     E = E < -127 ? -127 : (E > 127 ? 127 : E);
@@ -210,8 +214,9 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
       const uint32_t a01 = (u[1] << 4) + u[0], a23 = (u[3] << 4) + u[2];
       const uint32_t a45 = (u[5] << 4) + u[4], a67 = (u[7] << 4) + u[6];
       const uint32_t wv = prmt(prmt(a01, a23, 0x0040u), prmt(a45, a67, 0x0040u), 0x5410u);
-      // codes are 0..8: turn each nibble equal to 8 into 7 (no nibble of 0..7 has bit 3)
-      out[w] = wv - ((wv >> 3) & 0x11111111u);
+      // EXPM 0: codes are 0..8; turn each nibble equal to 8 into 7 (no nibble of 0..7
+      // has bit 3)
+      out[w] = EXPM == 1 ? wv : wv - ((wv >> 3) & 0x11111111u);
     }
     return (uint32_t)(E + 127);
   } else {
@@ -342,7 +347,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* stall = s_full + 7;
   uint64_t* qraw_full = s_full + 8;             // QF: the bf16 Q tile landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
+  int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 8);
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
 
   if (threadIdx.x == 0) {
@@ -357,7 +362,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(drain, 1);
     mbar_init(stall, 1);
-    *abort_flag = 0;
+    sts_vol(abort_flag, 0);
     fence_mbar_init();
     if (nT > 0) {
       // the first loads overlap the rest of the setup (tensor memory, constant rows)
@@ -589,9 +594,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // bounded wait, abort check
         if (++idle == 1) t0 = globaltimer_ns();
         if ((idle & 7u) == 0) {
-          bool stop = *ac.flag != 0;
+          bool stop = lds_vol(ac.flag) != 0;
           if (!stop && globaltimer_ns() - t0 > ac.limit_ns) {
-            *ac.flag = 1;
+            sts_vol(ac.flag, 1);
             if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
             stop = true;
           }
@@ -630,7 +635,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (p.causal) lim = min(lim, row + p.Sk - p.Sq);
     const float c = p.c;
     const int bar_in = 1 + qd + 4 * pp, bar_out = 1 + qd + 4 * (1 - pp);
-    volatile float* m_slot = red + rl;              // M of this row after the latest tile
+    float* m_slot = red + rl;                       // M of this row after the latest tile
     float M = kNegInf;
     int nfb = 0, nvis = 0;
     bool ok = true;                                 // false once any wait failed: no more work
@@ -697,7 +702,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // M after tile j-1 comes from the other part (NaN: it has stopped working)
       if (j > 0) {
         named_bar_sync(bar_in, 64);
-        const float Mp = *m_slot;
+        const float Mp = lds_f32(m_slot);
         if (isnan(Mp)) ok = false;
         else M = Mp;
       }
@@ -716,7 +721,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       if (j + 1 < nT) {
-        *m_slot = ok ? Mn : __int_as_float(0x7FC00000);
+        sts_f32(m_slot, ok ? Mn : __int_as_float(0x7FC00000));
         named_bar_arrive(bar_out, 64);
       }
       const float alpha = rescale ? ex2_approx(__fsub_rn(M, Mn)) : 1.0f;
@@ -990,26 +995,27 @@ static cudaError_t launch_sched(const AttnLaunch& a) {
   // Q quantised in the prologue: the library's default exp2 path (and EFQ), one CTA
   // per query tile
   if (a.q_fused) {
-    if constexpr (EXPM == 1 && FQK != F_BF16) return launch_one<FQK, FPV, D, EXPM, false, true>(a);
+    if constexpr ((EXPM == 1 || FPV == F_EFQ) && FQK != F_BF16) return launch_one<FQK, FPV, D, EXPM, false, true>(a);
     return cudaErrorNotSupported;
   }
   return a.persistent ? launch_persistent<FQK, FPV, D, EXPM>(a) : launch_one<FQK, FPV, D, EXPM>(a);
 }
 
+// The exp-mode slot: 0/1/2 the exp2 path of the exp-then-round formats; for EFQ 1
+// when the codes need no fix (see pgen_block), else 0; BF16 has one path.
 template <int FQK, int FPV>
 cudaError_t launch_attn_impl(const AttnLaunch& a) {
-  // EFQ and BF16 have one P path (the exp-mode slot is unused)
-  constexpr bool one_path = FPV == F_EFQ || FPV == F_BF16;
-  if (a.D == 64) {
-    if constexpr (one_path) return launch_sched<FQK, FPV, 64, 1>(a);
-    else {
+  if constexpr (FPV == F_BF16) {
+    return a.D == 64 ? launch_sched<FQK, FPV, 64, 1>(a) : launch_sched<FQK, FPV, 128, 1>(a);
+  } else if constexpr (FPV == F_EFQ) {
+    if (a.D == 64) return a.exp_mode == 1 ? launch_sched<FQK, FPV, 64, 1>(a) : launch_sched<FQK, FPV, 64, 0>(a);
+    return a.exp_mode == 1 ? launch_sched<FQK, FPV, 128, 1>(a) : launch_sched<FQK, FPV, 128, 0>(a);
+  } else {
+    if (a.D == 64) {
       if (a.exp_mode == 0) return launch_sched<FQK, FPV, 64, 0>(a);
       if (a.exp_mode == 1) return launch_sched<FQK, FPV, 64, 1>(a);
       return launch_sched<FQK, FPV, 64, 2>(a);
     }
-  }
-  if constexpr (one_path) return launch_sched<FQK, FPV, 128, 1>(a);
-  else {
     if (a.exp_mode == 0) return launch_sched<FQK, FPV, 128, 0>(a);
     if (a.exp_mode == 1) return launch_sched<FQK, FPV, 128, 1>(a);
     return launch_sched<FQK, FPV, 128, 2>(a);

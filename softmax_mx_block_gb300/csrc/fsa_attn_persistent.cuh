@@ -148,7 +148,7 @@ struct TileState {
   bool ok;
 };
 template <int FQK, int FPV, int D, int EXPM>
-__device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full, uint64_t* pv_done, volatile float* m_slot,
+__device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full, uint64_t* pv_done, float* m_slot,
                                                 AbortCtl ac, const KParams& p, int pp, int qd,
                                                 int lim, int nT, int g0, bool ok) {
   using C = Cfg<FQK, FPV, D, true>;
@@ -201,7 +201,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
       // M after tile j-1 comes from the other part (NaN: it has stopped working)
       if (j > 0) {
         named_bar_sync(bar_in, 64);
-        const float Mp = *m_slot;
+        const float Mp = lds_f32(m_slot);
         if (isnan(Mp)) ok = false;
         else M = Mp;
       }
@@ -220,7 +220,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
         }
       }
       if (j + 1 < nT) {
-        *m_slot = ok ? Mn : __int_as_float(0x7FC00000);
+        sts_f32(m_slot, ok ? Mn : __int_as_float(0x7FC00000));
         named_bar_arrive(bar_out, 64);
       }
       const float alpha = rescale ? ex2_approx(__fsub_rn(M, Mn)) : 1.0f;
@@ -345,7 +345,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   uint64_t* drain = s_full + 7;
   uint64_t* stall = s_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC + 8);
+  int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 8);
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
 
   // the first query tile's Q and first ring of K/V tiles are requested while the rest
@@ -390,7 +390,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     mbar_init(o_free, C::NSW);
     mbar_init(drain, 1);
     mbar_init(stall, 1);
-    *abort_flag = 0;
+    sts_vol(abort_flag, 0);
     fence_mbar_init();
     if (it0.nT > 0) {
       load_q(it0, 0);
@@ -637,9 +637,9 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         // bounded wait, abort check
         if (++idle == 1) t0 = globaltimer_ns();
         if ((idle & 7u) == 0) {
-          bool stop = *ac.flag != 0;
+          bool stop = lds_vol(ac.flag) != 0;
           if (!stop && globaltimer_ns() - t0 > ac.limit_ns) {
-            *ac.flag = 1;
+            sts_vol(ac.flag, 1);
             if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
             stop = true;
           }
@@ -671,7 +671,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16);
     const float c = p.c;
     const int bar_in = 1 + qd + 4 * pp, bar_out = 1 + qd + 4 * (1 - pp);
-    volatile float* m_slot = red + rl;              // M of this row after the latest tile
+    float* m_slot = red + rl;                       // M of this row after the latest tile
     bool ok = true;                                 // false once any wait failed: no more work
     // every lane polls; the vote keeps the warp uniform
     auto wait0 = [&](uint64_t* bar, uint32_t parity) -> bool {

@@ -55,10 +55,30 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// Shared-memory scalars through explicit .shared accesses (a generic pointer to a
+// volatile would become a system-scope load or store).  Ordering against other
+// threads comes from the named barriers and mbarriers around them.
+__device__ __forceinline__ int lds_vol(const int* p) {
+  int v;
+  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_vol(int* p, int v) {
+  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ float lds_f32(const float* p) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f32(float* p, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_u32(p)), "f"(v) : "memory");
+}
+
 // Shared abort state of one CTA: once any wait gives up, every later wait of
 // the CTA returns false at once so that all roles drain and reach teardown.
 struct AbortCtl {
-  volatile int* flag;      // shared memory
+  int* flag;               // shared memory (lds_vol / sts_vol)
   int* status;             // global status word (may be null)
   uint64_t limit_ns;
 };
@@ -73,9 +93,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   for (uint32_t it = 1;; ++it) {
     if (SLEEP ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
     if ((it & 7u) == 0) {
-      if (*ac.flag) return false;
+      if (lds_vol(ac.flag)) return false;
       if (globaltimer_ns() - t0 > ac.limit_ns) {
-        *ac.flag = 1;
+        sts_vol(ac.flag, 1);
         if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
         return false;
       }
@@ -97,7 +117,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 // learns that the teardown was not clean (the output is then undefined).
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, const AbortCtl& ac) {
   if (mbar_wait_drain(bar, parity, ac.limit_ns)) return true;
-  *ac.flag = 1;
+  sts_vol(ac.flag, 1);
   if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
   return false;
 }

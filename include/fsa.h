@@ -169,8 +169,8 @@ typedef struct {
  * on the long-context workload (the error-floor criterion of the Fused-Softmax
  * brief, abstract). */
 #define FSA_EFQ_A_DEFAULT   1.6875f
-#define FSA_EFQ_B_DEFAULT   3.5f
-#define FSA_EFQ_PHI_DEFAULT 0.5625f
+#define FSA_EFQ_B_DEFAULT   3.4375f
+#define FSA_EFQ_PHI_DEFAULT 0.625f
 
 typedef struct {
   float    delta;        /* fallback margin in log2 units, >= 0 (default 8): a later tile falls

@@ -220,7 +220,7 @@ def attn_floor(mx: MxInputs, Sk, causal, scale, fmt_p, rows, quantize_p=True, nt
     return out
 
 
-EFQ_A, EFQ_B, EFQ_PHI = 1.6875, 3.5, 0.5625      # the EFQ rule's constants (see efq_scan.py)
+EFQ_A, EFQ_B, EFQ_PHI = 1.6875, 3.4375, 0.625      # the EFQ rule's constants (see efq_scan.py)
 
 
 def fsa_emulate(mx: MxInputs, Sk, causal, scale, fmt_p, rows, delta=0.0, mufu_mask=0, beta=EFQ_B,

@@ -14,9 +14,10 @@ SPLIT_MASK = 0x77777777          # key positions 4k+3 use the cubic, the rest th
 TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
 # error vs fp64 exact over the error of exact softmax with the same MX operands (the
 # floor): 1.1 for the exp-then-round paths; for the EFQ direct codes the largest ratio
-# the chosen rule reaches on the parity cases (1.117, small 300-key case at delta 8)
-# plus 5%
-FLOOR_EXP, FLOOR_EFQ = 1.1, 1.17
+# the chosen rule reaches on the parity cases plus 5%, by QK^T format: E2M1 1.121
+# (300 keys, non-causal, margin 8), E3M2 1.159 (300 keys, margin 0)
+FLOOR_EXP = 1.1
+FLOOR_EFQ = {"E2M1": 1.18, "E3M2": 1.22}
 
 
 def _fsa():
@@ -98,7 +99,7 @@ def test_small_formats(fq, fp, D, causal):
     rows = sample_rows(w)
     gpu = run_mx(w, q, k, v, row_fb=True)
     orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK)
-    ratio = FLOOR_EFQ if fp == "E2M1_EFQ" else FLOOR_EXP
+    ratio = FLOOR_EFQ[fq] if fp == "E2M1_EFQ" else FLOOR_EXP
     check(w, gpu, orc, rows, ratio)
     assert np.array_equal(gpu["row_fallbacks"][rows], orc["fallbacks"])
 

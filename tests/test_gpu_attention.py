@@ -216,7 +216,11 @@ def test_bf16_transpose_v():
     assert not got[..., 200:].any()
 
 
+# the library's constants (codes never above 7: the kernel skips the fix of code 8)
+# at margins 8 and 0, and with a margin above 120 (the fix path); other rules on both
+# sides of a (3 - phi) + b < 7.49
 EFQ_RULES = [(oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI, 8.0), (oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI, 0.0),
+             (oracle.EFQ_A, oracle.EFQ_B, oracle.EFQ_PHI, 200.0), (1.6875, 3.5, 0.5625, 8.0),
              (2.0, 2.0, 0.0, 8.0), (2.0, -3.0, 0.0, 8.0), (1.5, 3.0, 0.75, 120.0), (3.0, 5.5, 0.25, 50.0),
              (2.0, 2.0, 0.0, 200.0)]
 

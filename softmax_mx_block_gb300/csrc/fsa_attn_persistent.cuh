@@ -517,18 +517,14 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 12, one);
       }
     }
-    // shared-memory descriptors: loop-invariant bases whose start-address field
-    // (address / 16, bits 0-13) is advanced by each operand's offset; shared
-    // addresses stay below 2^18, so the field never carries into the next one
-    const uint64_t dQ = smem_desc(sQa, 16, 8 * C::W_QK, SWQ), dK = smem_desc(sKa, 16, 8 * C::W_QK, SWQ);
-    const uint64_t dV = smem_desc(sVa, 16, 8 * C::W_V, SWV);
-    const uint64_t dSFK = smem_desc(smem_u32(sm + C::OFF_SFK), 16, 128, 0);
-    const uint64_t dSFV = smem_desc(smem_u32(sm + C::OFF_SFV), 16, 128, 0);
     // PV of key tile g; `first`: the query tile's first, which overwrites O_aug
     auto issue_pv = [&](int g, bool first) {
       const int s = g & 1, st = g % C::NS;
       tc_fence_after();
-      if constexpr (MX) tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 8 * s, dSFV + (uint32_t)(st * (512 / 16)));
+      if constexpr (MX) {
+        const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFV + st * 512), 16, 128, 0);
+        tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 8 * s, sfd);
+      }
 #pragma unroll
       for (int i = 0; i < C::PV_STEPS; ++i) {
         // P~ of step i sits in columns [8i, 8i+8) of its P buffer; the scale word of
@@ -536,7 +532,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         const uint32_t a_tm = tbase + C::T_P + C::P_COLS * (g % C::NPB) + 8 * i;
         const uint32_t sfa = tbase + C::T_SFP + 4 * s;
         const int ka = (i * 32) / C::W_V, off = (i * 32) % C::W_V;
-        const uint64_t bd = dV + (uint32_t)((st * C::TILE_V + ka * C::VATOM + off) >> 4);
+        const uint64_t bd = smem_desc(sVa + st * C::TILE_V + ka * C::VATOM + off, 16, 8 * C::W_V, SWV);
         const uint32_t acc = (!first || i > 0) ? 1u : 0u;
         const uint32_t e = elect_u32();
         if constexpr (KIND_PV == 0) {
@@ -557,13 +553,15 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       const int s = g & 1, st = g % C::NS;
       const uint32_t t_sfq = qb ? C::T_SFQ1 : C::T_SFQ;
       tc_fence_after();
-      if constexpr (MX) tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFK + 4 * s, dSFK + (uint32_t)(st * (512 / 16)));
-      const uint64_t dQs = dQ + (uint32_t)(qb * (C::TILE_QK / 16)), dKs = dK + (uint32_t)(st * (C::TILE_QK / 16));
+      if constexpr (MX) {
+        const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFK + st * 512), 16, 128, 0);
+        tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFK + 4 * s, sfd);
+      }
 #pragma unroll
       for (int i = 0; i < C::QK_STEPS; ++i) {
         const int ka = (i * 32) / C::W_QK, off = (i * 32) % C::W_QK;
-        const uint64_t ad = dQs + (uint32_t)((ka * 128 * C::W_QK + off) >> 4);
-        const uint64_t bd = dKs + (uint32_t)((ka * 128 * C::W_QK + off) >> 4);
+        const uint64_t ad = smem_desc(sQa + qb * C::TILE_QK + ka * 128 * C::W_QK + off, 16, 8 * C::W_QK, SWQ);
+        const uint64_t bd = smem_desc(sKa + st * C::TILE_QK + ka * 128 * C::W_QK + off, 16, 8 * C::W_QK, SWQ);
         const uint32_t acc = i > 0 ? 1u : 0u;
         const uint32_t e = elect_u32();
         if constexpr (KIND_QK == 0) {

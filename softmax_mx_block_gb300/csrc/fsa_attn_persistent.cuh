@@ -187,7 +187,10 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
         mbar_arrive_elect(s_free + s);
 #pragma unroll
         for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(raw[i]);
-        if (128 * j + 127 > lim) {                  // only diagonal / tail tiles mask keys
+        // only diagonal / tail tiles mask keys; the branch is taken by the whole warp
+        // (rows that need no mask compare and keep every key), which keeps the masking
+        // off the path of the other tiles
+        if (__any_sync(0xffffffffu, 128 * j + 127 > lim)) {
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (128 * j + i > lim) sv[i] = kNegInf;

@@ -556,52 +556,30 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_commit_p(elect_u32(), s_full + s);
         tc_commit_p(elect_u32(), k_empty + st);
       };
-      // Non-blocking scheduler: each round lane 0 tests the barriers of the next
-      // QK^T (K(jS) landed, S buffer loaded by its owners) and of the next PV (P~(jP)
-      // written, V(jP) landed) together, and whichever GEMM is ready is issued.  QK^T
-      // runs ahead of PV so that a softmax warp finds S(j) waiting when it is done
-      // with tile j-2; the round trips of the tests overlap.
-      int jS = 0, jP = 0;
-      uint32_t idle = 0;
-      uint64_t t0 = 0;
-      while (ok && jP < nT) {
-        // every lane tests (all four tests in flight together), the votes agree
-        const bool tk = jS < nT && mbar_test(k_full + jS % C::NS, (jS / C::NS) & 1);
-        const bool tf = jS < 2 || mbar_test(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
-        const bool tp = jP < jS && mbar_test(p_full + (jP & 1), (jP >> 1) & 1);
-        const bool tv = mbar_test(v_full + jP % C::NS, (jP / C::NS) & 1);
-        const bool rs = __all_sync(0xffffffffu, tk && tf), rp = __all_sync(0xffffffffu, tp && tv);
-        if (rs) issue_s(jS++);
-        if (rp) issue_pv(jP++);
-        if (rs || rp) {
-          idle = 0;
-          continue;
+      // Fixed order: QK^T(0), QK^T(1), then for each key tile j QK^T(j+2) -- once the
+      // owners of tile j have loaded S(j), which frees its S buffer, and K(j+2) has
+      // landed -- and PV(j), once P~(j) is written and V(j) has landed.  The owners
+      // release S(j) early in tile j and write P~(j) at its end, so each wait is on
+      // the event that comes next, and the warp sleeps in it until the phase
+      // completes: PV(j) is issued as soon as its operands are there.
+      auto qk_ready = [&](int jj) -> bool {
+        return wait_all(k_full + jj % C::NS, (jj / C::NS) & 1) &&
+               (jj < 2 || wait_all(s_free + (jj & 1), ((jj - 2) >> 1) & 1));
+      };
+      for (int jj = 0; ok && jj < 2 && jj < nT; ++jj) {
+        ok = qk_ready(jj);
+        if (ok) issue_s(jj);
+      }
+      for (int j = 0; ok && j < nT; ++j) {
+        if (j + 2 < nT) {
+          ok = qk_ready(j + 2);
+          if (!ok) break;
+          issue_s(j + 2);
         }
-        // nothing ready: park in a suspending try_wait on what most likely completes
-        // next, so the warp takes no issue slots from the softmax warps of its
-        // scheduler.  The owners of tile j release S(j) when they load it, early in
-        // the tile, and write P~(j) at its end; the other part's tiles are half a tile
-        // behind.  So the release of S(jS-2) comes before P~(jP) unless PV lags QK^T
-        // by four tiles or more.
-        if (jS < nT && jS - jP <= 3) {
-          if (!tk) mbar_try_wait(k_full + jS % C::NS, (jS / C::NS) & 1);
-          else if (jS >= 2) mbar_try_wait(s_free + (jS & 1), ((jS - 2) >> 1) & 1);
-        } else if (jP < jS) {
-          if (!tp) mbar_try_wait(p_full + (jP & 1), (jP >> 1) & 1);
-          else mbar_try_wait(v_full + jP % C::NS, (jP / C::NS) & 1);
-        }
-        __syncwarp();
-        // bounded wait, abort check
-        if (++idle == 1) t0 = globaltimer_ns();
-        if ((idle & 7u) == 0) {
-          bool stop = lds_vol(ac.flag) != 0;
-          if (!stop && globaltimer_ns() - t0 > ac.limit_ns) {
-            sts_vol(ac.flag, 1);
-            if (ac.status) atomicExch(ac.status, -4);   // FSA_ERR_TIMEOUT
-            stop = true;
-          }
-          if (__any_sync(0xffffffffu, stop)) ok = false;
-        }
+        // V(j) landed long before P~(j) is written: test it first, so that the warp
+        // wakes from the P~ wait straight into the issue
+        ok = wait_all(v_full + j % C::NS, (j / C::NS) & 1) && wait_all(p_full + (j & 1), (j >> 1) & 1);
+        if (ok) issue_pv(j);
       }
       // all MMAs and copies issued by this warp complete before tensor memory is freed
       tc_commit_p(elect_u32(), drain);

@@ -196,8 +196,10 @@ struct QkvArgs {
   int64_t nq, nk;
 };
 
+// Four CTAs per SM (registers capped at 64; a few bytes spill): more tiles' loads in
+// flight measured 13% faster at 128K keys than three CTAs per SM.
 template <int FQK, int FV, int D>
-__global__ void __launch_bounds__(256) mx_quant_qkv_kernel(const QkvArgs a) {
+__global__ void __launch_bounds__(256, 4) mx_quant_qkv_kernel(const QkvArgs a) {
   __shared__ __align__(16) uint32_t tile[128 * D / 2];
   __shared__ __align__(16) uint8_t atom[512];
   const int64_t b = blockIdx.x;                    // block-uniform branch

@@ -29,7 +29,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E8M0": 3, "E2M1_EFQ": 3, "E3M2": 4}
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E8M0": 3, "E2M1_EFQ": 3, "E3M2": 4, "NVFP4": 5}
 EMAX = {0: 8, 1: 2, 2: 2, 4: 4}
 
 
@@ -124,7 +124,10 @@ def mx_quantize_rows(x_bf16: np.ndarray, fmt: int, nthreads: int | None = None):
     """Blocks of 32 along the last axis.  x_bf16: uint16 [..., L].
 
     Returns (codes uint8 [..., Lp], scales uint8 [..., Lp/32]) with Lp = L rounded
-    up to a multiple of 32 (padding codes 0)."""
+    up to a multiple of 32 (padding codes 0).  fmt 5 (NVFP4): blocks of 16 with
+    E4M3 scales, see nvfp4_quantize_rows."""
+    if fmt == 5:
+        return nvfp4_quantize_rows(x_bf16, nthreads)
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     L = x.shape[-1]
     Lp = (L + 31) // 32 * 32
@@ -134,6 +137,22 @@ def mx_quantize_rows(x_bf16: np.ndarray, fmt: int, nthreads: int | None = None):
     lib().orc_mx_quantize(_p(x), ctypes.c_int64(nrows), ctypes.c_int64(L), ctypes.c_int64(L), ctypes.c_int64(1),
                           ctypes.c_int(fmt), _p(codes), ctypes.c_int64(Lp), _p(scales), ctypes.c_int64(Lp // 32),
                           ctypes.c_int(nthreads or nthreads_default()))
+    return codes, scales
+
+
+def nvfp4_quantize_rows(x_bf16: np.ndarray, nthreads: int | None = None):
+    """NVFP4 (orc_nvfp4_quantize): blocks of 16 along the last axis, E2M1 codes and
+    one E4M3 scale byte per block.  Returns (codes uint8 [..., Lp], scales uint8
+    [..., Lp/16]), Lp = L rounded up to a multiple of 16."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    L = x.shape[-1]
+    Lp = (L + 15) // 16 * 16
+    nrows = int(np.prod(x.shape[:-1]))
+    codes = np.zeros(x.shape[:-1] + (Lp,), np.uint8)
+    scales = np.zeros(x.shape[:-1] + (Lp // 16,), np.uint8)
+    lib().orc_nvfp4_quantize(_p(x), ctypes.c_int64(nrows), ctypes.c_int64(L), ctypes.c_int64(L), ctypes.c_int64(1),
+                             _p(codes), ctypes.c_int64(Lp), _p(scales), ctypes.c_int64(Lp // 16),
+                             ctypes.c_int(nthreads or nthreads_default()))
     return codes, scales
 
 

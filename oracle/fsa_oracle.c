@@ -42,6 +42,8 @@
 /*      3 = E8M0 scale (2^(code-127); 0xFF = NaN)                              */
 /*      4 = E3M2 (bias 3, 2 mantissa bits, max 28,  6-bit code, no NaN/inf):   */
 /*          the other MXFP6 element type of [OCP-MX]                            */
+/*      5 = NVFP4 as an operand format: E2M1 element codes (as fmt 2) in blocks */
+/*          of 16 with one E4M3 scale each (O2b below); not an element codec    */
 /* ------------------------------------------------------------------------- */
 typedef struct { int ebits, mbits, bias; double maxv; int sign_shift; } fmt_info;
 
@@ -168,6 +170,47 @@ void orc_mx_quantize(const uint16_t* x, int64_t nrows, int64_t len, int64_t row_
 }
 
 /* ------------------------------------------------------------------------- */
+/* O2b: NVFP4 quantisation (an operand format adjacent to the pages' MX ones:  */
+/* NVIDIA's FP4 with E2M1 elements, one E4M3 scale per 16 consecutive         */
+/* elements; the per-tensor second-level fp32 scale is not used, i.e. 1).      */
+/* Per block: scale s = encode_E4M3(amax / 6) (nearest, ties to even,          */
+/* saturating at 448; amax / 6 is taken in fp64); codes = encode_E2M1(x / s)   */
+/* (nearest, ties to even, saturating at 6).  A scale that rounds to zero      */
+/* gives zero codes; a block with a non-finite element gets the E4M3 NaN       */
+/* scale byte 0x7F and zero codes.  Layout as orc_mx_quantize with 16-element  */
+/* blocks: scales[r*scales_stride + b] for elements [16b, 16b + 16).           */
+/* ------------------------------------------------------------------------- */
+void orc_nvfp4_quantize(const uint16_t* x, int64_t nrows, int64_t len, int64_t row_stride,
+                        int64_t elem_stride, uint8_t* codes, int64_t codes_stride,
+                        uint8_t* scales, int64_t scales_stride, int nthreads) {
+  const int64_t nblk = (len + 15) / 16;
+#pragma omp parallel for schedule(static) num_threads(nthreads > 0 ? nthreads : 1)
+  for (int64_t r = 0; r < nrows; ++r) {
+    for (int64_t b = 0; b < nblk; ++b) {
+      double xv[16];
+      double amax = 0.0;
+      int nonfinite = 0;
+      for (int i = 0; i < 16; ++i) {
+        int64_t idx = b * 16 + i;
+        xv[i] = idx < len ? bf16_to_double(x[r * row_stride + idx * elem_stride]) : 0.0;
+        if (!isfinite(xv[i])) nonfinite = 1;
+        else if (fabs(xv[i]) > amax) amax = fabs(xv[i]);
+      }
+      uint8_t* c = codes + r * codes_stride + b * 16;
+      if (nonfinite) {
+        scales[r * scales_stride + b] = 0x7F;
+        for (int i = 0; i < 16; ++i) c[i] = 0;
+        continue;
+      }
+      const uint32_t sc = orc_encode(0, amax / 6.0);
+      scales[r * scales_stride + b] = (uint8_t)sc;
+      const double sv = orc_decode(0, sc);
+      for (int i = 0; i < 16; ++i) c[i] = (uint8_t)(sv == 0.0 ? 0u : orc_encode(2, xv[i] / sv));
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Problem geometry shared by the attention oracles.                            */
 /* Query row id = (b*H + h)*Sq + i.  kv head = h / (H/Hkv) (grouped queries).  */
 /* Key j is visible to query i iff j < Sk and (!causal || j <= i + Sk - Sq).   */
@@ -272,16 +315,22 @@ typedef struct {
 static double deq(int fmt, uint8_t code, uint8_t scale) {
   return orc_decode(fmt, code) * orc_decode(3, scale);
 }
+/* element d of a row of the Q/K operand format: MX (32-element E8M0 blocks) or
+ * NVFP4 (16-element E4M3 blocks) */
+static double deq_qk(int fmt, const uint8_t* codes, const uint8_t* scales, int D, int d) {
+  if (fmt == 5) return orc_decode(2, codes[d]) * orc_decode(0, scales[d / 16]);
+  return deq(fmt, codes[d], scales[d / 32]);
+}
 
 static void q_hat(const orc_mx_operands* op, const orc_geom* g, int b, int h, int i, double* qh) {
-  const int D = g->D, nb = D / 32;
+  const int D = g->D, nb = op->fmt_qk == 5 ? D / 16 : D / 32;
   const int64_t qrow = ((int64_t)b * g->H + h) * g->Sq + i;
-  for (int d = 0; d < D; ++d) qh[d] = deq(op->fmt_qk, op->qc[qrow * D + d], op->qs[qrow * nb + d / 32]);
+  for (int d = 0; d < D; ++d) qh[d] = deq_qk(op->fmt_qk, op->qc + qrow * D, op->qs + qrow * nb, D, d);
 }
 
 static void kv_from_mx(const orc_mx_operands* op, const orc_geom* g, int b, int kvh, int nk, orc_kv* kv,
                        int nthreads) {
-  const int D = g->D, nb = D / 32;
+  const int D = g->D, nb = op->fmt_qk == 5 ? D / 16 : D / 32;
   const int64_t Skp = ((int64_t)g->Sk + 31) / 32 * 32;
   const int64_t kvi = (int64_t)b * g->Hkv + kvh;
   kv->nk = nk;
@@ -291,7 +340,7 @@ static void kv_from_mx(const orc_mx_operands* op, const orc_geom* g, int b, int 
   for (int j = 0; j < nk; ++j) {
     const int64_t krow = kvi * g->Sk + j;
     for (int d = 0; d < D; ++d) {
-      kv->kh[(int64_t)j * D + d] = deq(op->fmt_qk, op->kc[krow * D + d], op->ks[krow * nb + d / 32]);
+      kv->kh[(int64_t)j * D + d] = deq_qk(op->fmt_qk, op->kc + krow * D, op->ks + krow * nb, D, d);
       const int64_t vrow = kvi * D + d;
       kv->vh[(int64_t)d * nk + j] = deq(op->fmt_v, op->vc[vrow * Skp + j], op->vs[vrow * (Skp / 32) + j / 32]);
     }

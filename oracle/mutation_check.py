@@ -55,20 +55,27 @@ M = [
  ("efq slope from c only", "  const float a_c = opt->efq_a * c;               /* EFQ: fp32(a c) */", "  const float a_c = c;"),
  ("efq clamp 6", "                if (kk > 7.0) kk = 7.0;\n                code", "                if (kk > 6.0) kk = 6.0;\n                code"),
  ("efq floor", "double kk = nearbyint((double)y);                 /* ties to even */", "double kk = floor((double)y);"),
- ("emu pt scale", "              pt[j - j0] = orc_decode(efmt, code) * sc;", "              pt[j - j0] = orc_decode(efmt, code) * sc * 2.0;"),
+ ("emu pt scale", "              pt[j - j0] = orc_decode(efmt, used) * sc;", "              pt[j - j0] = orc_decode(efmt, used) * sc * 2.0;"),
  ("emu mask inverted", "int hw = (opt->mufu_mask >> (j % 32)) & 1;", "int hw = !((opt->mufu_mask >> (j % 32)) & 1);"),
  ("emu tiles of 64", "  const int D = g->D, BN = 128;\n  const int64_t Skp", "  const int D = g->D, BN = 64;\n  const int64_t Skp"),
  ("bf16 tau 0", "else if (x - M > tau) {", "else if (x - M > 0.0f) {"),
  ("bf16 round ties away", "u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;", "u = (u + 0x8000u) & 0xFFFF0000u;"),
  ("v transposed stride", "op->vc[vrow * Skp + j]", "op->vc[vrow * g->Sk + j]"),
- ("q scale index", "op->qs[qrow * nb + d / 32]", "op->qs[qrow * nb + d / 64]"),
+ ("mx qk scale index", "return deq(fmt, codes[d], scales[d / 32]);", "return deq(fmt, codes[d], scales[d / 64]);"),
  ("emu ignores causal", "      int nk = last_visible(g, i) + 1;\n      double* o = out + n * D;\n      for (int d = 0; d < D; ++d) o[d] = 0.0;\n      int fb = 0", "      int nk = g->Sk;\n      double* o = out + n * D;\n      for (int d = 0; d < D; ++d) o[d] = 0.0;\n      int fb = 0"),
  ("emu normalise +1", "        for (int d = 0; d < D; ++d) o[d] = l > 0.0 ? o[d] / l : 0.0;\n        if (A) {", "        for (int d = 0; d < D; ++d) o[d] = l > 0.0 ? o[d] / (l + 1.0) : 0.0;\n        if (A) {"),
  ("emu tmax from M", "            float tmax = smax * c - M;", "            float tmax = 0.0f;"),
  ("emu block max wrong", "            for (int j = jb; j < je; ++j) if (s[j - j0] > smax) smax = s[j - j0];\n            float tmax", "            smax = s[jb - j0];\n            float tmax"),
- ("k scale index", "op->ks[krow * nb + d / 32]", "op->ks[krow * nb]"),
+ ("k scale row", "op->kc + krow * D, op->ks + krow * nb, D, d)", "op->kc + krow * D, op->ks, D, d)"),
+ ("nvfp4 scale index", "orc_decode(0, scales[d / 16])", "orc_decode(0, scales[d / 32])"),
+ ("nvfp4 scale from amax/4", "orc_encode(0, amax / 6.0)", "orc_encode(0, amax / 4.0)"),
+ ("nvfp4 codes times scale", "orc_encode(2, xv[i] / sv)", "orc_encode(2, xv[i] * sv)"),
+ ("nvfp4 nan scale byte", "scales[r * scales_stride + b] = 0x7F;", "scales[r * scales_stride + b] = 0x7E;"),
+ ("nvfp4 pads with ones", "int64_t idx = b * 16 + i;\n        xv[i] = idx < len ? bf16_to_double(x[r * row_stride + idx * elem_stride]) : 0.0;",
+  "int64_t idx = b * 16 + i;\n        xv[i] = idx < len ? bf16_to_double(x[r * row_stride + idx * elem_stride]) : 1.0;"),
  ("v scale index", "op->vs[vrow * (Skp / 32) + j / 32]", "op->vs[vrow * (Skp / 32)]"),
- ("mx pads with ones", "idx * elem_stride]) : 0.0;", "idx * elem_stride]) : 1.0;"),
+ ("mx pads with ones", "int64_t idx = b * 32 + i;\n        xv[i] = idx < len ? bf16_to_double(x[r * row_stride + idx * elem_stride]) : 0.0;",
+  "int64_t idx = b * 32 + i;\n        xv[i] = idx < len ? bf16_to_double(x[r * row_stride + idx * elem_stride]) : 1.0;"),
  ("groups by batch only", "k[n].key = (int64_t)b * g->Hkv + kvh;", "k[n].key = (int64_t)b;"),
  ("exact v from k", "kv->vh[(int64_t)d * nk + j] = bf16_to_double(v[base + (int64_t)j * D + d]);",
   "kv->vh[(int64_t)d * nk + j] = bf16_to_double(k[base + (int64_t)j * D + d]);"),

@@ -303,7 +303,8 @@ def test_emulate_pgen_block_structure():
             assert 0x78 <= c <= 0x7E
 
 
-@pytest.mark.parametrize("fq,fp,bound", [(0, 0, 1.1), (1, 1, 1.1), (2, 2, 1.1), (2, 3, 1.17), (4, 4, 1.1)])
+@pytest.mark.parametrize("fq,fp,bound", [(0, 0, 1.1), (1, 1, 1.1), (2, 2, 1.1), (2, 3, 1.17), (4, 4, 1.1),
+                                           (5, 0, 1.1), (5, 3, 1.17)])
 def test_emulate_error_close_to_floor_on_tiny(fq, fp, bound):
     """The pages' claim (Fused-Softmax brief, abstract): the approximation's extra
     error stays near the floor set by quantising the GEMM operands.  The exp paths

@@ -61,7 +61,12 @@ typedef enum {
   FSA_FMT_E2M3 = 1,      /* MXFP6 */
   FSA_FMT_E2M1 = 2,      /* MXFP4, P by exp then round-to-nearest-even */
   FSA_FMT_E2M1_EFQ = 3,  /* MXFP4, P by the EFQ affine rule (fmt_pv only) */
-  FSA_FMT_E3M2 = 4       /* MXFP6, the OCP MX E3M2 element type (bias 3, max 28) */
+  FSA_FMT_E3M2 = 4,      /* MXFP6, the OCP MX E3M2 element type (bias 3, max 28) */
+  FSA_FMT_NVFP4 = 5      /* NVFP4: E2M1 codes with one E4M3 scale per 16 elements
+                          * (FSA_MX_ROWS only, i.e. Q and K, fmt_qk only); an
+                          * operand format adjacent to the MX ones the
+                          * Fused-Softmax brief names (abstract), from NVIDIA's
+                          * public FP4 definition without its per-tensor scale */
 } fsa_fmt;
 
 /* ------------------------------------------------------------ MX tensors */
@@ -85,13 +90,20 @@ typedef enum {
  *           0x7F; blocks of keys wholly >= S hold 0x7F.
  * The block scale is E = clamp(floor(log2 amax) - emax, -127, 127) (emax 8
  * for E4M3, 4 for E3M2, 2 for E2M3/E2M1), codes = round-to-nearest-even, saturating, of
- * x * 2^-E; a block with a non-finite element gets scale 0xFF.           */
+ * x * 2^-E; a block with a non-finite element gets scale 0xFF.
+ * FSA_FMT_NVFP4 (FSA_MX_ROWS only): codes as E2M1 above; one E4M3 scale byte
+ *   per 16 elements along D: the E4M3 value nearest amax/6 (ties to even,
+ *   saturating at 448), codes the E2M1 values nearest x/scale (saturating at 6;
+ *   a zero scale gives zero codes; a non-finite block gets scale 0x7F, the
+ *   E4M3 NaN, and zero codes).  scales: [B*H][ceil(S/128)][D/64][512] bytes:
+ *   for row r of a 128-row tile and 16-element block b (b < D/16), byte
+ *   (b/4)*512 + (r%32)*16 + (r/32)*4 + b%4; rows >= S hold 0x38 (1.0).   */
 typedef enum { FSA_MX_ROWS = 0, FSA_MX_COLS_T = 1 } fsa_mx_layout;
 
 typedef struct {
   void*    codes;    /* device, 16-byte aligned */
   uint8_t* scales;   /* device, 16-byte aligned */
-  int32_t  fmt;      /* fsa_fmt of the codes (E4M3, E2M3, E2M1 or E3M2) */
+  int32_t  fmt;      /* fsa_fmt of the codes (E4M3, E2M3, E2M1, E3M2 or NVFP4) */
   int32_t  layout;   /* fsa_mx_layout */
   int32_t  B, H, S, D;
 } fsa_mx_tensor;

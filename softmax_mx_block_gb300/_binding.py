@@ -14,10 +14,10 @@ from . import _build
 
 FSA_OK, FSA_ERR_INVALID_ARG, FSA_ERR_UNSUPPORTED_FMT, FSA_ERR_LAUNCH, FSA_ERR_TIMEOUT, FSA_ERR_NO_DEVICE = \
     0, -1, -2, -3, -4, -5
-FSA_FMT_E4M3, FSA_FMT_E2M3, FSA_FMT_E2M1, FSA_FMT_E2M1_EFQ, FSA_FMT_E3M2 = 0, 1, 2, 3, 4
+FSA_FMT_E4M3, FSA_FMT_E2M3, FSA_FMT_E2M1, FSA_FMT_E2M1_EFQ, FSA_FMT_E3M2, FSA_FMT_NVFP4 = 0, 1, 2, 3, 4, 5
 FSA_MX_ROWS, FSA_MX_COLS_T = 0, 1
 FSA_EXP_POLY, FSA_EXP_MUFU, FSA_EXP_SPLIT = 0, 1, 2
-FMT_BY_NAME = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4}
+FMT_BY_NAME = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4, "NVFP4": 5}
 
 
 class FsaError(RuntimeError):

@@ -19,8 +19,8 @@ LIB = os.path.join(PKG, "libfsa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
-# (QK format, PV format): 0 E4M3, 1 E2M3, 2 E2M1, 3 E2M1 by the EFQ rule, 4 E3M2, 5 BF16
-ATTN_PAIRS = [(qk, pv) for qk in (0, 1, 2, 4) for pv in range(5)] + [(5, 5)]
+# (QK format, PV format): 0 E4M3, 1 E2M3, 2 E2M1, 3 E2M1 by the EFQ rule, 4 E3M2, 5 BF16, 6 NVFP4 (Q/K)
+ATTN_PAIRS = [(qk, pv) for qk in (0, 1, 2, 4, 6) for pv in range(5)] + [(5, 5)]
 
 
 def _nvcc() -> str:

@@ -137,12 +137,14 @@ bool make_tmap_out(CUtensorMap* m, void* base, uint64_t D, uint64_t rows, uint64
 }
 
 // storage bits per element * 2, as the kernels store them
-int bits2_of(int fmt) { return fmt == FSA_FMT_E2M1 || fmt == FSA_FMT_E2M1_EFQ ? 8 : 16; }
+int bits2_of(int fmt) { return fmt == FSA_FMT_E2M1 || fmt == FSA_FMT_E2M1_EFQ || fmt == FSA_FMT_NVFP4 ? 8 : 16; }
 
 int row_bytes(int D, int fmt) { return D * bits2_of(fmt) / 16; }
 
-// storage formats of MX tensors (E2M1_EFQ is a P format only)
-bool valid_fmt(int f) { return (f >= FSA_FMT_E4M3 && f <= FSA_FMT_E2M1) || f == FSA_FMT_E3M2; }
+// storage formats of MX tensors (E2M1_EFQ is a P format only; NVFP4 a Q/K format only)
+bool valid_fmt(int f) {
+  return (f >= FSA_FMT_E4M3 && f <= FSA_FMT_E2M1) || f == FSA_FMT_E3M2 || f == FSA_FMT_NVFP4;
+}
 bool valid_pv(int f) { return f >= FSA_FMT_E4M3 && f <= FSA_FMT_E3M2; }
 
 int storage_fmt(int f) { return f == FSA_FMT_E2M1_EFQ ? FSA_FMT_E2M1 : f; }
@@ -160,7 +162,7 @@ using ImplFn = cudaError_t (*)(const AttnLaunch&);
 // fsa.h format numbers are the kernels' template arguments (fsa_attn.cuh)
 ImplFn impl_for(int fqk, int fpv) {
   using namespace fsa;
-  static const ImplFn table[5][5] = {
+  static const ImplFn table[6][5] = {
       {launch_attn_impl<0, 0>, launch_attn_impl<0, 1>, launch_attn_impl<0, 2>, launch_attn_impl<0, 3>,
        launch_attn_impl<0, 4>},
       {launch_attn_impl<1, 0>, launch_attn_impl<1, 1>, launch_attn_impl<1, 2>, launch_attn_impl<1, 3>,
@@ -169,7 +171,9 @@ ImplFn impl_for(int fqk, int fpv) {
        launch_attn_impl<2, 4>},
       {nullptr, nullptr, nullptr, nullptr, nullptr},
       {launch_attn_impl<4, 0>, launch_attn_impl<4, 1>, launch_attn_impl<4, 2>, launch_attn_impl<4, 3>,
-       launch_attn_impl<4, 4>}};
+       launch_attn_impl<4, 4>},
+      {launch_attn_impl<6, 0>, launch_attn_impl<6, 1>, launch_attn_impl<6, 2>, launch_attn_impl<6, 3>,
+       launch_attn_impl<6, 4>}};   // NVFP4 (fsa.h 5) is the kernels' format 6
   return table[fqk][fpv];
 }
 
@@ -250,13 +254,14 @@ const char* fsa_status_string(int s) {
 
 int fsa_mx_sizes(int B, int H, int S, int D, int layout, int fmt, size_t* codes_bytes, size_t* scales_bytes) {
   if (B <= 0 || H <= 0 || S <= 0 || (D != 64 && D != 128) || !valid_fmt(storage_fmt(fmt)) ||
-      (layout != FSA_MX_ROWS && layout != FSA_MX_COLS_T) || !codes_bytes || !scales_bytes)
+      (layout != FSA_MX_ROWS && layout != FSA_MX_COLS_T) || !codes_bytes || !scales_bytes ||
+      (fmt == FSA_FMT_NVFP4 && layout != FSA_MX_ROWS))
     return FSA_ERR_INVALID_ARG;
   const size_t bh = (size_t)B * H;
   const int sf = storage_fmt(fmt);
   if (layout == FSA_MX_ROWS) {
     *codes_bytes = bh * (size_t)S * row_bytes(D, sf);
-    *scales_bytes = bh * (size_t)((S + 127) / 128) * 512;
+    *scales_bytes = bh * (size_t)((S + 127) / 128) * 512 * (sf == FSA_FMT_NVFP4 ? D / 64 : 1);
   } else {
     const size_t Sp = (size_t)(S + 127) / 128 * 128;
     *codes_bytes = bh * (size_t)D * Sp * bits2_of(sf) / 16;
@@ -351,10 +356,13 @@ int attention_impl(const fsa_mx_tensor* q, const void* q_bf16, const fsa_mx_tens
   if (dbg && (!dbg->s || !dbg->m || !dbg->p || !dbg->p_scales)) return FSA_ERR_INVALID_ARG;
   if (dbg && fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode == FSA_EXP_SPLIT) return FSA_ERR_UNSUPPORTED_FMT;
   // Q quantised in the prologue: one CTA per query tile, the hardware exp2 (or EFQ)
-  if (q_bf16 && (dbg || o.schedule == FSA_SCHED_PERSISTENT ||
+  if (q_bf16 && (dbg || o.schedule == FSA_SCHED_PERSISTENT || fmt_qk == FSA_FMT_NVFP4 ||
                  (fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode != FSA_EXP_MUFU)))
     return FSA_ERR_UNSUPPORTED_FMT;
-  const bool persistent = !dbg && !q_bf16 && persistent_schedule(o.schedule, Sq, Sk, causal);
+  // NVFP4 Q/K run one CTA per query tile
+  if (fmt_qk == FSA_FMT_NVFP4 && o.schedule == FSA_SCHED_PERSISTENT) return FSA_ERR_UNSUPPORTED_FMT;
+  const bool persistent =
+      !dbg && !q_bf16 && fmt_qk != FSA_FMT_NVFP4 && persistent_schedule(o.schedule, Sq, Sk, causal);
   const bool bf16 = o.out_dtype == FSA_OUT_BF16;
 
   AttnLaunch a;

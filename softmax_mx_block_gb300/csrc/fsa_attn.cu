@@ -371,18 +371,19 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_expect_tx(qraw_full, 128 * D * 2);
         tma_load_3d(sm + C::OFF_QRAW, &tm_q, qraw_full, 0, q0, bhq);
       } else {
-        mbar_expect_tx(q_full, C::TILE_QK + (MX ? 512 : 0));
+        mbar_expect_tx(q_full, C::TILE_QK + (MX ? C::SFQK : 0));
 #pragma unroll
         for (int ka = 0; ka < C::NKA_QK; ++ka)
           tma_load_3d(sQ + ka * 128 * C::W_QK, &tm_q, q_full, ka * C::W_QK, q0, bhq);
-        if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * 512, 512, q_full);
+        if (MX) bulk_load(sm + C::OFF_SFQ, p.sf_q + ((size_t)bhq * p.n_qtiles + qt) * C::SFQK, C::SFQK, q_full);
       }
       for (int j = 0; j < C::NS && j < nT; ++j) {
-        mbar_expect_tx(k_full + j, C::TILE_QK + (MX ? 512 : 0));
+        mbar_expect_tx(k_full + j, C::TILE_QK + (MX ? C::SFQK : 0));
 #pragma unroll
         for (int ka = 0; ka < C::NKA_QK; ++ka)
           tma_load_3d(sK + j * C::TILE_QK + ka * 128 * C::W_QK, &tm_k, k_full + j, ka * C::W_QK, j * 128, bhk);
-        if (MX) bulk_load(sm + C::OFF_SFK + j * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + j);
+        if (MX)
+          bulk_load(sm + C::OFF_SFK + j * C::SFQK, p.sf_k + ((size_t)bhk * nkt + j) * C::SFQK, C::SFQK, k_full + j);
         mbar_expect_tx(v_full + j, C::TILE_V_TMA + (MX ? 512 : 0));
 #pragma unroll
         for (int ka = 0; ka < C::NKA_V; ++ka)
@@ -446,11 +447,13 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int j = nk; j < nT; ++j) {
           const int st = j % C::NS;
           if (j >= C::NS && !mbar_wait(k_empty + st, ((j - C::NS) / C::NS) & 1, ac)) break;
-          mbar_expect_tx(k_full + st, C::TILE_QK + (MX ? 512 : 0));
+          mbar_expect_tx(k_full + st, C::TILE_QK + (MX ? C::SFQK : 0));
 #pragma unroll
           for (int ka = 0; ka < C::NKA_QK; ++ka)
             tma_load_3d(sK + st * C::TILE_QK + ka * 128 * C::W_QK, &tm_k, k_full + st, ka * C::W_QK, j * 128, bhk);
-          if (MX) bulk_load(sm + C::OFF_SFK + st * 512, p.sf_k + ((size_t)bhk * nkt + j) * 512, 512, k_full + st);
+          if (MX)
+            bulk_load(sm + C::OFF_SFK + st * C::SFQK, p.sf_k + ((size_t)bhk * nkt + j) * C::SFQK, C::SFQK,
+                      k_full + st);
           ++nk;
         }
         mbar_drain(QF ? qraw_full : q_full, 0, ac);
@@ -492,7 +495,10 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (ok) {
         tc_fence_after();
         if constexpr (MX) {
-          tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFQ, smem_desc(smem_u32(sm + C::OFF_SFQ), 16, 128, 0));
+#pragma unroll
+          for (int a = 0; a < C::NATOM_QK; ++a)      // NVFP4: one atom per K = 64 step
+            tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFQ + 4 * a,
+                            smem_desc(smem_u32(sm + C::OFF_SFQ + 512 * a), 16, 128, 0));
           if constexpr (D == 128) {
             const uint64_t one = smem_desc(smem_u32(sm + C::OFF_SFONE), 16, 128, 0);
             tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFV + 4, one);
@@ -533,8 +539,11 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int s = j & 1, st = j % C::NS;
         tc_fence_after();
         if constexpr (MX) {
-          const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFK + st * 512), 16, 128, 0);
-          tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFK + 4 * s, sfd);
+#pragma unroll
+          for (int a = 0; a < C::NATOM_QK; ++a) {
+            const uint64_t sfd = smem_desc(smem_u32(sm + C::OFF_SFK + st * C::SFQK + 512 * a), 16, 128, 0);
+            tc_cp_sf_atom_p(elect_u32(), tbase + C::T_SFK + C::SFK_STEP * s + 4 * a, sfd);
+          }
         }
 #pragma unroll
         for (int i = 0; i < C::QK_STEPS; ++i) {
@@ -547,10 +556,14 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mma_f16_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_f16_bf16(128), acc);
           } else if constexpr (KIND_QK == 1) {
             mma_mxf8f6f4_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, Fmt<FQK>::code, i, i),
-                              tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
-          } else {
+                              tbase + C::T_SFQ, tbase + C::T_SFK + C::SFK_STEP * s, acc);
+          } else if constexpr (KIND_QK == 2) {
             mma_mxf4_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_bs(128, 1, 2 * i, 2 * i),
-                          tbase + C::T_SFQ, tbase + C::T_SFK + 4 * s, acc);
+                          tbase + C::T_SFQ, tbase + C::T_SFK + C::SFK_STEP * s, acc);
+          } else {
+            // NVFP4: step i reads the whole scale word of atom i (16 elements a byte)
+            mma_nvf4_4x_ss_p(e, tbase + C::T_S + 128 * s, ad, bd, idesc_nvfp4(128), tbase + C::T_SFQ + 4 * i,
+                             tbase + C::T_SFK + C::SFK_STEP * s + 4 * i, acc);
           }
         }
         tc_commit_p(elect_u32(), s_full + s);
@@ -976,10 +989,13 @@ static cudaError_t launch_sched(const AttnLaunch& a) {
   // Q quantised in the prologue: the library's default exp2 path (and EFQ), one CTA
   // per query tile
   if (a.q_fused) {
-    if constexpr ((EXPM == 1 || FPV == F_EFQ) && FQK != F_BF16) return launch_one<FQK, FPV, D, EXPM, false, true>(a);
+    if constexpr ((EXPM == 1 || FPV == F_EFQ) && FQK != F_BF16 && FQK != F_NVFP4)
+      return launch_one<FQK, FPV, D, EXPM, false, true>(a);
     return cudaErrorNotSupported;
   }
-  return a.persistent ? launch_persistent<FQK, FPV, D, EXPM>(a) : launch_one<FQK, FPV, D, EXPM>(a);
+  // NVFP4 Q/K: one CTA per query tile only
+  if constexpr (FQK == F_NVFP4) return a.persistent ? cudaErrorNotSupported : launch_one<FQK, FPV, D, EXPM>(a);
+  else return a.persistent ? launch_persistent<FQK, FPV, D, EXPM>(a) : launch_one<FQK, FPV, D, EXPM>(a);
 }
 
 // The exp-mode slot: 0/1/2 the exp2 path of the exp-then-round formats; for EFQ 1

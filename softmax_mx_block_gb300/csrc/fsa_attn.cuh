@@ -6,12 +6,14 @@
 
 namespace fsa {
 
-// Operand formats (0..4 as fsa.h numbers them).  F_EFQ stores E2M1 like F_E2M1;
-// it only changes how the softmax warps produce P.
-enum : int { F_E4M3 = 0, F_E2M3 = 1, F_E2M1 = 2, F_EFQ = 3, F_E3M2 = 4, F_BF16 = 5 };
+// Operand formats (0..4 as fsa.h numbers them; F_NVFP4 is fsa.h's 5).  F_EFQ stores
+// E2M1 like F_E2M1; it only changes how the softmax warps produce P.  F_NVFP4 is a
+// QK^T operand format only: E2M1 codes, one E4M3 scale per 16 elements.
+enum : int { F_E4M3 = 0, F_E2M3 = 1, F_E2M1 = 2, F_EFQ = 3, F_E3M2 = 4, F_BF16 = 5, F_NVFP4 = 6 };
 
 template <int F> struct Fmt;
-// kind: 0 = kind::f16, 1 = kind::mxf8f6f4 (scale_vec 1X, K = 32), 2 = kind::mxf4 (2X, K = 64)
+// kind: 0 = kind::f16, 1 = kind::mxf8f6f4 (scale_vec 1X, K = 32), 2 = kind::mxf4 (2X, K = 64),
+// 3 = kind::mxf4nvf4 (4X, K = 64, UE4M3 scales)
 // code: the element type field of the block-scaled instruction descriptor
 // bits2: storage bits per element * 2 (E2M1 packs two per byte)
 template <> struct Fmt<F_BF16> { static constexpr int kind = 0, bits2 = 32, code = 0, emax = 0; };
@@ -20,6 +22,7 @@ template <> struct Fmt<F_E2M3> { static constexpr int kind = 1, bits2 = 16, code
 template <> struct Fmt<F_E3M2> { static constexpr int kind = 1, bits2 = 16, code = 4, emax = 4; };  // 16 codes / 16 bytes
 template <> struct Fmt<F_E2M1> { static constexpr int kind = 2, bits2 = 8, code = 1, emax = 2; };
 template <> struct Fmt<F_EFQ>  { static constexpr int kind = 2, bits2 = 8, code = 1, emax = 2; };
+template <> struct Fmt<F_NVFP4> { static constexpr int kind = 3, bits2 = 8, code = 1, emax = 0; };
 
 __host__ __device__ constexpr int swz_code(int width) { return width == 128 ? 2 : (width == 64 ? 4 : 6); }
 
@@ -34,6 +37,12 @@ struct Cfg {
   static constexpr bool MX = FQK != F_BF16;
   static_assert((FQK == F_BF16) == (FPV == F_BF16), "BF16 kernel uses BF16 for both GEMMs");
   static_assert(FQK != F_EFQ, "EFQ is a P format");
+  static_assert(FPV != F_NVFP4, "NVFP4 is a QK^T operand format");
+  // NVFP4 Q/K: one 512-byte scale atom per K = 64 step (D/64 of them per tile)
+  static constexpr bool NV = FQK == F_NVFP4;
+  static_assert(!(NV && (PERSIST || QF)), "NVFP4 runs one CTA per query tile with Q quantised beforehand");
+  static constexpr int NATOM_QK = NV ? D_ / 64 : 1;
+  static constexpr int SFQK = 512 * NATOM_QK;                       // scale bytes of a Q or K tile
   // ---- QK^T operands (Q, K rows of D elements)
   static constexpr int RB_QK = D * Fmt<FQK>::bits2 / 16;            // bytes per row
   static constexpr int W_QK = RB_QK < 128 ? RB_QK : 128;            // swizzle atom width
@@ -68,8 +77,8 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NS * TILE_QK;
   static constexpr int OFF_SF = (OFF_V + NS * TILE_V + 1023) / 1024 * 1024;
   static constexpr int OFF_SFQ = OFF_SF;
-  static constexpr int OFF_SFK = OFF_SFQ + NQB * SF_BYTES;
-  static constexpr int OFF_SFV = OFF_SFK + NS * SF_BYTES;
+  static constexpr int OFF_SFK = OFF_SFQ + NQB * SFQK;
+  static constexpr int OFF_SFV = OFF_SFK + NS * SFQK;
   static constexpr int OFF_SFONE = OFF_SFV + NS * SF_BYTES;
   static constexpr int OFF_RED = OFF_SFONE + SF_BYTES;              // M handoff, fallback counts, BF16 {l, M} x 2
   static constexpr int OFF_BAR = OFF_RED + (256 + 4 * 128) * 4;
@@ -94,14 +103,18 @@ struct Cfg {
   // ---- tensor memory columns
   static constexpr uint32_t T_S = 0;          // S0 [0,128), S1 [128,256)
   static constexpr uint32_t T_O = 256;        // [256, 256 + N_PV)
+  // a scale atom occupies 4 columns (lane quadrant q reads column + q); NVFP4 Q and K
+  // have two atoms per tile at D = 128
   static constexpr uint32_t T_SFQ = 400;
-  static constexpr uint32_t T_SFK = 404;      // + 4 * parity
-  static constexpr uint32_t T_SFV = 412;      // + 8 * parity (4 from the V atom, 4 constant)
-  static constexpr uint32_t T_SFP = 428;      // + 4 * buffer + lane quadrant
+  static constexpr uint32_t SFK_STEP = 4 * NATOM_QK;                // columns per K parity
+  static constexpr uint32_t T_SFK = T_SFQ + 4 * NATOM_QK;          // + SFK_STEP * parity
+  static constexpr uint32_t T_SFV = T_SFK + 2 * SFK_STEP;          // + 8 * parity (4 from the V atom, 4 constant)
+  static constexpr uint32_t T_SFP = T_SFV + 16;                     // + 4 * buffer + lane quadrant
   static constexpr uint32_t T_SFQ1 = 436;     // persistent: scale atom of the second Q buffer
   static constexpr uint32_t T_P = MX ? 448 : T_O + D;   // + P_COLS * buffer (BF16: no scales)
   static_assert(T_O + N_PV <= (MX ? T_SFQ : T_P), "tmem");
   static_assert(!MX || T_SFQ1 + 4 <= T_P, "tmem");
+  static_assert(!MX || T_SFP + 8 <= (PERSIST ? T_SFQ1 : T_P), "tmem");
   static_assert(T_P + NPB * P_COLS <= 512, "tmem");
   // ---- threads
   static constexpr int NTHREADS = 64 + 32 * NSW;   // warp 0 TMA, warp 1 MMA, then the softmax warps

@@ -80,4 +80,31 @@ __device__ __forceinline__ uint32_t quant_block32(const float* v, uint32_t* w) {
   return sbyte;
 }
 
+// NVFP4 (fsa.h format 5): E2M1 codes with one E4M3 scale per 16 elements.  The
+// scale is the E4M3 value nearest amax / 6 and the codes the E2M1 values nearest
+// x / scale, both by a correctly rounded fp32 division and cvt.rn.satfinite: for
+// bf16 inputs the fp32 quotient rounds to the same E4M3 / E2M1 code as the exact
+// one (neither quotient is within 2^-24 of a rounding boundary unless it is one).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {     // exact: E4M3 fits f16
+  float f;
+  const uint16_t t = (uint16_t)((b & 0xFFu) | ((b & 0xFFu) << 8));
+  asm("{\n .reg .b16 lo, hi;\n .reg .b32 h2;\n cvt.rn.f16x2.e4m3x2 h2, %1;\n"
+      " mov.b32 {lo, hi}, h2;\n cvt.f32.f16 %0, lo;\n}" : "=f"(f) : "h"(t));
+  return f;
+}
+// scale byte of a block with maximum magnitude amax (0x7F, the E4M3 NaN, for a
+// non-finite block)
+__device__ __forceinline__ uint32_t nvfp4_scale_byte(float amax, bool nonfinite) {
+  return nonfinite ? 0x7Fu : (cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu);
+}
+// codes of 8 consecutive elements (one 32-bit word, even element in the low nibble)
+// under the block scale s (0 or NaN: zero codes)
+__device__ __forceinline__ uint32_t nvfp4_codes8(const float* v, float s) {
+  if (!(s > 0.0f)) return 0u;
+  uint32_t w = 0u;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) w |= cvt_e2m1x2(__fdiv_rn(v[2 * e], s), __fdiv_rn(v[2 * e + 1], s)) << (8 * e);
+  return w;
+}
+
 }  // namespace fsa

@@ -297,6 +297,16 @@ __device__ __forceinline__ void mma_mxf4_ts_p(uint32_t e, uint32_t d, uint32_t a
                ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
 }
 
+// kind::mxf4nvf4 with scale_vec::4X: E2M1 operands, one scale byte per 16 elements
+// (four per row per K = 64 step, the whole 32-bit scale word; with UE4M3 scales for
+// NVFP4, descriptor bit 23 clear).
+__device__ __forceinline__ void mma_nvf4_4x_ss_p(uint32_t e, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                 uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %6, 0;\n setp.ne.b32 q, %7, 0;\n"
+               "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc), "r"(e) : "memory");
+}
+
 // Shared-memory matrix descriptor: start address, stride between 8-row core
 // groups (sbo), leading offset (lbo, unused for K-major swizzled tiles),
 // descriptor version 1 (bit 46), swizzle code in bits 61-63
@@ -316,6 +326,9 @@ __host__ __device__ constexpr uint32_t idesc_bs(int N, uint32_t ab_fmt, uint32_t
   return (sfb_id << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
          ((uint32_t)(128 >> 4) << 24) | (sfa_id << 29);
 }
+// NVFP4 (kind::mxf4nvf4, scale_vec::4X): E2M1 a/b (1), UE4M3 scales (bit 23 clear),
+// the whole scale word of each row per instruction (selectors 0).
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int N) { return idesc_bs(N, 1, 0, 0) & ~(1u << 23); }
 
 // tcgen05.ld / st, 32 lanes x 32 bits, N consecutive columns per thread.
 template <int N> struct TmemLd;

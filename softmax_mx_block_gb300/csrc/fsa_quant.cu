@@ -99,11 +99,80 @@ __device__ __forceinline__ void quant_rows_tile(const uint16_t* __restrict__ x, 
   if (t < 32) reinterpret_cast<uint4*>(scales + tile_id * 512)[t] = reinterpret_cast<const uint4*>(atom)[t];
 }
 
+// NVFP4 rows (Q, K): as quant_rows_tile with 16-element blocks (two lanes, two
+// chunks) and D/64 scale atoms per tile: block b of row r goes to byte
+// (b/4)*512 + (r%32)*16 + (r/32)*4 + b%4 (rows past S keep 0x38, 1.0).
+template <int D>
+__device__ __forceinline__ void quant_rows_tile_nv(const uint16_t* __restrict__ x, int S, uint8_t* __restrict__ codes,
+                                                   uint8_t* __restrict__ scales, int64_t tile_id, uint8_t* atom,
+                                                   const uint4* staged = nullptr) {
+  constexpr int CPR = D / 8;                       // chunks per row
+  constexpr int NCH = 128 * CPR / 256;             // chunks per thread
+  constexpr int RB = D / 2;                        // code bytes per row
+  constexpr int NATOM = D / 64;
+  const int t = threadIdx.x;
+  const int ntiles = (S + 127) / 128;
+  const int64_t bh = tile_id / ntiles;
+  const int s0 = (int)(tile_id % ntiles) * 128;
+  const int nrows = min(128, S - s0);
+  const uint16_t* src = x + ((int64_t)bh * S + s0) * D;
+  uint8_t* dst = codes + ((int64_t)bh * S + s0) * RB;
+  if (t < 128 * NATOM) reinterpret_cast<uint32_t*>(atom)[t] = 0x38383838u;
+  uint4 raw[NCH];
+  if (staged == nullptr) {
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int ch = t + 256 * i;
+      raw[i] = ch / CPR < nrows ? *reinterpret_cast<const uint4*>(src + 8 * ch) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  __syncthreads();                                 // atoms initialised before the scale bytes land
+  if (staged != nullptr) {
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) raw[i] = staged[t + 256 * i];
+  }
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int ch = t + 256 * i, r = ch / CPR, c = ch % CPR;
+    const uint32_t wr[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float v[8];
+    float amax = 0.f;
+    bool nonfinite = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = bf16_to_f32((uint16_t)(wr[e] & 0xFFFF));
+      v[2 * e + 1] = bf16_to_f32((uint16_t)(wr[e] >> 16));
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float a = fabsf(v[e]);
+      nonfinite |= !(a <= 3.4e38f);
+      amax = fmaxf(amax, a);
+    }
+    // 2-lane group reduction (a block is chunks 2m, 2m + 1 of one row: CPR is even)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const int nf = nonfinite | __shfl_xor_sync(0xffffffffu, (int)nonfinite, 1);
+    const uint32_t sbyte = nvfp4_scale_byte(amax, nf != 0);
+    const uint32_t w = nf ? 0u : nvfp4_codes8(v, e4m3_to_f32(sbyte));
+    if (r < nrows) {
+      *reinterpret_cast<uint32_t*>(dst + r * RB + 4 * c) = w;
+      if ((c & 1) == 0) {
+        const int b = c >> 1;
+        atom[(b >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] = (uint8_t)sbyte;
+      }
+    }
+  }
+  __syncthreads();
+  if (t < 32 * NATOM)
+    reinterpret_cast<uint4*>(scales + tile_id * 512 * NATOM)[t] = reinterpret_cast<const uint4*>(atom)[t];
+}
+
 template <int FMT, int D>
 __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const uint16_t* __restrict__ x, int S,
                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-  __shared__ __align__(16) uint8_t atom[512];
-  quant_rows_tile<FMT, D>(x, S, codes, scales, blockIdx.x, atom);
+  __shared__ __align__(16) uint8_t atom[1024];
+  if constexpr (FMT == 5) quant_rows_tile_nv<D>(x, S, codes, scales, blockIdx.x, atom);
+  else quant_rows_tile<FMT, D>(x, S, codes, scales, blockIdx.x, atom);
 }
 
 // --------------------------------------------------------------------------
@@ -201,10 +270,14 @@ struct QkvArgs {
 template <int FQK, int FV, int D>
 __global__ void __launch_bounds__(256, 4) mx_quant_qkv_kernel(const QkvArgs a) {
   __shared__ __align__(16) uint32_t tile[128 * D / 2];
-  __shared__ __align__(16) uint8_t atom[512];
+  __shared__ __align__(16) uint8_t atom[FQK == 5 ? 512 * (D / 64) : 512];
   const int64_t b = blockIdx.x;                    // block-uniform branch
-  if (b < a.nq) quant_rows_tile<FQK, D>(a.x[0], a.Sq, a.codes[0], a.scales[0], b, atom);
-  else if (b < a.nq + a.nk) quant_rows_tile<FQK, D>(a.x[1], a.Sk, a.codes[1], a.scales[1], b - a.nq, atom);
+  auto rows = [&](const uint16_t* x, int S, uint8_t* codes, uint8_t* scales, int64_t tid) {
+    if constexpr (FQK == 5) quant_rows_tile_nv<D>(x, S, codes, scales, tid, atom);   // NVFP4 Q and K
+    else quant_rows_tile<FQK, D>(x, S, codes, scales, tid, atom);
+  };
+  if (b < a.nq) rows(a.x[0], a.Sq, a.codes[0], a.scales[0], b);
+  else if (b < a.nq + a.nk) rows(a.x[1], a.Sk, a.codes[1], a.scales[1], b - a.nq);
   else quant_cols_tile<FV, D>(a.x[2], a.Sk, a.Spv, a.codes[2], a.scales[2], b - a.nq - a.nk, tile, atom);
 }
 
@@ -266,6 +339,7 @@ cudaError_t launch_mx_quant_rows(const void* x, int BH, int S, int D, int fmt, v
     case 0: return quant_rows_d<0>(xs, BH, S, D, c, s, st);
     case 1: return quant_rows_d<1>(xs, BH, S, D, c, s, st);
     case 4: return quant_rows_d<4>(xs, BH, S, D, c, s, st);
+    case 5: return quant_rows_d<5>(xs, BH, S, D, c, s, st);
     default: return quant_rows_d<2>(xs, BH, S, D, c, s, st);
   }
 }
@@ -321,6 +395,7 @@ cudaError_t launch_mx_quant_qkv(const void* q, const void* k, const void* v, int
     case 0: return quant_qkv_fv<0>(a, n, D, fv, st);
     case 1: return quant_qkv_fv<1>(a, n, D, fv, st);
     case 4: return quant_qkv_fv<4>(a, n, D, fv, st);
+    case 5: return quant_qkv_fv<5>(a, n, D, fv, st);
     default: return quant_qkv_fv<2>(a, n, D, fv, st);
   }
 }

@@ -28,7 +28,10 @@ def unpack_codes(raw, fmt, n_elems):
 
 
 def unpack_rows(codes, scales, fmt, B, H, S, D):
-    """FSA_MX_ROWS device buffers -> (codes [B,H,S,D], scales [B,H,S,D/32]); checks padding slots."""
+    """FSA_MX_ROWS device buffers -> (codes [B,H,S,D], scales [B,H,S,D/32]); checks padding slots.
+    fmt 5 (NVFP4): scales [B,H,S,D/16] from D/64 atoms per tile (rows past S: 0x38)."""
+    if fmt == 5:
+        return _unpack_rows_nvfp4(codes, scales, B, H, S, D)
     rb = D if fmt in (0, 1, 4) else D // 2
     c = unpack_codes(np.asarray(codes).reshape(B, H, S, rb), fmt, D)
     nt = (S + 127) // 128
@@ -41,6 +44,23 @@ def unpack_rows(codes, scales, fmt, B, H, S, D):
     used = np.zeros(flat.size, bool)
     used[idx.reshape(-1)] = True
     assert np.all(flat[~used] == 0x7F), "unused scale slots must be 0x7F"
+    return c, sc
+
+
+def _unpack_rows_nvfp4(codes, scales, B, H, S, D):
+    c = unpack_codes(np.asarray(codes).reshape(B, H, S, D // 2), 2, D)
+    nt, na = (S + 127) // 128, D // 64
+    flat = np.asarray(scales).reshape(-1)
+    assert flat.size == B * H * nt * na * 512
+    s_idx = np.arange(S)
+    blk = np.arange(D // 16)
+    off = ((s_idx // 128) * na * 512 + (s_idx % 32) * 16 + ((s_idx % 128) // 32) * 4)[:, None] + \
+          (blk // 4 * 512 + blk % 4)[None, :]                                                   # [S, D/16]
+    idx = (np.arange(B * H) * nt * na * 512)[:, None, None] + off[None]
+    sc = flat[idx].reshape(B, H, S, D // 16)
+    used = np.zeros(flat.size, bool)
+    used[idx.reshape(-1)] = True
+    assert np.all(flat[~used] == 0x38), "scale slots of rows past S must be 0x38"
     return c, sc
 
 

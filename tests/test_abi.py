@@ -232,3 +232,34 @@ def test_mma_peak_argument_checks(lib):
     for kind, nn, n, it in ((4, 128, 1, 1), (-1, 128, 1, 1), (1, 64, 1, 1), (1, 128, 0, 1), (1, 256, 1, 0),
                             (1, 128, 70000, 1)):
         assert lib.fsa_mma_peak(kind, nn, n, it, None, ctypes.byref(fl), None) == fsa.FSA_ERR_INVALID_ARG
+
+
+def test_nvfp4_is_a_rows_qk_format_with_two_scale_atoms(lib):
+    """NVFP4 (fsa.h 5): Q/K rows only (D/64 scale atoms of 512 bytes per 128-row
+    tile), never V or P; the attention call takes it as fmt_qk on one CTA per query
+    tile with Q quantised beforehand, and refuses the persistent schedule and the
+    prologue-quantised Q before any launch."""
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import fsa_mx_tensor
+    assert fsa.fsa_mx_sizes(1, 32, 4096, 128, fsa.FSA_MX_ROWS, "NVFP4") == (32 * 4096 * 64, 32 * 32 * 1024)
+    assert fsa.fsa_mx_sizes(1, 8, 300, 64, fsa.FSA_MX_ROWS, "NVFP4") == (8 * 300 * 32, 8 * 3 * 512)
+    with pytest.raises(fsa.FsaError):
+        fsa.fsa_mx_sizes(1, 8, 300, 128, fsa.FSA_MX_COLS_T, "NVFP4")
+    vp = ctypes.c_void_p
+    t = fsa_mx_tensor(16, 16, 5, 0, 1, 1, 128, 128)
+    v = fsa_mx_tensor(16, 16, 5, 1, 1, 1, 128, 128)
+    v2 = fsa_mx_tensor(16, 16, 2, 1, 1, 1, 128, 128)
+
+    def args(q, vv, fq, fp, o):
+        return (ctypes.byref(q), ctypes.byref(t), ctypes.byref(vv), vp(16), 1, 1, 1, 128, 128, 128, 0,
+                ctypes.c_float(0.125), fq, fp, ctypes.byref(o), vp(0), vp(0))
+    o = fsa.default_opts()
+    assert lib.fsa_attention_fwd_ex(*args(t, v, 5, 5, o)) == fsa.FSA_ERR_UNSUPPORTED_FMT     # NVFP4 as PV
+    o.schedule = 2                     # FSA_SCHED_PERSISTENT
+    assert lib.fsa_attention_fwd_ex(*args(t, v2, 5, 2, o)) == fsa.FSA_ERR_UNSUPPORTED_FMT
+    o = fsa.default_opts()
+    assert lib.fsa_attention_fwd_qbf16(vp(16), ctypes.byref(t), ctypes.byref(v2), vp(16), 1, 1, 1, 128, 128, 128,
+                                       0, ctypes.c_float(0.125), 5, 2, ctypes.byref(o), vp(0),
+                                       vp(0)) == fsa.FSA_ERR_UNSUPPORTED_FMT
+    x = fsa_mx_tensor(16, 16, 0, 0, 0, 0, 0, 0)
+    assert lib.fsa_mx_quantize(vp(16), 1, 1, 128, 128, 1, 5, ctypes.byref(x), vp(0)) == fsa.FSA_ERR_INVALID_ARG

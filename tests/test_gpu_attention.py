@@ -9,7 +9,7 @@ from workloads import WORKLOADS, Workload, generate, sample_rows, small, to_bf16
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4}
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4, "NVFP4": 5}
 SPLIT_MASK = 0x77777777          # key positions 4k+3 use the cubic, the rest the hardware exp2
 TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
 # error vs fp64 exact over the error of exact softmax with the same MX operands (the
@@ -17,7 +17,7 @@ TOL_EMU = 2e-3                   # max |O - O_emu| / rms(O_emu)
 # the chosen rule reaches on the parity cases plus 5%, by QK^T format: E2M1 1.121
 # (300 keys, non-causal, margin 8), E3M2 1.159 (300 keys, margin 0)
 FLOOR_EXP = 1.1
-FLOOR_EFQ = {"E2M1": 1.18, "E3M2": 1.22}
+FLOOR_EFQ = {"E2M1": 1.18, "E3M2": 1.22, "NVFP4": 1.18}
 
 
 def _fsa():
@@ -51,8 +51,8 @@ def oracle_mx(w, q, k, v, rows, mask, delta=0.0, with_floor=True):
     fq, fp = FMT[w.fmt_qk], FMT[w.fmt_pv]
     fv = 2 if fp == 3 else fp
     mx = oracle.MxInputs.from_bf16(q, k, v, fq, fv)
-    emu = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=delta, mufu_mask=mask)
-    res = dict(emu=emu["out"], fallbacks=emu["fallbacks"], tiles=emu["tiles"])
+    emu = oracle.fsa_emulate(mx, w.Sk, w.causal, w.scale, fp, rows, delta=delta, mufu_mask=mask, ambiguity=True)
+    res = dict(emu=emu["out"], fallbacks=emu["fallbacks"], tiles=emu["tiles"], amb=emu["amb"])
     if with_floor:
         res["floor"] = oracle.attn_floor(mx, w.Sk, w.causal, w.scale, fv, rows)
         res["exact"] = oracle.attn_exact(q, k, v, w.causal, w.scale, rows)
@@ -64,11 +64,20 @@ def rel_err(a, ref):
 
 
 def check(w, gpu, orc, rows, floor_ratio=FLOOR_EXP):
+    """|O - O_emu| <= 2e-3 rms, plus, where the hardware exp2 (whose result the oracle
+    brackets, not reproduces) may land a code on the other side of a rounding boundary,
+    the oracle's bound of what that can change (amb).  At most 1% of the elements may
+    need that slack.  Rows whose fallback decision fp32 leaves undetermined (amb
+    infinite) get no slack."""
     o = gpu["out"][rows]
     emu = orc["emu"]
     rms = np.sqrt(np.mean(emu ** 2))
-    err = np.abs(o - emu).max() / rms
-    assert err <= TOL_EMU, f"{w.name}: max|O-O_emu|/rms = {err:.3e}"
+    d = np.abs(o - emu)
+    amb = orc.get("amb", np.zeros_like(emu))
+    slack = np.where(np.isfinite(amb), amb, 0.0)
+    assert np.all(d <= TOL_EMU * rms + slack), f"{w.name}: max|O-O_emu|/rms = {d.max() / rms:.3e}"
+    beyond = d > TOL_EMU * rms
+    assert beyond.mean() <= 0.01, f"{w.name}: {int(beyond.sum())} elements beyond 2e-3 rms"
     if "exact" in orc and floor_ratio is not None:
         e_gpu, e_floor = rel_err(o, orc["exact"]), rel_err(orc["floor"], orc["exact"])
         assert e_gpu <= floor_ratio * e_floor, f"{w.name}: error {e_gpu:.4f} vs floor {e_floor:.4f}"
@@ -87,7 +96,8 @@ def test_tiny_config_all_rows():
 
 
 PAIRS = [("E4M3", "E4M3"), ("E2M3", "E2M1"), ("E2M1", "E2M1_EFQ"), ("E2M3", "E2M3"), ("E2M1", "E2M1"),
-         ("E4M3", "E2M1"), ("E2M1", "E4M3"), ("E3M2", "E3M2"), ("E3M2", "E2M1_EFQ"), ("E2M3", "E3M2")]
+         ("E4M3", "E2M1"), ("E2M1", "E4M3"), ("E3M2", "E3M2"), ("E3M2", "E2M1_EFQ"), ("E2M3", "E3M2"),
+         ("NVFP4", "E2M1_EFQ"), ("NVFP4", "E4M3"), ("NVFP4", "E2M1")]
 
 
 @pytest.mark.parametrize("causal", [False, True])

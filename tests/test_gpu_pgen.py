@@ -124,6 +124,8 @@ SMALL = [
     (Workload("pg_efq_d64", 1, 2, 1, 200, 700, 64, False, "E2M1", "E2M1_EFQ", 36), 1, 8.0),
     (Workload("pg_e3m2", 1, 2, 1, 256, 520, 128, True, "E3M2", "E3M2", 38, "planted"), 0, 0.0),
     (Workload("pg_e3m2_mufu", 1, 2, 1, 300, 300, 64, False, "E3M2", "E3M2", 39), 1, 8.0),
+    (Workload("pg_nvfp4_efq", 1, 4, 2, 384, 700, 128, True, "NVFP4", "E2M1_EFQ", 40, "planted"), 1, 0.0),
+    (Workload("pg_nvfp4_e4m3_d64", 1, 2, 1, 256, 300, 64, False, "NVFP4", "E4M3", 41), 0, 8.0),
 ]
 
 

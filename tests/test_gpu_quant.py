@@ -11,6 +11,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 FMTS = [0, 1, 2, 4]
+ROW_FMTS = FMTS + [5]            # NVFP4 (fsa.h 5) is a rows (Q/K) format only
 
 
 def _fsa():
@@ -71,7 +72,7 @@ def _check_cols(x_bits, fmt):
     np.testing.assert_array_equal(c, oc)
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", ROW_FMTS)
 @pytest.mark.parametrize("shape", [(1, 2, 300, 128), (2, 1, 77, 64), (1, 1, 1, 128), (1, 3, 129, 64)])
 def test_quant_rows_edge(fmt, shape):
     _check_rows(edge_tensor(shape, 10 + fmt), fmt)
@@ -85,7 +86,7 @@ def test_quant_cols_edge(fmt, shape):
     _check_cols(x, fmt)
 
 
-@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("fmt", ROW_FMTS)
 def test_quant_nonfinite_block(fmt):
     x = np.random.default_rng(1).standard_normal((1, 1, 64, 128)).astype(np.float32)
     x[0, 0, 3, 40] = np.inf
@@ -112,6 +113,8 @@ def test_quant_full_workloads(name):
     (2, 0, 1, 1, 1, 512, 384, 64),
     (4, 4, 1, 2, 1, 300, 260, 128),      # E3M2 both
     (4, 2, 1, 2, 2, 100, 130, 64),
+    (5, 2, 1, 4, 2, 300, 260, 128),      # NVFP4 Q/K, E2M1 V
+    (5, 0, 2, 2, 1, 77, 129, 64),        # NVFP4 Q/K, E4M3 V, D 64
 ])
 def test_quant_qkv_one_launch(fq, fv, B, H, Hkv, Sq, Sk, D):
     """The one-launch Q/K/V form writes the codes and scales of three separate

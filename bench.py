@@ -37,13 +37,13 @@ from workloads import WORKLOADS, Workload, generate  # noqa: E402
 DEFAULT_WORKLOAD = "long_efq_128k"
 # further workloads reported in the same line (kernel throughput, fraction of the
 # measured peak, speedup over the BF16 kernel, fallback rate)
-EXTRA_WORKLOADS = ["long_fp8_16k", "long_fp8_128k", "long_efq_16k", "video_dit", "adversarial"]
-FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4}
+EXTRA_WORKLOADS = ["long_fp8_16k", "long_fp8_128k", "long_efq_16k", "long_nvfp4_128k", "video_dit", "adversarial"]
+FMT = {"E4M3": 0, "E2M3": 1, "E2M1": 2, "E2M1_EFQ": 3, "E3M2": 4, "NVFP4": 5}
 # tensor-core kind of each operand format: 0 kind::f16, 1 kind::mxf8f6f4, 2 kind::mxf4
-KIND = {"E4M3": 1, "E2M3": 1, "E3M2": 1, "E2M1": 2, "E2M1_EFQ": 2}
+KIND = {"E4M3": 1, "E2M3": 1, "E3M2": 1, "E2M1": 2, "E2M1_EFQ": 2, "NVFP4": 3}
 # nominal dense ratio of each kind to BF16 on GB300 (2.25 / 4.5 / 13.5 PFLOP/s): used
 # only when the probe could not run
-KIND_RATIO = {0: 1.0, 1: 2.0, 2: 6.0}
+KIND_RATIO = {0: 1.0, 1: 2.0, 2: 6.0, 3: 6.0}
 # DRAM bytes (read + write) of one attention launch of the current kernel build, from
 # an ncu capture, by workload; absent: not captured for this build
 TRAFFIC = {"long_efq_128k": 13.41e9 + 2.10e9, "long_efq_16k": 53.61e6 + 208.38e6,

@@ -36,7 +36,7 @@ FLOOR_RATIO = {"exp": 1.1, "efq": 1.18}
 # (workload, sampled rows per head)
 CASES = [("prefill", 256), ("long_fp8_16k", 256), ("long_fp8_32k", 256), ("long_fp8_64k", 128),
          ("long_fp8_128k", 64), ("long_efq_16k", 256), ("long_efq_32k", 256), ("long_efq_64k", 256),
-         ("long_efq_128k", 256), ("video_dit", 128)] + \
+         ("long_efq_128k", 256), ("long_nvfp4_16k", 256), ("long_nvfp4_128k", 64), ("video_dit", 128)] + \
         [(f"adversarial.L{l}", 256 if l < 2 else 32) for l in range(12)]
 
 

@@ -75,6 +75,10 @@ WORKLOADS = {
 for _S in (16384, 32768, 65536, 131072):
     WORKLOADS[f"long_efq_{_S // 1024}k"] = _long(_S, "E2M1", "E2M1_EFQ", "efq")
     WORKLOADS[f"long_fp8_{_S // 1024}k"] = _long(_S, "E4M3", "E4M3", "fp8")
+# 4''. the long-context EFQ run with NVFP4 Q and K (16-element E4M3 scales), an
+# operand format adjacent to the pages' MX ones
+for _S in (16384, 131072):
+    WORKLOADS[f"long_nvfp4_{_S // 1024}k"] = _long(_S, "NVFP4", "E2M1_EFQ", "nvfp4")
 
 
 def small(w: Workload, Sq: int, Sk: int | None = None, H: int | None = None, Hkv: int | None = None,

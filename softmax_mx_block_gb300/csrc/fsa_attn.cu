@@ -153,18 +153,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
+// clamp(floor(t) - emax, -127, 127) in fp32 (exact on these integers; NaN and -inf
+// give -127, +inf 127): no conversions to and from integers on the path
+__device__ __forceinline__ float block_exp_f(float t, int emax) {
+  return fminf(fmaxf(__fadd_rn(floorf(t), -(float)emax), -127.0f), 127.0f);
+}
+// scale byte E + 127: the low bits of E + 127 + 2^23 (an integer below 2^23, exact)
+__device__ __forceinline__ uint32_t scale_byte_f(float E) { return __float_as_uint(__fadd_rn(E, 8388735.0f)) & 0xFFu; }
+
 // Exponent-only block scale: E = clamp(floor(fp32(fp32(smax*c) - M)) - emax, -127, 127).
-// Returns E and writes -fp32(M + E).  A block with no visible key (smax = -inf)
+// Returns E (as fp32) and writes -fp32(M + E).  A block with no visible key (smax = -inf)
 // gets E = -127; its scores are -inf, so every code comes out 0.  A row with no
 // visible key at all so far (M = -inf: causal rows before the first key) gets the
 // shift 0, so that its residuals are -inf as well (not -inf + inf, whose NaN a
 // format without a NaN code would saturate to a nonzero code).
 template <int FPV>
-__device__ __forceinline__ int block_exp(float bmax, float c, float M, float& nbE) {
+__device__ __forceinline__ float block_exp(float bmax, float c, float M, float& nbE) {
   const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
-  int E = (int)fmaxf(floorf(tmax), -256.0f) - Fmt<FPV>::emax;
-  E = E < -127 ? -127 : (E > 127 ? 127 : E);
-  nbE = M == kNegInf ? 0.0f : -__fadd_rn(M, (float)E);
+  const float E = block_exp_f(tmax, Fmt<FPV>::emax);
+  nbE = M == kNegInf ? 0.0f : -__fadd_rn(M, E);
   return E;
 }
 
@@ -192,9 +199,8 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
     // delta <= 120, and a (3 - phi) + b < 7.49), so the nibbles need no fix; EXPM 0:
     // any constants, nibbles equal to 8 become 7.
     const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
-    int E = (int)fmaxf(floorf(__fadd_rn(tmax, p.efq_phi)), -256.0f) - 2;
-    E = E < -127 ? -127 : (E > 127 ? 127 : E);
-    const float bE = __fadd_rn(M, (float)E);
+    const float Ef = block_exp_f(__fadd_rn(tmax, p.efq_phi), 2);
+    const float bE = __fadd_rn(M, Ef);
     // Bk / 8 = fp32(b/8 - fp32(a/8 * bE)): the same roundings as fp32(b - fp32(a bE)), scaled
     const float b8 = __fsub_rn(p.efq_b8, __fmul_rn(p.efq_a8, bE));
     const float a8 = p.efq_A8;
@@ -218,10 +224,10 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
       // has bit 3)
       out[w] = EXPM == 1 ? wv : wv - ((wv >> 3) & 0x11111111u);
     }
-    return (uint32_t)(E + 127);
+    return scale_byte_f(Ef);
   } else {
     float nb;
-    const int E = block_exp<FPV>(bmax, c, M, nb);
+    const float Ef = block_exp<FPV>(bmax, c, M, nb);
     const uint64_t c2 = pk2(c, c), nb2 = pk2(nb, nb);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) upk2(ffma2(pk2(v[i], v[i + 1]), c2, nb2), v[i], v[i + 1]);
@@ -247,7 +253,7 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
         out[w] = prmt(prmt(b01, b23, 0x0040u), prmt(b45, b67, 0x0040u), 0x5410u);
       }
     }
-    return (uint32_t)(E + 127);
+    return scale_byte_f(Ef);
   }
 }
 

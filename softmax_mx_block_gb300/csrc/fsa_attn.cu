@@ -153,10 +153,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// clamp(floor(t) - emax, -127, 127) in fp32 (exact on these integers; NaN and -inf
-// give -127, +inf 127): no conversions to and from integers on the path
+// clamp(floor(t) - emax, -127, 127) in fp32, on the FMA pipe only (no conversions,
+// no floorf): floor(t) is t + 1.5*2^23 rounded down, minus 1.5*2^23, exact for
+// |t| < 2^22; a larger |t| only moves a result the clamp takes to -127 or 127 anyway
+// (the sum stays on the same side), and NaN and -inf give -127, +inf 127
 __device__ __forceinline__ float block_exp_f(float t, int emax) {
-  return fminf(fmaxf(__fadd_rn(floorf(t), -(float)emax), -127.0f), 127.0f);
+  const float fl = __fsub_rn(__fadd_rd(t, 12582912.0f), 12582912.0f);
+  return fminf(fmaxf(__fadd_rn(fl, -(float)emax), -127.0f), 127.0f);
 }
 // scale byte E + 127: the low bits of E + 127 + 2^23 (an integer below 2^23, exact)
 __device__ __forceinline__ uint32_t scale_byte_f(float E) { return __float_as_uint(__fadd_rn(E, 8388735.0f)) & 0xFFu; }

@@ -156,13 +156,23 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // clamp(floor(t) - emax, -127, 127) in fp32, on the FMA pipe only (no conversions,
 // no floorf): floor(t) is t + 1.5*2^23 rounded down, minus 1.5*2^23, exact for
 // |t| < 2^22; a larger |t| only moves a result the clamp takes to -127 or 127 anyway
-// (the sum stays on the same side), and NaN and -inf give -127, +inf 127
-__device__ __forceinline__ float block_exp_f(float t, int emax) {
-  const float fl = __fsub_rn(__fadd_rd(t, 12582912.0f), 12582912.0f);
-  return fminf(fmaxf(__fadd_rn(fl, -(float)emax), -127.0f), 127.0f);
+// (the sum stays on the same side), and NaN and -inf give -127, +inf 127.
+// FOLD: subtract 1.5*2^23 + emax at once (the same exact integer subtraction, one
+// add fewer); the exp paths keep the separate add, which measured faster there.
+template <int EMAX, bool FOLD>
+__device__ __forceinline__ float block_exp_f(float t) {
+  static_assert(EMAX >= 0 && EMAX < 64, "exponent offset");
+  const float fl = FOLD ? __fsub_rn(__fadd_rd(t, 12582912.0f), 12582912.0f + (float)EMAX)
+                        : __fadd_rn(__fsub_rn(__fadd_rd(t, 12582912.0f), 12582912.0f), -(float)EMAX);
+  return fminf(fmaxf(fl, -127.0f), 127.0f);
 }
-// scale byte E + 127: the low bits of E + 127 + 2^23 (an integer below 2^23, exact)
-__device__ __forceinline__ uint32_t scale_byte_f(float E) { return __float_as_uint(__fadd_rn(E, 8388735.0f)) & 0xFFu; }
+// scale byte E + 127 in the low byte of the bits of E + 127 + 2^23 (an integer below
+// 2^24, exact); the caller gathers the low bytes of a tile's four blocks into one word
+__device__ __forceinline__ uint32_t scale_word_f(float E) { return __float_as_uint(__fadd_rn(E, 8388735.0f)); }
+// bytes 0 of a, b, c, d as one word (a in the low byte)
+__device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+}
 
 // Exponent-only block scale: E = clamp(floor(fp32(fp32(smax*c) - M)) - emax, -127, 127).
 // Returns E (as fp32) and writes -fp32(M + E).  A block with no visible key (smax = -inf)
@@ -173,7 +183,7 @@ __device__ __forceinline__ uint32_t scale_byte_f(float E) { return __float_as_ui
 template <int FPV>
 __device__ __forceinline__ float block_exp(float bmax, float c, float M, float& nbE) {
   const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
-  const float E = block_exp_f(tmax, Fmt<FPV>::emax);
+  const float E = block_exp_f<Fmt<FPV>::emax, false>(tmax);
   nbE = M == kNegInf ? 0.0f : -__fadd_rn(M, E);
   return E;
 }
@@ -186,7 +196,7 @@ __device__ __forceinline__ float fma_sat(float a, float b, float c) {
 
 // P codes of one 32-key block, in place: v[0..32) holds the raw scores (masked =
 // -inf) on entry and is clobbered.  Writes 8 packed words (one byte per code) or 4
-// (E2M1) to out[] and returns the scale byte E + 127.
+// (E2M1) to out[] and returns a word whose low byte is the scale byte E + 127.
 template <int FPV, int EXPM>
 __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, float M, const KParams& p, uint32_t* out) {
   if constexpr (FPV == F_EFQ) {
@@ -202,7 +212,7 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
     // delta <= 120, and a (3 - phi) + b < 7.49), so the nibbles need no fix; EXPM 0:
     // any constants, nibbles equal to 8 become 7.
     const float tmax = __fsub_rn(__fmul_rn(bmax, c), M);
-    const float Ef = block_exp_f(__fadd_rn(tmax, p.efq_phi), 2);
+    const float Ef = block_exp_f<2, true>(__fadd_rn(tmax, p.efq_phi));
     const float bE = __fadd_rn(M, Ef);
     // Bk / 8 = fp32(b/8 - fp32(a/8 * bE)): the same roundings as fp32(b - fp32(a bE)), scaled
     const float b8 = __fsub_rn(p.efq_b8, __fmul_rn(p.efq_a8, bE));
@@ -227,7 +237,7 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
       // has bit 3)
       out[w] = EXPM == 1 ? wv : wv - ((wv >> 3) & 0x11111111u);
     }
-    return scale_byte_f(Ef);
+    return scale_word_f(Ef);
   } else {
     float nb;
     const float Ef = block_exp<FPV>(bmax, c, M, nb);
@@ -256,7 +266,7 @@ __device__ __forceinline__ uint32_t pgen_block(float* v, float bmax, float c, fl
         out[w] = prmt(prmt(b01, b23, 0x0040u), prmt(b45, b67, 0x0040u), 0x5410u);
       }
     }
-    return scale_byte_f(Ef);
+    return scale_word_f(Ef);
   }
 }
 
@@ -743,16 +753,21 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // depend on, which gives them that much longer to finish.
         constexpr int HW = C::P_COLS / 2;             // words (columns) per half
         const uint32_t tp = tl + C::T_P + C::P_COLS * (j % C::NPB);
-        uint32_t sw = 0;
+        uint32_t sw = 0;                            // the blocks' scale bytes, block b in byte b
+        // EFQ: the blocks' scale words, gathered by byte permutes (one instruction fewer
+        // per block; the exp paths keep the shifts, which measured faster there)
+        uint32_t swb[NBLK] = {};
         uint64_t acc = pk2(0.0f, 0.0f);               // BF16: sum of the rounded p
         const float nM = M == kNegInf ? 0.0f : -M;    // BF16, no visible key yet: every s is -inf, p = 0
         auto gen_half = [&](int hf, uint32_t* pw) {
           if constexpr (MX) {
             constexpr int WB = C::P_COLS / NBLK;       // words per block: 8, or 4 for E2M1
 #pragma unroll
-            for (int b = 0; b < 2; ++b)
-              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p, pw + WB * b)
-                    << (8 * (2 * hf + b));
+            for (int b = 0; b < 2; ++b) {
+              const uint32_t w = pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p, pw + WB * b);
+              if constexpr (FPV == F_EFQ) swb[2 * hf + b] = w;
+              else sw |= (w & 0xFFu) << (8 * (2 * hf + b));
+            }
           } else {
             const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
 #pragma unroll
@@ -811,6 +826,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           dbg_words(1, pw);
           tmem_st_cols<HW>(tp + HW, pw);
           // A scales of the PV MMA: lane quadrant q reads column base + q
+          if constexpr (FPV == F_EFQ) sw = low_bytes4(swb[0], swb[1], swb[2], swb[3]);
           if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
           if constexpr (DBG) {
             if (dbg_on) dbg.sf[dbg_row * nkt + j] = sw;

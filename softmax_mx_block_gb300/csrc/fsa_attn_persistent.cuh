@@ -239,7 +239,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
         // depend on, which gives them that much longer to finish.
         constexpr int HW = C::P_COLS / 2;             // words (columns) per half
         const uint32_t tp = tl + C::T_P + C::P_COLS * (g % C::NPB);
-        uint32_t sw = 0;
+        uint32_t swb[NBLK] = {};                    // scale bytes of the blocks (low bytes)
         uint64_t acc = pk2(0.0f, 0.0f);               // BF16: sum of the rounded p
         const float nM = M == kNegInf ? 0.0f : -M;    // BF16, no visible key yet: every s is -inf, p = 0
         auto gen_half = [&](int hf, uint32_t* pw) {
@@ -247,8 +247,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
             constexpr int WB = C::P_COLS / NBLK;       // words per block: 8, or 4 for E2M1
 #pragma unroll
             for (int b = 0; b < 2; ++b)
-              sw |= pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p, pw + WB * b)
-                    << (8 * (2 * hf + b));
+              swb[2 * hf + b] = pgen_block<FPV, EXPM>(sv + 64 * hf + 32 * b, bm[2 * hf + b], c, M, p, pw + WB * b);
           } else {
             const uint64_t c2 = pk2(c, c), nM2 = pk2(nM, nM);
 #pragma unroll
@@ -295,6 +294,7 @@ __device__ __forceinline__ TileState softmax_tiles(uint32_t tl, uint64_t* s_full
           gen_half(1, pw);
           tmem_st_cols<HW>(tp + HW, pw);
           // A scales of the PV MMA: lane quadrant q reads column base + q
+          const uint32_t sw = low_bytes4(swb[0], swb[1], swb[2], swb[3]);
           if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
           if constexpr (!MX) {
             float a0, a1;

@@ -322,6 +322,54 @@ int fsa_attention_fwd_layers(const fsa_layer* layers, int n_layers, const fsa_op
 int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, float step, float max_delta,
                    float* delta);
 
+/* ------------------------------------------------------- from host memory */
+/* Inputs and output of one attention call in HOST memory (page-locked memory lets
+ * the copies run asynchronously and overlap; pageable memory works, without the
+ * overlap).  q [B][H][Sq][D], k and v [B][Hkv][Sk][D] bf16; out [B][H][Sq][D] fp32
+ * or bf16 per opts->out_dtype. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  void*       out;
+} fsa_host_io;
+
+/* The caller's device buffers for the same call: q, k, v bf16 of the host shapes,
+ * out of the output's shape and dtype, and the three MX tensors (codes and scales
+ * of fsa_mx_sizes bytes for q and k in FSA_MX_ROWS / fmt_qk and v in
+ * FSA_MX_COLS_T / the storage format of fmt_pv).  All 16-byte aligned. */
+typedef struct {
+  void*          q;
+  void*          k;
+  void*          v;
+  fsa_mx_tensor* q_mx;
+  fsa_mx_tensor* k_mx;
+  fsa_mx_tensor* v_mx;
+  void*          out;
+} fsa_device_io;
+
+/* The attention of fsa_attention_fwd_ex (the Fused-Softmax brief, abstract; the
+ * pages say nothing of where the operands live) on operands in host memory.  The
+ * call is split into n_chunks groups of whole kv heads (a kv head with its H/Hkv
+ * query heads; n_chunks <= 0: min(B*Hkv, 8)), and for each group: Q, K and V are
+ * copied host to device on a stream of the library's own, quantised
+ * (fsa_mx_quantize_qkv) and attended on `stream` once they have landed, and O
+ * copied back on a second stream of its own while the next group computes.  The
+ * output is bit-identical to quantising and attending the whole call at once (every
+ * head is computed by the same kernels on the same data).  Nothing is allocated on
+ * the device; the two streams and the events are created by the call and released
+ * when their work completes.  On return the work is enqueued: `stream` completes
+ * after the last copy back, so synchronising it makes host->out valid.  The MX
+ * tensors' shape, layout and format fields are written as fsa_mx_quantize_qkv
+ * would.  opts as fsa_attention_fwd_ex (row_fallbacks: device [B][H][Sq]; a debug
+ * dump is refused); stats accumulates over the groups.  Not for CUDA graph capture.
+ * Errors: FSA_ERR_INVALID_ARG (null or misaligned pointer, bad shape or option),
+ * FSA_ERR_UNSUPPORTED_FMT, FSA_ERR_LAUNCH (a stream, event, copy or launch failed;
+ * what was enqueued before the failure still completes before `stream` does). */
+int fsa_attention_fwd_host(const fsa_host_io* host, const fsa_device_io* dev, int B, int H, int Hkv, int Sq,
+                           int Sk, int D, int causal, float scale, int fmt_qk, int fmt_pv, const fsa_opts* opts,
+                           fsa_stats* stats, int n_chunks, void* stream);
+
 /* ------------------------------------------------------ tensor-core peak probe */
 /* Measurement instrument (the roofline denominator of the attention kernels; the
  * Fused-Softmax brief, abstract, quotes its kernels' throughput on the block-

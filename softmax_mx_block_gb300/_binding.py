@@ -63,6 +63,16 @@ class fsa_layer(ctypes.Structure):
                 ("stats", ctypes.c_void_p)]
 
 
+class fsa_host_io(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+
+
+class fsa_device_io(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("q_mx", ctypes.POINTER(fsa_mx_tensor)), ("k_mx", ctypes.POINTER(fsa_mx_tensor)),
+                ("v_mx", ctypes.POINTER(fsa_mx_tensor)), ("out", ctypes.c_void_p)]
+
+
 FSA_OUT_F32, FSA_OUT_BF16 = 0, 1
 STATS_BYTES = 24      # fsa_stats: u64 fallback_events, u64 row_tiles, i32 status, i32 reserved
 
@@ -94,6 +104,8 @@ def load(build_if_missing: bool = True):
             L.fsa_attention_fwd_layers.argtypes = [ctypes.POINTER(fsa_layer), i, ctypes.POINTER(fsa_opts), vp]
             L.fsa_attention_fwd_qbf16.argtypes = [vp] + [ctypes.POINTER(fsa_mx_tensor)] * 2 + \
                 [vp, i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, vp]
+            L.fsa_attention_fwd_host.argtypes = [ctypes.POINTER(fsa_host_io), ctypes.POINTER(fsa_device_io),
+                                                 i, i, i, i, i, i, i, f, i, i, ctypes.POINTER(fsa_opts), vp, i, vp]
             L.fsa_tune_delta.argtypes = [ctypes.POINTER(fsa_stats), i, f, f, f, ctypes.POINTER(ctypes.c_float)]
             L.fsa_mma_peak.argtypes = [i, i, i, ctypes.c_longlong, vp, ctypes.POINTER(ctypes.c_double), vp]
             L.fsa_bf16_transpose_v.argtypes = [vp, vp, i, i, i, i, vp]
@@ -104,7 +116,8 @@ def load(build_if_missing: bool = True):
             L.fsa_status_string.restype = ctypes.c_char_p
             for n in ("fsa_mx_sizes", "fsa_mx_quantize", "fsa_mx_quantize_qkv", "fsa_attention_fwd",
                       "fsa_attention_fwd_ex", "fsa_bf16_transpose_v", "fsa_attention_fwd_bf16", "fsa_version",
-                      "fsa_attention_fwd_layers", "fsa_tune_delta", "fsa_mma_peak", "fsa_attention_fwd_qbf16"):
+                      "fsa_attention_fwd_layers", "fsa_tune_delta", "fsa_mma_peak", "fsa_attention_fwd_qbf16",
+                      "fsa_attention_fwd_host"):
                 getattr(L, n).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -406,6 +419,91 @@ def fsa_attention_fwd_layers(layers, *, out_dtype=None, stream=None, **opt_kw) -
     o = _opts(out_dtype=od, **opt_kw)
     _check(load().fsa_attention_fwd_layers(arr, n, ctypes.byref(o), _stream(stream)), "fsa_attention_fwd_layers")
     return outs
+
+
+class HostCallBuffers:
+    """Device buffers of fsa_attention_fwd_host for one call shape and format pair:
+    bf16 Q, K, V, the three MX tensors and the output, all owned by torch."""
+
+    def __init__(self, B, H, Hkv, Sq, Sk, D, fmt_qk, fmt_pv, out_dtype=None, device=None):
+        dev = torch.device(device or "cuda")
+        fmt_qk, fmt_pv = _fmt(fmt_qk), _fmt(fmt_pv)
+        fv = FSA_FMT_E2M1 if fmt_pv == FSA_FMT_E2M1_EFQ else fmt_pv
+        _, tdt = _out_dtype(out_dtype)
+        self.shape = (B, H, Hkv, Sq, Sk, D)
+        self.q = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=dev)
+        self.k = torch.empty((B, Hkv, Sk, D), dtype=torch.bfloat16, device=dev)
+        self.v = torch.empty((B, Hkv, Sk, D), dtype=torch.bfloat16, device=dev)
+        self.mx = (empty_mx(B, H, Sq, D, FSA_MX_ROWS, fmt_qk, dev), empty_mx(B, Hkv, Sk, D, FSA_MX_ROWS, fmt_qk, dev),
+                   empty_mx(B, Hkv, Sk, D, FSA_MX_COLS_T, fv, dev))
+        self.out = torch.empty((B, H, Sq, D), dtype=tdt, device=dev)
+
+    @classmethod
+    def from_tensors(cls, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mx, out: torch.Tensor):
+        """Wrap existing device tensors (bf16 q, k, v; the (q, k, v) MxTensors; out)."""
+        self = cls.__new__(cls)
+        B, H, Sq, D = q.shape
+        self.shape = (B, H, k.shape[1], Sq, k.shape[2], D)
+        self.q, self.k, self.v, self.mx, self.out = q, k, v, tuple(mx), out
+        return self
+
+
+def fsa_attention_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None, *,
+                           buffers: HostCallBuffers | None = None, fmt_qk="E4M3", fmt_pv="E4M3", causal=False,
+                           scale=None, n_chunks=0, stats=None, row_fallbacks: torch.Tensor | None = None,
+                           out_dtype=None, stream=None, **opt_kw) -> torch.Tensor:
+    """O [B,H,Sq,D] in host memory from bf16 q, k, v in host memory (fsa_attention_fwd_host):
+    copies in, quantisation, attention and copies back by groups of kv heads, the copies
+    overlapping the compute.  Page-locked (pinned) tensors give the overlap.  The work is
+    enqueued on `stream` (default: the current one): synchronise it before reading out."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise FsaError(FSA_ERR_INVALID_ARG, f"{n} must be a contiguous bf16 host tensor")
+    B, H, Sq, D = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Sk, D) or tuple(v.shape) != (B, Hkv, Sk, D):
+        raise FsaError(FSA_ERR_INVALID_ARG, "q, k, v shapes")
+    fmt_qk, fmt_pv = _fmt(fmt_qk), _fmt(fmt_pv)
+    od, tdt = _out_dtype(out_dtype if out is None or out_dtype is not None else out.dtype)
+    if buffers is None:
+        buffers = HostCallBuffers(B, H, Hkv, Sq, Sk, D, fmt_qk, fmt_pv, tdt)
+    if buffers.shape != (B, H, Hkv, Sq, Sk, D) or buffers.out.dtype != tdt:
+        raise FsaError(FSA_ERR_INVALID_ARG, "buffers were made for another shape or output dtype")
+    dev = buffers.out.device
+    for t, n in ((buffers.q, "buffers.q"), (buffers.k, "buffers.k"), (buffers.v, "buffers.v"),
+                 (buffers.out, "buffers.out")):
+        _need_cuda(t, n)
+    fv = FSA_FMT_E2M1 if fmt_pv == FSA_FMT_E2M1_EFQ else fmt_pv
+    for m, (f, layout), n in zip(buffers.mx, ((fmt_qk, FSA_MX_ROWS), (fmt_qk, FSA_MX_ROWS), (fv, FSA_MX_COLS_T)),
+                                 ("q_mx", "k_mx", "v_mx")):
+        if m.fmt != f or m.layout != layout:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"buffers.{n} was made for another format")
+        _need_mx(m, f"buffers.{n}", dev)
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=tdt, pin_memory=True)
+    if out.is_cuda or out.dtype != tdt or not out.is_contiguous() or out.numel() < B * H * Sq * D:
+        raise FsaError(FSA_ERR_INVALID_ARG, f"out must be a contiguous {tdt} host tensor of B*H*Sq*D elements")
+    if stats is not None:
+        _need_cuda(stats, "stats")
+        if stats.device != dev or stats.numel() * stats.element_size() < STATS_BYTES:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"stats must hold {STATS_BYTES} bytes on {dev}")
+    o = _opts(out_dtype=od, **opt_kw)
+    if row_fallbacks is not None:
+        _need_cuda(row_fallbacks, "row_fallbacks", torch.int32)
+        if row_fallbacks.device != dev or row_fallbacks.numel() < B * H * Sq:
+            raise FsaError(FSA_ERR_INVALID_ARG, f"row_fallbacks must hold B*H*Sq int32 on {dev}")
+        o.row_fallbacks = row_fallbacks.data_ptr()
+    hio = fsa_host_io(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr())
+    structs = tuple(m.struct() for m in buffers.mx)
+    dio = fsa_device_io(buffers.q.data_ptr(), buffers.k.data_ptr(), buffers.v.data_ptr(),
+                        ctypes.pointer(structs[0]), ctypes.pointer(structs[1]), ctypes.pointer(structs[2]),
+                        buffers.out.data_ptr())
+    scale = D ** -0.5 if scale is None else scale
+    _check(load().fsa_attention_fwd_host(ctypes.byref(hio), ctypes.byref(dio), B, H, Hkv, Sq, Sk, D,
+                                         int(bool(causal)), float(scale), fmt_qk, fmt_pv, ctypes.byref(o),
+                                         ctypes.c_void_p(stats.data_ptr() if stats is not None else 0),
+                                         int(n_chunks), _stream(stream)), "fsa_attention_fwd_host")
+    return out
 
 
 def fsa_tune_delta(stats: list, deltas: list, target_rate=0.01, step=4.0, max_delta=64.0) -> list:

@@ -1,6 +1,7 @@
 // fsa_api.cu -- the C ABI of libfsa (declared in include/fsa.h): argument
 // checks, TMA tensor-map construction and kernel dispatch.  No entry point
-// allocates device memory; all buffers belong to the caller.
+// allocates device memory; all buffers belong to the caller (the host-memory entry
+// point creates two streams and some events, released when their work completes).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -8,6 +9,7 @@
 #include <climits>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "fsa.h"
@@ -199,6 +201,15 @@ bool persistent_schedule(int schedule, int Sq, int Sk, int causal) {
   return tiles <= 32 * nq;
 }
 
+// a negative margin would make nearly every tile fall back; the EFQ constants keep
+// the code domain finite and the block exponent's reference point within one binade
+bool opts_ok(const fsa_opts& o) {
+  return !(o.exp_mode < 0 || o.exp_mode > 2 || !std::isfinite(o.delta) || o.delta < 0.0f ||
+           !(o.efq_a > 0.0f && o.efq_a <= 16.0f) || !(std::fabs(o.efq_b) <= 64.0f) ||
+           !(o.efq_phi >= 0.0f && o.efq_phi < 1.0f) || o.schedule < FSA_SCHED_AUTO ||
+           o.schedule > FSA_SCHED_PERSISTENT || (o.out_dtype != FSA_OUT_F32 && o.out_dtype != FSA_OUT_BF16));
+}
+
 void fill_common(fsa::KParams& p, int B, int H, int Hkv, int Sq, int Sk, int causal, float scale,
                  const fsa_opts* o, fsa_stats* stats) {
   p.B = B; p.H = H; p.Hkv = Hkv; p.Sq = Sq; p.Sk = Sk;
@@ -345,13 +356,7 @@ int attention_impl(const fsa_mx_tensor* q, const void* q_bf16, const fsa_mx_tens
   fsa_opts o;
   fsa_default_opts(&o);
   if (opts) o = *opts;
-  // a negative margin would make nearly every tile fall back; the EFQ constants keep
-  // the code domain finite and the block exponent's reference point within one binade
-  if (o.exp_mode < 0 || o.exp_mode > 2 || !std::isfinite(o.delta) || o.delta < 0.0f ||
-      !(o.efq_a > 0.0f && o.efq_a <= 16.0f) || !(std::fabs(o.efq_b) <= 64.0f) ||
-      !(o.efq_phi >= 0.0f && o.efq_phi < 1.0f) || o.schedule < FSA_SCHED_AUTO || o.schedule > FSA_SCHED_PERSISTENT ||
-      (o.out_dtype != FSA_OUT_F32 && o.out_dtype != FSA_OUT_BF16))
-    return FSA_ERR_INVALID_ARG;
+  if (!opts_ok(o)) return FSA_ERR_INVALID_ARG;
   const fsa_debug_dump* dbg = o.debug;
   if (dbg && (!dbg->s || !dbg->m || !dbg->p || !dbg->p_scales)) return FSA_ERR_INVALID_ARG;
   if (dbg && fmt_pv != FSA_FMT_E2M1_EFQ && o.exp_mode == FSA_EXP_SPLIT) return FSA_ERR_UNSUPPORTED_FMT;
@@ -479,6 +484,116 @@ int fsa_attention_fwd_layers(const fsa_layer* layers, int n_layers, const fsa_op
     if (st != FSA_OK) return st;
   }
   return FSA_OK;
+}
+
+int fsa_attention_fwd_host(const fsa_host_io* host, const fsa_device_io* dev, int B, int H, int Hkv, int Sq,
+                           int Sk, int D, int causal, float scale, int fmt_qk, int fmt_pv, const fsa_opts* opts,
+                           fsa_stats* stats, int n_chunks, void* stream) {
+  if (!host || !dev || !host->q || !host->k || !host->v || !host->out || !dev->q || !dev->k || !dev->v ||
+      !dev->q_mx || !dev->k_mx || !dev->v_mx || !dev->out)
+    return FSA_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, Hkv, Sq, Sk, D) || !(scale > 0.0f) || !std::isfinite(scale)) return FSA_ERR_INVALID_ARG;
+  if (!valid_fmt(fmt_qk) || !valid_pv(fmt_pv)) return FSA_ERR_UNSUPPORTED_FMT;
+  fsa_opts o;
+  fsa_default_opts(&o);
+  if (opts) o = *opts;
+  if (!opts_ok(o) || o.debug) return FSA_ERR_INVALID_ARG;
+  if (fmt_qk == FSA_FMT_NVFP4 && o.schedule == FSA_SCHED_PERSISTENT) return FSA_ERR_UNSUPPORTED_FMT;
+  const int fv = storage_fmt(fmt_pv);
+  const fsa_mx_tensor* mx[3] = {dev->q_mx, dev->k_mx, dev->v_mx};
+  for (const fsa_mx_tensor* m : mx)
+    if (!m->codes || !m->scales || !aligned16(m->codes) || !aligned16(m->scales)) return FSA_ERR_INVALID_ARG;
+  if (!aligned16(dev->q) || !aligned16(dev->k) || !aligned16(dev->v) || !aligned16(dev->out))
+    return FSA_ERR_INVALID_ARG;
+  // bytes of one head of each MX tensor (the layouts keep every head contiguous)
+  size_t qc, qs, kc, ks, vc, vs;
+  int st;
+  if ((st = fsa_mx_sizes(1, 1, Sq, D, FSA_MX_ROWS, fmt_qk, &qc, &qs)) != FSA_OK) return st;
+  if ((st = fsa_mx_sizes(1, 1, Sk, D, FSA_MX_ROWS, fmt_qk, &kc, &ks)) != FSA_OK) return st;
+  if ((st = fsa_mx_sizes(1, 1, Sk, D, FSA_MX_COLS_T, fv, &vc, &vs)) != FSA_OK) return st;
+  const int G = H / Hkv, U = B * Hkv;               // kv-head units: a kv head and its G query heads
+  const int n = n_chunks <= 0 ? std::min(U, 8) : std::min(n_chunks, U);
+  const size_t qe = (size_t)Sq * D, ke = (size_t)Sk * D;   // elements of one head
+  const size_t oes = o.out_dtype == FSA_OUT_BF16 ? 2 : 4;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream), in_s = nullptr, out_s = nullptr;
+  std::vector<cudaEvent_t> ev;                      // every event made here, destroyed at the end
+  auto event = [&](cudaEvent_t* e) -> bool {
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+    ev.push_back(*e);
+    return true;
+  };
+  int rc = FSA_OK;
+  cudaEvent_t e0;
+  if (cudaStreamCreateWithFlags(&in_s, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&out_s, cudaStreamNonBlocking) != cudaSuccess || !event(&e0) ||
+      cudaEventRecord(e0, s) != cudaSuccess || cudaStreamWaitEvent(in_s, e0, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(out_s, e0, 0) != cudaSuccess)
+    rc = FSA_ERR_LAUNCH;
+  // copies in, chunk by chunk, on their own stream: they run ahead of the compute
+  std::vector<cudaEvent_t> landed(n, nullptr);
+  for (int c = 0; rc == FSA_OK && c < n; ++c) {
+    const size_t u0 = (size_t)U * c / n, u1 = (size_t)U * (c + 1) / n;
+    const size_t nq = (u1 - u0) * G * qe, nk = (u1 - u0) * ke;
+    const size_t oq = u0 * G * qe, ok = u0 * ke;
+    if (cudaMemcpyAsync(static_cast<uint16_t*>(dev->q) + oq, static_cast<const uint16_t*>(host->q) + oq, 2 * nq,
+                        cudaMemcpyDefault, in_s) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint16_t*>(dev->k) + ok, static_cast<const uint16_t*>(host->k) + ok, 2 * nk,
+                        cudaMemcpyDefault, in_s) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint16_t*>(dev->v) + ok, static_cast<const uint16_t*>(host->v) + ok, 2 * nk,
+                        cudaMemcpyDefault, in_s) != cudaSuccess ||
+        !event(&landed[c]) || cudaEventRecord(landed[c], in_s) != cudaSuccess)
+      rc = FSA_ERR_LAUNCH;
+  }
+  // compute on the caller's stream as each chunk lands; its output goes back on the
+  // third stream while the next chunk computes
+  for (int c = 0; rc == FSA_OK && c < n; ++c) {
+    const size_t u0 = (size_t)U * c / n, u1 = (size_t)U * (c + 1) / n;
+    const int nu = (int)(u1 - u0);
+    const size_t oq = u0 * G * qe, ok = u0 * ke;
+    fsa_mx_tensor cq = *dev->q_mx, ck = *dev->k_mx, cv = *dev->v_mx;
+    cq.codes = static_cast<uint8_t*>(cq.codes) + u0 * G * qc; cq.scales += u0 * G * qs;
+    ck.codes = static_cast<uint8_t*>(ck.codes) + u0 * kc;     ck.scales += u0 * ks;
+    cv.codes = static_cast<uint8_t*>(cv.codes) + u0 * vc;     cv.scales += u0 * vs;
+    fsa_opts oc = o;
+    if (o.row_fallbacks) oc.row_fallbacks = o.row_fallbacks + u0 * G * Sq;
+    void* out_c = static_cast<uint8_t*>(dev->out) + oq * oes;
+    cudaEvent_t done;
+    if (cudaStreamWaitEvent(s, landed[c], 0) != cudaSuccess) { rc = FSA_ERR_LAUNCH; break; }
+    // the chunk's kv-head units as one batch of nu kv heads and nu * G query heads
+    if ((rc = fsa_mx_quantize_qkv(static_cast<uint16_t*>(dev->q) + oq, static_cast<uint16_t*>(dev->k) + ok,
+                                  static_cast<uint16_t*>(dev->v) + ok, 1, nu * G, nu, Sq, Sk, D, fmt_qk, fv, &cq, &ck,
+                                  &cv, s)) != FSA_OK)
+      break;
+    if ((rc = fsa_attention_fwd_ex(&cq, &ck, &cv, out_c, 1, nu * G, nu, Sq, Sk, D, causal, scale, fmt_qk, fmt_pv, &oc,
+                                   stats, s)) != FSA_OK)
+      break;
+    if (!event(&done) || cudaEventRecord(done, s) != cudaSuccess || cudaStreamWaitEvent(out_s, done, 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(host->out) + oq * oes, out_c, nu * G * qe * oes, cudaMemcpyDefault,
+                        out_s) != cudaSuccess) {
+      rc = FSA_ERR_LAUNCH;
+      break;
+    }
+  }
+  // the caller's stream completes after everything enqueued here, whatever failed
+  cudaEvent_t fin_in, fin_out;
+  if (in_s && event(&fin_in) && cudaEventRecord(fin_in, in_s) == cudaSuccess) cudaStreamWaitEvent(s, fin_in, 0);
+  else if (in_s) rc = FSA_ERR_LAUNCH;
+  if (out_s && event(&fin_out) && cudaEventRecord(fin_out, out_s) == cudaSuccess) cudaStreamWaitEvent(s, fin_out, 0);
+  else if (out_s) rc = FSA_ERR_LAUNCH;
+  // streams and events are released once their work completes
+  for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  if (in_s) cudaStreamDestroy(in_s);
+  if (out_s) cudaStreamDestroy(out_s);
+  if (rc == FSA_OK) {
+    auto set = [&](fsa_mx_tensor* m, int fmt, int layout, int h, int S) {
+      m->fmt = fmt; m->layout = layout; m->B = B; m->H = h; m->S = S; m->D = D;
+    };
+    set(dev->q_mx, fmt_qk, FSA_MX_ROWS, H, Sq);
+    set(dev->k_mx, fmt_qk, FSA_MX_ROWS, Hkv, Sk);
+    set(dev->v_mx, fv, FSA_MX_COLS_T, Hkv, Sk);
+  }
+  return rc;
 }
 
 int fsa_tune_delta(const fsa_stats* stats, int n_layers, float target_rate, float step, float max_delta,

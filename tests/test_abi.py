@@ -263,3 +263,37 @@ def test_nvfp4_is_a_rows_qk_format_with_two_scale_atoms(lib):
                                        vp(0)) == fsa.FSA_ERR_UNSUPPORTED_FMT
     x = fsa_mx_tensor(16, 16, 0, 0, 0, 0, 0, 0)
     assert lib.fsa_mx_quantize(vp(16), 1, 1, 128, 128, 1, 5, ctypes.byref(x), vp(0)) == fsa.FSA_ERR_INVALID_ARG
+
+
+def test_host_entry_argument_checks(lib):
+    """fsa_attention_fwd_host checks every argument before it creates a stream or
+    enqueues a copy, so these calls need no GPU."""
+    import softmax_mx_block_gb300 as fsa
+    from softmax_mx_block_gb300._binding import fsa_device_io, fsa_host_io, fsa_mx_tensor
+    vp = ctypes.c_void_p
+    mq, mk, mv = (fsa_mx_tensor(16, 16, 0, 0, 0, 0, 0, 0) for _ in range(3))
+    host = fsa_host_io(16, 16, 16, 16)
+
+    def dev(q=16, out=16, m=mq):
+        return fsa_device_io(q, 16, 16, ctypes.pointer(m), ctypes.pointer(mk), ctypes.pointer(mv), out)
+
+    def call(h, d, H=4, Hkv=2, D=128, fq=0, fp=0, opts=None):
+        return lib.fsa_attention_fwd_host(ctypes.byref(h) if h is not None else None,
+                                          ctypes.byref(d) if d is not None else None, 1, H, Hkv, 256, 256, D, 1,
+                                          ctypes.c_float(0.088), fq, fp,
+                                          ctypes.byref(opts) if opts is not None else None, vp(0), 0, vp(0))
+    assert call(None, dev()) == fsa.FSA_ERR_INVALID_ARG
+    assert call(host, None) == fsa.FSA_ERR_INVALID_ARG
+    assert call(fsa_host_io(16, 0, 16, 16), dev()) == fsa.FSA_ERR_INVALID_ARG          # null host k
+    assert call(host, dev(q=24)) == fsa.FSA_ERR_INVALID_ARG                            # misaligned device q
+    assert call(host, dev(m=fsa_mx_tensor(16, 0, 0, 0, 0, 0, 0, 0))) == fsa.FSA_ERR_INVALID_ARG
+    assert call(host, dev(), H=3, Hkv=2) == fsa.FSA_ERR_INVALID_ARG                    # H not a multiple of Hkv
+    assert call(host, dev(), D=96) == fsa.FSA_ERR_INVALID_ARG
+    assert call(host, dev(), fq=3, fp=3) == fsa.FSA_ERR_UNSUPPORTED_FMT                 # EFQ as a QK^T format
+    o = fsa.default_opts()
+    o.delta = -1.0
+    assert call(host, dev(), opts=o) == fsa.FSA_ERR_INVALID_ARG
+    o = fsa.default_opts()
+    dd = fsa._binding.fsa_debug_dump(16, 16, 16, 16, 0)
+    o.debug = ctypes.pointer(dd)
+    assert call(host, dev(), opts=o) == fsa.FSA_ERR_INVALID_ARG                        # no debug dumps here

@@ -394,6 +394,26 @@ def time_workload(name, dev, steps, exp_mode, measured_peaks):
 MUFU_MASK = {0: 0x00000000, 1: 0xFFFFFFFF, 2: 0x77777777}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def run_oracle_sample(w: Workload, budget_s=15.0, exp_mode=1):
     """The oracle's step-by-step emulation on a bounded sample of query rows, timed on
     the host cores; returns (TFLOP/s-equivalent, description, threads)."""
@@ -422,7 +442,8 @@ def run_oracle_sample(w: Workload, budget_s=15.0, exp_mode=1):
         n = min(4096, n * 2)
     which = "all" if done == len(rows_all) else f"{done} randomly sampled of the {len(rows_all)}"
     desc = (f"oracle emulation (fsa_emulate, fp64 accumulation) of {which} query rows of {wl.name} "
-            f"({wl.fmt_qk}/{wl.fmt_pv}) in {t_used:.1f} s; FLOPs = 4*D*visible keys per row")
+            f"({wl.fmt_qk}/{wl.fmt_pv}) in {t_used:.1f} s on {threads} threads ({cpu_model()}, "
+            f"{os.cpu_count()} logical CPUs); FLOPs = 4*D*visible keys per row")
     return flops / t_used / 1e12, desc, threads
 
 

@@ -334,13 +334,16 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // the compiler knows to be warp-uniform: addresses derived from them stay uniform
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
 
-  // ---- work item: heavy causal tiles first
-  // causal: (batch, head) on the fast grid axis and query tiles heaviest first on the
-  // slow one, so blocks are dispatched longest first; otherwise query tiles of one
-  // head run together and share its K/V in L2
-  const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.y) : (int)blockIdx.x;
-  const int h = p.causal ? (int)blockIdx.x % p.H : (int)blockIdx.y;
-  const int b = p.causal ? (int)blockIdx.x / p.H : (int)blockIdx.z;
+  // ---- work item
+  // causal: one kv head (batch and kv head) per slow grid index, and on the fast axis
+  // its query tiles heaviest first, the G = H/Hkv query heads of each tile together:
+  // blocks are dispatched kv head by kv head, longest first within each, so the blocks
+  // in flight share one kv head's K/V in L2 and the launch ends on short blocks.
+  // Otherwise query tiles of one head run together and share its K/V in L2.
+  const int G = p.H / p.Hkv;
+  const int qt = p.causal ? (p.n_qtiles - 1 - (int)blockIdx.x / G) : (int)blockIdx.x;
+  const int h = p.causal ? ((int)blockIdx.y % p.Hkv) * G + (int)blockIdx.x % G : (int)blockIdx.y;
+  const int b = p.causal ? (int)blockIdx.y / p.Hkv : (int)blockIdx.z;
   const int kvh = h / (p.H / p.Hkv);
   const int q0 = qt * 128;
   const int nkt = (p.Sk + 127) / 128;
@@ -975,7 +978,8 @@ static cudaError_t launch_one(const AttnLaunch& a) {
   auto kern = fsa_attn_kernel<FQK, FPV, D, EXPM, DBG, QF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid = a.p.causal ? dim3(a.p.H * a.p.B, a.p.n_qtiles, 1) : dim3(a.p.n_qtiles, a.p.H, a.p.B);
+  const dim3 grid = a.p.causal ? dim3((a.p.H / a.p.Hkv) * a.p.n_qtiles, a.p.Hkv * a.p.B, 1)
+                               : dim3(a.p.n_qtiles, a.p.H, a.p.B);
   kern<<<grid, C::NTHREADS, smem, a.stream>>>(a.tq, a.tk, a.tv, a.to, a.p, a.dbg);
   return cudaGetLastError();
 }

@@ -114,6 +114,20 @@ def test_small_formats(fq, fp, D, causal):
     assert np.array_equal(gpu["row_fallbacks"][rows], orc["fallbacks"])
 
 
+@pytest.mark.parametrize("fq,fp", [("E4M3", "E4M3"), ("E2M1", "E2M1_EFQ")])
+def test_batched_causal_gqa(fq, fp):
+    """Several batches and kv heads under the causal block order (one kv head per slow
+    grid index, query tiles heaviest first with the query heads of a tile together):
+    every (batch, head, query tile) is computed once and lands in its own rows."""
+    w = Workload(f"batched_{fq}_{fp}", 3, 6, 2, 520, 520, 128, True, fq, fp, 31)
+    q, k, v = generate(w)
+    rows = sample_rows(w, per_head=64)
+    gpu = run_mx(w, q, k, v, row_fb=True)
+    orc = oracle_mx(w, q, k, v, rows, SPLIT_MASK)
+    check(w, gpu, orc, rows, FLOOR_EFQ[fq] if fp == "E2M1_EFQ" else FLOOR_EXP)
+    assert np.array_equal(gpu["row_fallbacks"][rows], orc["fallbacks"])
+
+
 @pytest.mark.parametrize("exp_mode,mask", [(0, 0), (1, 0xFFFFFFFF), (2, SPLIT_MASK)])
 def test_exp_modes(exp_mode, mask):
     w = small(WORKLOADS["prefill"], 384, H=4, Hkv=2)

@@ -88,6 +88,11 @@ def test_full_size_sampled_rows(name, per_head):
     e_gpu, e_floor = rel_err(o, ex), rel_err(fl, ex)
     print(f"{name}: error {e_gpu:.5f}, floor {e_floor:.5f}, ratio {e_gpu / e_floor:.4f}")
     assert e_gpu <= ratio * e_floor, f"{name}: error {e_gpu:.4f} vs floor {e_floor:.4f}"
+    # the error condition itself is 1.1x the floor; the EFQ rule family's best reaches
+    # 1.04-1.11x depending on the rows, so where an EFQ case misses it the gap is
+    # reported as an expected failure rather than hidden by the regression bound above
+    if e_gpu > 1.1 * e_floor:
+        pytest.xfail(f"{name}: error {e_gpu / e_floor:.3f}x the operand-quantisation floor, above 1.1x")
 
 
 def test_bf16_full_size_sampled_rows():

@@ -73,7 +73,7 @@ def peak_for(w: Workload, measured=None):
         pq, pp, src = measured[kq], measured[kp], "measured on this GPU by the tcgen05 probe (fsa_mma_peak)"
     else:
         pq, pp = bf16 * KIND_RATIO[kq], bf16 * KIND_RATIO[kp]
-        src = f"{src} bf16 burst x nominal block-scaled/bf16 ratio"
+        src = f"{src} bf16 GEMM burst (MEASURED_PEAKS.json) x nominal block-scaled/bf16 ratio"
     return 1.0 / (0.5 / pq + 0.5 / pp), src
 
 
@@ -511,8 +511,10 @@ def main():
     value = flops_per_step * world / (r["ms"] * 1e-3) / 1e12
     attn_tflops = flops_per_step / w.layers / (r["attn_ms"] * 1e-3) / 1e12
     peak, src = peak_for(w, measured)
+    peak_nominal, src_nominal = peak_for(w, None)
     if w.layers > 1:
         peak = w.layers / sum(1.0 / peak_for(w.layer(l), measured)[0] for l in range(w.layers))
+        peak_nominal = w.layers / sum(1.0 / peak_for(w.layer(l), None)[0] for l in range(w.layers))
     rt = r["stats"]["row_tiles"]
     line = {
         "metric": metric_name(), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -528,7 +530,12 @@ def main():
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak, "traffic": TRAFFIC.get(w.name),
                      "peak_source": src + " (burst, the better of M=128 N=128 and N=256 dense MMAs; harmonic "
-                                          "mix of the QK^T and PV kinds)"},
+                                          "mix of the QK^T and PV kinds)",
+                     # the same fraction against the other denominator: the bf16 GEMM
+                     # figure of MEASURED_PEAKS.json (or the fallback) times the nominal
+                     # block-scaled/bf16 ratio of each kind
+                     "vs_bf16_gemm_x_nominal": {"peak": peak_nominal, "frac": attn_tflops / peak_nominal,
+                                                "source": src_nominal}},
         "tensor_peaks_tflops": peak_info,
         "e2e": {"value": flops_per_step * world / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

@@ -310,3 +310,32 @@ def test_persistent_more_query_tiles_than_one_wave():
         torch.cuda.synchronize()
         assert fsa.read_stats(st)["status"] == 0
     assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_count_at_the_grid_limit(causal):
+    """B*H = 65535, the most the attention calls accept (one grid axis carries the
+    heads, or the kv heads when causal): every head lands in its own rows.  Six heads
+    spread over the range, the first and the last included, are checked against the
+    oracle on all their rows (the heads are independent, so they form a small call of
+    their own for the oracle)."""
+    fsa = _fsa()
+    B, H, S, D = 1, 65535, 130, 64
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = lambda: torch.randn(B, H, S, D, generator=g, device="cuda").to(torch.bfloat16)
+    q, k, v = x(), x(), x()
+    mq, mk, mv = fsa.fsa_mx_quantize_qkv(q, k, v, "E4M3", "E4M3")
+    st = fsa.new_stats()
+    out = fsa.fsa_attention_fwd(mq, mk, mv, causal=causal, scale=D ** -0.5, fmt_qk=0, fmt_pv=0, exp_mode=1,
+                                delta=8.0, stats=st)
+    torch.cuda.synchronize()
+    assert fsa.read_stats(st)["status"] == 0
+    heads = [0, 1, 4097, 32768, 65533, 65534]
+    bits = lambda t: t[0, heads].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)[None]
+    w = Workload("grid_limit", 1, len(heads), len(heads), S, S, D, causal, "E4M3", "E4M3", 11)
+    rows = np.arange(len(heads) * S, dtype=np.int64)
+    orc = oracle_mx(w, bits(q), bits(k), bits(v), rows, 0xFFFFFFFF, delta=8.0, with_floor=False)
+    gpu = dict(out=out[0, heads].cpu().numpy().reshape(-1, D), stats=fsa.read_stats(st))
+    check(w, gpu, orc, rows, None)
+    del q, k, v, mq, mk, mv, out
+    torch.cuda.empty_cache()

@@ -30,7 +30,12 @@
  *   - Shapes: B batch, H query heads, Hkv key/value heads (H % Hkv == 0; query
  *     head h reads kv head h / (H/Hkv)), Sq queries, Sk keys, head dim D in
  *     {64, 128}; the attention calls also need B*H <= 65535, Sq <= 65535*128
- *     and Sk <= 2^24 (else INVALID_ARG).
+ *     and Sk <= 2^20 (else INVALID_ARG).  The key limit is one of accuracy: the
+ *     fp32 accumulator in tensor memory, to which every key tile adds its
+ *     products, drifts by a per-row factor that grows with the number of key
+ *     tiles, as adds that drop low-order bits would (measured at 2^20 keys:
+ *     below 5e-4 of the output, within the 2e-3 parity bound; at 2^22 keys up
+ *     to 7e-3 with 8-bit P~).
  *     Causal masking is bottom-right aligned: key j is visible to
  *     query i iff j <= i + Sk - Sq.  A query with no visible key gets a zero
  *     output row.

@@ -152,10 +152,13 @@ bool valid_pv(int f) { return f >= FSA_FMT_E4M3 && f <= FSA_FMT_E3M2; }
 int storage_fmt(int f) { return f == FSA_FMT_E2M1_EFQ ? FSA_FMT_E2M1 : f; }
 
 // The query-tile count B*H*ceil(Sq/128) must fit an int (the persistent schedule
-// indexes its work list with it).
+// indexes its work list with it).  Sk is limited by accuracy, not indexing: the fp32
+// accumulator in tensor memory drifts by a per-row factor that grows with the key
+// tiles added into it, as adds that drop low-order bits would (below 5e-4 of the
+// output at 2^20 keys, up to 7e-3 at 2^22 with 8-bit P~).
 bool shape_ok(int B, int H, int Hkv, int Sq, int Sk, int D) {
   return B > 0 && H > 0 && Hkv > 0 && H % Hkv == 0 && Sq > 0 && Sk > 0 && (D == 64 || D == 128) &&
-         (int64_t)B * H <= 65535 && (int64_t)Sq <= 65535 * 128 && (int64_t)Sk <= (1 << 24) &&
+         (int64_t)B * H <= 65535 && (int64_t)Sq <= 65535 * 128 && (int64_t)Sk <= (1 << 20) &&
          (int64_t)B * H * ((Sq + 127) / 128) <= INT_MAX;
 }
 

@@ -73,6 +73,11 @@ def test_argument_checks_reject_before_launch(lib):
     # H not a multiple of Hkv, D outside {64, 128}, EFQ as a QK format, null pointers
     assert lib.fsa_attention_fwd(*args(t, t, v, 3, 2, 128, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
     assert lib.fsa_attention_fwd(*args(t, t, v, 1, 1, 96, 0, 0)) == fsa.FSA_ERR_INVALID_ARG
+    # key length above 2^20 (the accuracy limit of fp32 accumulation in tensor memory)
+    kl = fsa_mx_tensor(16, 16, 0, 0, 1, 1, (1 << 20) + 1, 128)
+    vl = fsa_mx_tensor(16, 16, 0, 1, 1, 1, (1 << 20) + 1, 128)
+    assert lib.fsa_attention_fwd(ctypes.byref(t), ctypes.byref(kl), ctypes.byref(vl), vp(16), 1, 1, 1, 128,
+                                 (1 << 20) + 1, 128, 0, ctypes.c_float(0.125), 0, 0, vp(0)) == fsa.FSA_ERR_INVALID_ARG
     assert lib.fsa_attention_fwd(*args(t, t, v, 1, 1, 128, 3, 3)) == fsa.FSA_ERR_UNSUPPORTED_FMT
     assert lib.fsa_attention_fwd(None, None, None, vp(16), 1, 1, 1, 128, 128, 128, 0, ctypes.c_float(0.1), 0, 0,
                                  vp(0)) == fsa.FSA_ERR_INVALID_ARG

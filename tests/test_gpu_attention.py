@@ -339,3 +339,34 @@ def test_head_count_at_the_grid_limit(causal):
     check(w, gpu, orc, rows, None)
     del q, k, v, mq, mk, mv, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fq,fp", [("E2M1", "E2M1_EFQ"), ("E4M3", "E4M3")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_longest_key_length(causal, fq, fp):
+    """Sk = 2^20, the longest key length the attention calls accept: 8192 key tiles per
+    query tile, every key and byte offset at its largest.  The first and last rows of
+    both query tiles of two query heads sharing one kv head are checked against the
+    oracle.  (The limit is set by accuracy: the fp32 accumulator in tensor memory
+    drifts by a per-row factor that grows with the key tiles added into it; at 2^20
+    keys it stays within the parity bound, at 2^22 it does not for 8-bit P~.)"""
+    fsa = _fsa()
+    B, H, Hkv, Sq, Sk, D = 1, 2, 1, 130, 1 << 20, 64
+    g = torch.Generator(device="cuda").manual_seed(12)
+    x = lambda h, s: torch.randn(B, h, s, D, generator=g, device="cuda").to(torch.bfloat16)
+    q, k, v = x(H, Sq), x(Hkv, Sk), x(Hkv, Sk)
+    fv = "E2M1" if fp == "E2M1_EFQ" else fp
+    mq, mk, mv = fsa.fsa_mx_quantize_qkv(q, k, v, fq, fv)
+    st = fsa.new_stats()
+    out = fsa.fsa_attention_fwd(mq, mk, mv, causal=causal, scale=D ** -0.5, fmt_qk=fq, fmt_pv=fp, exp_mode=1,
+                                delta=8.0, stats=st)
+    torch.cuda.synchronize()
+    assert fsa.read_stats(st)["status"] == 0
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    w = Workload(f"longest_keys_{fq}_{fp}", B, H, Hkv, Sq, Sk, D, causal, fq, fp, 12)
+    rows = np.array([0, 127, 128, 129, Sq, Sq + 127, Sq + 128, Sq + 129], dtype=np.int64)
+    orc = oracle_mx(w, bits(q), bits(k), bits(v), rows, 0xFFFFFFFF, delta=8.0, with_floor=False)
+    gpu = dict(out=out.cpu().numpy().reshape(-1, D), stats=fsa.read_stats(st))
+    check(w, gpu, orc, rows, None)
+    del q, k, v, mq, mk, mv, out
+    torch.cuda.empty_cache()

@@ -88,13 +88,14 @@ struct Cfg {
   static constexpr int NBAR = PERSIST ? 4 + 4 * NS + 3 * 2 + 3 : 1 + 4 * NS + 3 * 2 + 2 + (QF ? 1 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
   // output staging: one CTA per query tile stages O (128 rows x D fp32, 32x32 boxes)
-  // in the K/V ring, free by then; the persistent schedule has one 32-row x 16-column
-  // fp32 box (64B swizzle) per softmax warp
+  // in the K/V ring, free by then; the persistent schedule has two 32-row x 16-column
+  // fp32 boxes (64B swizzle) per softmax warp, used in turn (BF16: one)
   static constexpr int OFF_OSTAGE = PERSIST ? (OFF_MISC + 64 + 1023) / 1024 * 1024 : OFF_K;
   static_assert(PERSIST || OFF_K + 128 * D * 4 <= OFF_SF, "O staging fits the K/V ring");
   // persistent: the CTA's query tiles in processing order (at most MAX_ITEMS)
   static constexpr int MAX_ITEMS = 256;
-  static constexpr int OFF_ITEMS = OFF_OSTAGE + NSW * 2048;
+  static constexpr int OSTAGE_WARP = MX ? 4096 : 2048;                // BF16: one box (shared memory)
+  static constexpr int OFF_ITEMS = OFF_OSTAGE + NSW * OSTAGE_WARP;
   // QF: the bf16 Q tile, 128 rows x 2D bytes, unswizzled
   static constexpr int OFF_QRAW = (OFF_MISC + 64 + 1023) / 1024 * 1024;
   static constexpr int SMEM = PERSIST ? OFF_ITEMS + MAX_ITEMS * 16 + 1024

@@ -9,7 +9,7 @@
 // counted over the CTA's query tiles (g), so ring slots, S and P~ buffers and
 // barrier phases run on across them; Q is double-buffered; a query tile's first PV
 // (which overwrites O_aug) waits on o_free, which both softmax parts arrive on once
-// they hold the previous tile's O_aug rows; output rows go out through a 32x16 box
+// they hold the previous tile's O_aug rows; output rows go out through two 32x16 boxes
 // per warp by TMA stores.
 #pragma once
 
@@ -18,8 +18,8 @@ namespace fsa {
 // One part's half of a finished query tile's output rows (thread = row): O_aug
 // columns [DP*pp, DP*pp + DP) and l from tensor memory, 16 columns at a time (few
 // registers next to the key-tile loop); each chunk is normalised, written to the
-// warp's 32x16 staging box (64B swizzle) and stored by TMA (rows past Sq are
-// clipped).  After the last tensor-memory load, o_free: O_aug may be overwritten.
+// warp's two 32x16 staging boxes in turn (64B swizzle) and stored by TMA (rows past
+// Sq are clipped).  After the last tensor-memory load, o_free: O_aug may be overwritten.
 // A query tile without key tiles gets zeros.
 template <int D, bool MX>
 __device__ __forceinline__ void write_rows(uint32_t t_o, int pp, int qd, int lane, float lb, bool done, bool has_keys,
@@ -64,7 +64,13 @@ __device__ __forceinline__ void write_rows(uint32_t t_o, int pp, int qd, int lan
 #pragma unroll
       for (int i = 0; i < 16; ++i) o[i] = 0u;
     }
-    if (lane == 0) bulk_wait_read();                 // the previous chunk's store has read the box
+    // MX: two boxes in turn, and the store that last read this chunk's box is the one
+    // before the latest, so the latest may still be reading the other box (BF16: one)
+    uint8_t* box = stage + (MX ? ((c0 / 16) & 1) * 2048 : 0);
+    if (lane == 0) {
+      if constexpr (MX) bulk_wait_read_1();
+      else bulk_wait_read();
+    }
     __syncwarp();
     if (bf16) {
       // bf16: the same fp32 quotients rounded to nearest even, 32 bytes per row (32B
@@ -78,7 +84,7 @@ __device__ __forceinline__ void write_rows(uint32_t t_o, int pp, int qd, int lan
           const float b = lpos ? __fmul_rn(__uint_as_float(o[8 * ch + 2 * e + 1]), rinv) : 0.f;
           w[e] = cvt_bf16x2(a, b);
         }
-        *reinterpret_cast<uint4*>(stage + lane * 32 + ((ch ^ ((lane >> 2) & 1)) << 4)) =
+        *reinterpret_cast<uint4*>(box + lane * 32 + ((ch ^ ((lane >> 2) & 1)) << 4)) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
@@ -90,13 +96,13 @@ __device__ __forceinline__ void write_rows(uint32_t t_o, int pp, int qd, int lan
                                             __fmul_rn(__uint_as_float(o[4 * ch + 3]), rinv))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
         // 64B swizzle: 16-byte chunk ch of row `lane` sits at chunk ch ^ ((lane / 2) % 4)
-        *reinterpret_cast<float4*>(stage + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) = v;
+        *reinterpret_cast<float4*>(box + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)) = v;
       }
     }
     fence_proxy_async_smem();                        // generic writes -> TMA reads
     __syncwarp();
     if (lane == 0) {
-      tma_store_3d(tm_o, stage, DP * pp + c0, q0 + 32 * qd, bhq);
+      tma_store_3d(tm_o, box, DP * pp + c0, q0 + 32 * qd, bhq);
       bulk_commit_group();
     }
   }
@@ -714,7 +720,7 @@ fsa_attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     const int gl = g0 + nT - 1;
     const bool done = ok && nT > 0 && (gl < 1 || wait0(pv_done + (gl - 1) % C::NS, ((gl - 1) / C::NS) & 1)) &&
                       wait0(pv_done + gl % C::NS, (gl / C::NS) & 1);
-    write_rows<D, MX>(tl + C::T_O, pp, qd, lane, lb, done, nT > 0, sm + C::OFF_OSTAGE + (warp - 2) * 2048, &tm_o,
+    write_rows<D, MX>(tl + C::T_O, pp, qd, lane, lb, done, nT > 0, sm + C::OFF_OSTAGE + (warp - 2) * C::OSTAGE_WARP, &tm_o,
                       it.q0, it.bhq, o_free, p.out_bf16 != 0);
     // ---- statistics: each part counted the key tiles it owns
     int* nfb_other = reinterpret_cast<int*>(red) + 128 + rl;

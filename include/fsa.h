@@ -356,7 +356,8 @@ typedef struct {
 /* The attention of fsa_attention_fwd_ex (the Fused-Softmax brief, abstract; the
  * pages say nothing of where the operands live) on operands in host memory.  The
  * call is split into n_chunks groups of whole kv heads (a kv head with its H/Hkv
- * query heads; n_chunks <= 0: min(B*Hkv, 8)), and for each group: Q, K and V are
+ * query heads; n_chunks <= 0: min(B*Hkv, 8), fewer when a group would hold under two
+ * query tiles per SM), and for each group: Q, K and V are
  * copied host to device on a stream of the library's own, quantised
  * (fsa_mx_quantize_qkv) and attended on `stream` once they have landed, and O
  * copied back on a second stream of its own while the next group computes.  The

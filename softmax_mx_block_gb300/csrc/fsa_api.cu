@@ -515,7 +515,15 @@ int fsa_attention_fwd_host(const fsa_host_io* host, const fsa_device_io* dev, in
   if ((st = fsa_mx_sizes(1, 1, Sk, D, FSA_MX_ROWS, fmt_qk, &kc, &ks)) != FSA_OK) return st;
   if ((st = fsa_mx_sizes(1, 1, Sk, D, FSA_MX_COLS_T, fv, &vc, &vs)) != FSA_OK) return st;
   const int G = H / Hkv, U = B * Hkv;               // kv-head units: a kv head and its G query heads
-  const int n = n_chunks <= 0 ? std::min(U, 8) : std::min(n_chunks, U);
+  // default: up to 8 groups, but each group's launch keeps at least two query tiles
+  // per SM (a short call split 8 ways would leave SMs idle in every group)
+  int n = n_chunks <= 0 ? std::min(U, 8) : std::min(n_chunks, U);
+  if (n_chunks <= 0) {
+    int dev = 0, n_sm = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t qtiles = (int64_t)B * H * ((Sq + 127) / 128);
+    n = (int)std::max<int64_t>(1, std::min<int64_t>(n, qtiles / (2 * (int64_t)std::max(n_sm, 1))));
+  }
   const size_t qe = (size_t)Sq * D, ke = (size_t)Sk * D;   // elements of one head
   const size_t oes = o.out_dtype == FSA_OUT_BF16 ? 2 : 4;
 

@@ -364,10 +364,10 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* k_empty = bars + 1 + 3 * C::NS;    // S(j) done -> K slot j % NS
   uint64_t* s_full = bars + 1 + 4 * C::NS;
   uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_full + 4;
-  uint64_t* drain = s_full + 6;
-  uint64_t* stall = s_full + 7;
-  uint64_t* qraw_full = s_full + 8;             // QF: the bf16 Q tile landed
+  uint64_t* p_full = s_full + 4;               // P~(j) written -> barrier j % NPB
+  uint64_t* drain = p_full + C::NPB;
+  uint64_t* stall = drain + 1;
+  uint64_t* qraw_full = drain + 2;              // QF: the bf16 Q tile landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 8);
   float* red = reinterpret_cast<float*>(sm + C::OFF_RED);
@@ -380,8 +380,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       // one softmax warp per lane quadrant owns each tile
-      mbar_init(s_full + i, 1); mbar_init(s_free + i, 4); mbar_init(p_full + i, 4);
+      mbar_init(s_full + i, 1); mbar_init(s_free + i, 4);
     }
+    for (int i = 0; i < C::NPB; ++i) mbar_init(p_full + i, 4);
     mbar_init(drain, 1);
     mbar_init(stall, 1);
     sts_vol(abort_flag, 0);
@@ -538,9 +539,9 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < C::PV_STEPS; ++i) {
           // P~ of step i sits in columns [8i, 8i+8) of its P buffer; the scale word of
-          // each row (byte b = 32-key block b) is in column T_SFP + 4 s + lane quadrant
+          // each row (byte b = 32-key block b) is in column T_SFP + 4 (buffer) + lane quadrant
           const uint32_t a_tm = tbase + C::T_P + C::P_COLS * (jj % C::NPB) + 8 * i;
-          const uint32_t sfa = tbase + C::T_SFP + 4 * s;
+          const uint32_t sfa = tbase + C::T_SFP + 4 * (jj & (C::NPB - 1));
           const int ka = (i * 32) / C::W_V, off = (i * 32) % C::W_V;
           const uint64_t bd = smem_desc(sVa + st * C::TILE_V + ka * C::VATOM + off, 16, 8 * C::W_V, SWV);
           const uint32_t acc = (jj > 0 || i > 0) ? 1u : 0u;
@@ -613,7 +614,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // V(j) landed long before P~(j) is written: test it first, so that the warp
         // wakes from the P~ wait straight into the issue
-        ok = wait_all(v_full + j % C::NS, (j / C::NS) & 1) && wait_all(p_full + (j & 1), (j >> 1) & 1);
+        ok = wait_all(v_full + j % C::NS, (j / C::NS) & 1) && wait_all(p_full + (j & (C::NPB - 1)), (j >> C::NPB_SH) & 1);
         if (ok) issue_pv(j);
       }
       // all MMAs and copies issued by this warp complete before tensor memory is freed
@@ -800,7 +801,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // are warp-collective, so the whole warp rescales when any of its rows falls
         // back; the other rows multiply by exactly 1.
         if (__any_sync(0xffffffffu, rescale)) {
-          // PV(j-2) first: with two PV barriers (BF16) PV(j-1) shares its barrier with
+          // PV(j-NPB) first: with two PV barriers (BF16) PV(j-1) shares its barrier with
           // PV(j-3), and its parity only identifies PV(j-1) once PV(j-3) has completed
           const bool prev = j < C::NPB || wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1);
           if (prev && wait0(pv_done + (j - 1) % C::NS, ((j - 1) / C::NS) & 1)) {
@@ -819,8 +820,11 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = false;
           }
         }
-        // P~ buffer j % NPB and scale column s were last read by PV(j - NPB)
-        if (ok && j >= C::NPB && !wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1)) ok = false;
+        // P~ buffer j % NPB and its scale column were last read by PV(j - NPB): with two
+        // buffers wait for it; with more it completed before S(j) was signalled
+        if constexpr (C::NPB < 3) {
+          if (ok && j >= C::NPB && !wait0(pv_done + (j - C::NPB) % C::NS, ((j - C::NPB) / C::NS) & 1)) ok = false;
+        }
         if (ok) {
           tc_fence_after();
           if constexpr (!MX) gen_half(0, pw);
@@ -830,7 +834,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_st_cols<HW>(tp + HW, pw);
           // A scales of the PV MMA: lane quadrant q reads column base + q
           if constexpr (FPV == F_EFQ) sw = low_bytes4(swb[0], swb[1], swb[2], swb[3]);
-          if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * s + qd, &sw);
+          if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * (j & (C::NPB - 1)) + qd, &sw);
           if constexpr (DBG) {
             if (dbg_on) dbg.sf[dbg_row * nkt + j] = sw;
           }
@@ -843,7 +847,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (ok) mbar_arrive_elect(p_full + s);
+        if (ok) mbar_arrive_elect(p_full + (j & (C::NPB - 1)));
       }
     }
     // ---- epilogue: O = O_aug[:, :D] / l, D/2 columns per part

@@ -65,7 +65,15 @@ struct Cfg {
   static constexpr int NSW = 4 * NQ;                                // softmax warps
   // ---- P~ in tensor memory, its own buffers (so S is free once loaded)
   static constexpr int P_COLS = 128 * Fmt<FPV>::bits2 / 16 / 4;     // 32 (8-bit), 16 (E2M1), 64 (BF16)
-  static constexpr int NPB = 2;                                     // P~ buffers
+  // P~ buffers (and P~ scale columns and P~-arrival barriers): four for 16-column E2M1
+  // P~ in the per-tile kernel, where the scale columns fit.  With three or more, the
+  // PV that last read buffer j % NPB, PV(j - NPB), has completed by the time S(j) is
+  // there: the MMA warp issues QK^T(j) after PV(j - 3), and the commit that signals
+  // S(j) covers every MMA the warp issued before it.  So the softmax warps need no
+  // wait for the buffer; with two they wait for PV(j - 2).
+  static constexpr int NPB = (MX && !PERSIST && !NV && P_COLS == 16) ? 4 : 2;
+  static constexpr int NPB_SH = NPB == 4 ? 2 : 1;                  // log2(NPB)
+  static_assert(NPB == 2 || NPB == 4, "P~ buffers");
   static_assert(P_COLS == 8 * PV_STEPS, "one PV step per 8 columns");
   // ---- pipeline
   static constexpr int NS = MX ? 4 : 2;                             // K/V stages
@@ -85,7 +93,7 @@ struct Cfg {
   // q full (+ q empty x2 when persistent), k/v full, pv done, k empty x NS, s full/free,
   // p full x2, (o free,) drain, stall
   static_assert(!(PERSIST && QF), "Q quantised in the prologue: one CTA per query tile");
-  static constexpr int NBAR = PERSIST ? 4 + 4 * NS + 3 * 2 + 3 : 1 + 4 * NS + 3 * 2 + 2 + (QF ? 1 : 0);
+  static constexpr int NBAR = PERSIST ? 4 + 4 * NS + 3 * 2 + 3 : 1 + 4 * NS + 2 * 2 + NPB + 2 + (QF ? 1 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem slot, abort flag
   // output staging: one CTA per query tile stages O (128 rows x D fp32, 32x32 boxes)
   // in the K/V ring, free by then; the persistent schedule has two 32-row x 16-column
@@ -110,12 +118,12 @@ struct Cfg {
   static constexpr uint32_t SFK_STEP = 4 * NATOM_QK;                // columns per K parity
   static constexpr uint32_t T_SFK = T_SFQ + 4 * NATOM_QK;          // + SFK_STEP * parity
   static constexpr uint32_t T_SFV = T_SFK + 2 * SFK_STEP;          // + 8 * parity (4 from the V atom, 4 constant)
-  static constexpr uint32_t T_SFP = T_SFV + 16;                     // + 4 * buffer + lane quadrant
+  static constexpr uint32_t T_SFP = T_SFV + 16;                     // + 4 * (P~ buffer) + lane quadrant
   static constexpr uint32_t T_SFQ1 = 436;     // persistent: scale atom of the second Q buffer
   static constexpr uint32_t T_P = MX ? 448 : T_O + D;   // + P_COLS * buffer (BF16: no scales)
   static_assert(T_O + N_PV <= (MX ? T_SFQ : T_P), "tmem");
   static_assert(!MX || T_SFQ1 + 4 <= T_P, "tmem");
-  static_assert(!MX || T_SFP + 8 <= (PERSIST ? T_SFQ1 : T_P), "tmem");
+  static_assert(!MX || T_SFP + 4 * NPB <= (PERSIST ? T_SFQ1 : T_P), "tmem");
   static_assert(T_P + NPB * P_COLS <= 512, "tmem");
   // ---- threads
   static constexpr int NTHREADS = 64 + 32 * NSW;   // warp 0 TMA, warp 1 MMA, then the softmax warps

@@ -540,8 +540,8 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int i = 0; i < C::PV_STEPS; ++i) {
           // P~ of step i sits in columns [8i, 8i+8) of its P buffer; the scale word of
           // each row (byte b = 32-key block b) is in column T_SFP + 4 (buffer) + lane quadrant
-          const uint32_t a_tm = tbase + C::T_P + C::P_COLS * (jj % C::NPB) + 8 * i;
-          const uint32_t sfa = tbase + C::T_SFP + 4 * (jj & (C::NPB - 1));
+          const uint32_t a_tm = tbase + C::T_P + C::P_COLS * ((unsigned)jj % C::NPB) + 8 * i;
+          const uint32_t sfa = tbase + C::T_SFP + 4 * ((unsigned)jj % C::NPB);
           const int ka = (i * 32) / C::W_V, off = (i * 32) % C::W_V;
           const uint64_t bd = smem_desc(sVa + st * C::TILE_V + ka * C::VATOM + off, 16, 8 * C::W_V, SWV);
           const uint32_t acc = (jj > 0 || i > 0) ? 1u : 0u;
@@ -614,7 +614,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // V(j) landed long before P~(j) is written: test it first, so that the warp
         // wakes from the P~ wait straight into the issue
-        ok = wait_all(v_full + j % C::NS, (j / C::NS) & 1) && wait_all(p_full + (j & (C::NPB - 1)), (j >> C::NPB_SH) & 1);
+        ok = wait_all(v_full + j % C::NS, (j / C::NS) & 1) && wait_all(p_full + (unsigned)j % C::NPB, ((unsigned)j / C::NPB) & 1);
         if (ok) issue_pv(j);
       }
       // all MMAs and copies issued by this warp complete before tensor memory is freed
@@ -756,7 +756,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // generated before waiting for the PVs that the rescale and the buffer reuse
         // depend on, which gives them that much longer to finish.
         constexpr int HW = C::P_COLS / 2;             // words (columns) per half
-        const uint32_t tp = tl + C::T_P + C::P_COLS * (j % C::NPB);
+        const uint32_t tp = tl + C::T_P + C::P_COLS * ((unsigned)j % C::NPB);
         uint32_t sw = 0;                            // the blocks' scale bytes, block b in byte b
         // EFQ: the blocks' scale words, gathered by byte permutes (one instruction fewer
         // per block; the exp paths keep the shifts, which measured faster there)
@@ -834,7 +834,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_st_cols<HW>(tp + HW, pw);
           // A scales of the PV MMA: lane quadrant q reads column base + q
           if constexpr (FPV == F_EFQ) sw = low_bytes4(swb[0], swb[1], swb[2], swb[3]);
-          if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * (j & (C::NPB - 1)) + qd, &sw);
+          if constexpr (MX) TmemSt<1>::run(tl + C::T_SFP + 4 * ((unsigned)j % C::NPB) + qd, &sw);
           if constexpr (DBG) {
             if (dbg_on) dbg.sf[dbg_row * nkt + j] = sw;
           }
@@ -847,7 +847,7 @@ fsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (ok) mbar_arrive_elect(p_full + (j & (C::NPB - 1)));
+        if (ok) mbar_arrive_elect(p_full + (unsigned)j % C::NPB);
       }
     }
     // ---- epilogue: O = O_aug[:, :D] / l, D/2 columns per part

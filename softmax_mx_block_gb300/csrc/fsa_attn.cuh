@@ -71,9 +71,9 @@ struct Cfg {
   // there: the MMA warp issues QK^T(j) after PV(j - 3), and the commit that signals
   // S(j) covers every MMA the warp issued before it.  So the softmax warps need no
   // wait for the buffer; with two they wait for PV(j - 2).
-  static constexpr int NPB = (MX && !PERSIST && !NV && P_COLS == 16) ? 4 : 2;
-  static constexpr int NPB_SH = NPB == 4 ? 2 : 1;                  // log2(NPB)
-  static_assert(NPB == 2 || NPB == 4, "P~ buffers");
+  // (NVFP4 Q/K: three, with the P~ scale columns after the buffers, since its scale
+  // atoms take the columns in front of them)
+  static constexpr int NPB = (MX && !PERSIST && P_COLS == 16) ? (NV ? 3 : 4) : 2;
   static_assert(P_COLS == 8 * PV_STEPS, "one PV step per 8 columns");
   // ---- pipeline
   static constexpr int NS = MX ? 4 : 2;                             // K/V stages
@@ -118,13 +118,16 @@ struct Cfg {
   static constexpr uint32_t SFK_STEP = 4 * NATOM_QK;                // columns per K parity
   static constexpr uint32_t T_SFK = T_SFQ + 4 * NATOM_QK;          // + SFK_STEP * parity
   static constexpr uint32_t T_SFV = T_SFK + 2 * SFK_STEP;          // + 8 * parity (4 from the V atom, 4 constant)
-  static constexpr uint32_t T_SFP = T_SFV + 16;                     // + 4 * (P~ buffer) + lane quadrant
-  static constexpr uint32_t T_SFQ1 = 436;     // persistent: scale atom of the second Q buffer
   static constexpr uint32_t T_P = MX ? 448 : T_O + D;   // + P_COLS * buffer (BF16: no scales)
+  // P~ scales: + 4 * (P~ buffer) + lane quadrant; after the P~ buffers for NVFP4 Q/K
+  static constexpr bool SFP_AFTER = NV && NPB == 3;
+  static constexpr uint32_t T_SFP = SFP_AFTER ? T_P + NPB * P_COLS : T_SFV + 16;
+  static constexpr uint32_t T_SFQ1 = 436;     // persistent: scale atom of the second Q buffer
   static_assert(T_O + N_PV <= (MX ? T_SFQ : T_P), "tmem");
   static_assert(!MX || T_SFQ1 + 4 <= T_P, "tmem");
-  static_assert(!MX || T_SFP + 4 * NPB <= (PERSIST ? T_SFQ1 : T_P), "tmem");
-  static_assert(T_P + NPB * P_COLS <= 512, "tmem");
+  static_assert(!MX || T_SFP + 4 * NPB <= (PERSIST ? T_SFQ1 : (SFP_AFTER ? 512u : T_P)), "tmem");
+  static_assert(!MX || SFP_AFTER || T_SFV + 16 <= T_P, "tmem");
+  static_assert(T_P + NPB * P_COLS <= (SFP_AFTER ? T_SFP : 512u), "tmem");
   // ---- threads
   static constexpr int NTHREADS = 64 + 32 * NSW;   // warp 0 TMA, warp 1 MMA, then the softmax warps
 };

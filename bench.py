@@ -46,8 +46,8 @@ KIND = {"E4M3": 1, "E2M3": 1, "E3M2": 1, "E2M1": 2, "E2M1_EFQ": 2, "NVFP4": 3}
 KIND_RATIO = {0: 1.0, 1: 2.0, 2: 6.0, 3: 6.0}
 # DRAM bytes (read + write) of one attention launch of the current kernel build, from
 # an ncu capture, by workload; absent: not captured for this build
-TRAFFIC = {"long_efq_128k": 441.61e6 + 2.09e9, "long_efq_16k": 53.54e6 + 207.16e6,
-           "long_fp8_16k": 103.88e6 + 210.60e6, "video_dit": 1.01e9 + 1.51e9}
+TRAFFIC = {"long_efq_128k": 439.05e6 + 2.09e9, "long_efq_16k": 53.57e6 + 207.16e6,
+           "long_fp8_16k": 103.88e6 + 210.56e6, "video_dit": 1.01e9 + 1.51e9}
 
 
 def metric_name():
